@@ -1,0 +1,377 @@
+"""CPU oracle of the fused MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s cpu_baseline /
+reference arm may import or run anything in this package. The product path
+(the CUDA library and its binding) never imports it, and this module imports
+nothing from the product.
+
+What it computes, and where the pages define it
+-----------------------------------------------
+The layer is the pipeline ``[Router] -> [Quantize-Dispatch] ->
+[Permute-Experts-Unpermute] -> [Combine]`` (modular_kernel.py, module header
+comment). Each step below is written plainly in numpy, in float64 unless a
+page fixes the precision:
+
+* route_softmax_topk / route_sigmoid_grouped -- the [Router] step. The pages
+  name it and pass its outputs (``topk_ids``, ``topk_weights``;
+  modular_kernel.py ``FusedMoEModularKernel.forward``) but never give its
+  math; the readings used here (softmax -> top-k -> renormalise, and sigmoid
+  + bias -> grouped top-k -> renormalise x scale) are listed in the design doc.
+  Where floating point decides an integer (the sigmoid router's selection),
+  the decision is taken in float32 with the written ``sigmoid_f32_spec``,
+  the same spec the CUDA router implements independently.
+* permute -- groups routes by local expert; ``expanded_idx_to_permuted_idx``
+  with -1 for a non-local expert (moe_output.py ``UnfinalizedMoEOutput``,
+  field comments; ``expert_map`` in modular_kernel.py
+  ``FusedMoEPrepareAndFinalize.prepare``).
+* expert_mlp / experts -- GEMM1, ``silu_and_mul``, GEMM2; unweighted and
+  unreduced (modular_kernel.py header comment on
+  ``FusedMoEPermuteExpertsUnpermute`` and its ``activation`` method).
+* finalize -- applies the routing weights and reduces over top_k
+  (modular_kernel.py ``FusedMoEPrepareAndFinalize.finalize``), then the
+  routed scale and the shared-expert add (moe_output.py ``MoEOutput`` field
+  comments).
+* e2m1 / E8M0 decode (flashinfer_moe_ep.py ``_E2M1_LUT`` and
+  ``_dequant_fp4_ue8m0_gran32``): here the page fixes the arithmetic --
+  an fp32 product of the table value and the scale, returned as bf16 -- and
+  the oracle follows it.
+
+Parity pins: every function here is pinned by tests in ``tests/`` against
+values the pages print (the e2m1 table), closed forms, brute force over every
+subset / every expert, and invariants the pages state. None is unpinned.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+__all__ = [
+    "E2M1_TABLE", "e2m1_value", "ue8m0_scale", "dequant_mxfp4",
+    "sigmoid_f32_spec", "route_softmax_topk", "route_sigmoid_grouped",
+    "permute", "expert_mlp", "experts", "finalize", "shared_expert",
+    "moe_forward", "bf16_round",
+]
+
+# --------------------------------------------------------------------------
+# MXFP4 decode (flashinfer_moe_ep.py: ``_E2M1_LUT``, ``_dequant_fp4_ue8m0_gran32``,
+# ``_dequant_expert_weights_to_bf16``)
+# --------------------------------------------------------------------------
+
+#: The 16 e2m1 code values in code order. Codes 0-7 are the non-negative
+#: magnitudes; codes 8-15 repeat them with the sign bit (bit 3) set. The table
+#: is an interface both sides must agree on, so it is kept value for value.
+E2M1_TABLE = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0)
+
+
+def e2m1_value(code: int) -> float:
+    """Value of one 4-bit e2m1 code (``_E2M1_LUT``)."""
+    return E2M1_TABLE[int(code) & 0xF]
+
+
+def ue8m0_scale(s) -> np.ndarray:
+    """E8M0 scale byte -> float32: the byte becomes the fp32 exponent field,
+    i.e. the float whose bits are ``s << 23`` (``_dequant_fp4_ue8m0_gran32``).
+    Byte 0 therefore decodes to 0.0 and byte 255 to +inf, as the bit rule says.
+    """
+    s = np.asarray(s, dtype=np.uint32)
+    return (s << np.uint32(23)).astype(np.uint32).view(np.float32)
+
+
+def bf16_round(x) -> np.ndarray:
+    """float -> nearest bfloat16 (ties to even), returned as float32 values."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    nan = np.isnan(f)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    u = (u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
+    out = u.astype(np.uint32).view(np.float32).copy()
+    out[nan] = np.float32(np.nan)
+    return out
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Packed e2m1 [rows, C/2] + E8M0 scales [rows, C/32] -> values [rows, C].
+
+    Byte j of a row holds element 2j in its low nibble and element 2j+1 in its
+    high nibble; scale byte b covers elements 32b..32b+31. The product is taken
+    in float32 and rounded to bf16, as ``_dequant_fp4_ue8m0_gran32`` does; for
+    scale bytes 1..254 every product is exactly representable, so the bf16
+    rounding changes nothing there. Returned as float64.
+    """
+    packed = np.asarray(packed, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    rows, half = packed.shape
+    C = 2 * half
+    assert scales.shape == (rows, C // 32)
+    table = np.array(E2M1_TABLE, dtype=np.float32)
+    vals = np.empty((rows, C), dtype=np.float32)
+    vals[:, 0::2] = table[packed & 0x0F]
+    vals[:, 1::2] = table[packed >> 4]
+    sf = np.repeat(ue8m0_scale(scales), 32, axis=1)
+    with np.errstate(over="ignore", invalid="ignore"):
+        prod = vals * sf
+    return bf16_round(prod).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Router
+# --------------------------------------------------------------------------
+
+def _topk_desc(keys: np.ndarray, k: int, allowed=None) -> list:
+    """Indices of the k largest keys, ordered by key descending; equal keys
+    go to the lower index. ``allowed`` masks candidates (None = all)."""
+    idx = [i for i in range(len(keys)) if allowed is None or allowed[i]]
+    idx.sort(key=lambda i: (-float(keys[i]), i))
+    return idx[:k]
+
+
+def route_softmax_topk(logits: np.ndarray, top_k: int, routed_scaling_factor: float = 1.0):
+    """Softmax router: probabilities over all E experts, the top_k largest
+    kept and renormalised to sum to one, times the routed scale.
+
+    Selection is made on the float32 logits themselves (softmax is strictly
+    increasing, so the top_k probabilities are the top_k logits), ordered by
+    logit descending, ties to the lower expert id. Weights: float64 softmax
+    over all experts, restricted to the selected ones, divided by their sum.
+    Returns (ids int32 [M, k], weights float64 [M, k]).
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    M, E = logits.shape
+    ids = np.zeros((M, top_k), dtype=np.int32)
+    w = np.zeros((M, top_k), dtype=np.float64)
+    for t in range(M):
+        sel = _topk_desc(logits[t], top_k)
+        l64 = logits[t].astype(np.float64)
+        p = np.exp(l64 - l64.max())
+        p = p / p.sum()
+        ps = p[sel]
+        ids[t] = sel
+        w[t] = ps / ps.sum() * routed_scaling_factor
+    return ids, w
+
+
+# Constants of the written float32 exp spec (Cody & Waite argument reduction,
+# Taylor polynomial). LN2_HI is ln 2 cut to 16 significant bits so that
+# n * LN2_HI is exact for |n| <= 256; LN2_LO is the float32 remainder.
+_LOG2E = np.float32(1.4426950408889634)
+_LN2_HI = np.float32(0.693145751953125)
+_LN2_LO = np.float32(1.4286068203094173e-06)
+_INV_FACT = [np.float32(1.0 / math.factorial(i)) for i in range(8)]   # 1/0! .. 1/7!
+
+
+def _exp_f32_spec(t: np.float32) -> np.float32:
+    """exp(t) in float32 by the written spec: every step one IEEE float32
+    operation rounded to nearest (no fused multiply-add).
+
+      t > 88      -> +inf            t < -80 -> 0
+      n = rint(t * LOG2E)            (float32 product, round half to even)
+      r = (t - n*LN2_HI) - n*LN2_LO
+      p = ((((((c7 r + c6) r + c5) r + c4) r + c3) r + c2) r + c1) r + c0,  c_i = fl32(1/i!)
+      exp = p * 2^n                  (exact: 2^n is built from its bits)
+    """
+    t = np.float32(t)
+    if np.isnan(t):
+        return np.float32(np.nan)
+    if t > np.float32(88.0):
+        return np.float32(np.inf)
+    if t < np.float32(-80.0):
+        return np.float32(0.0)
+    n = np.rint(np.float32(t * _LOG2E))
+    r = np.float32(t - np.float32(n * _LN2_HI))
+    r = np.float32(r - np.float32(n * _LN2_LO))
+    p = _INV_FACT[7]
+    for c in reversed(_INV_FACT[:7]):
+        p = np.float32(np.float32(p * r) + c)
+    two_n = np.array([(int(n) + 127) << 23], dtype=np.uint32).view(np.float32)[0]
+    return np.float32(p * two_n)
+
+
+def sigmoid_f32_spec(x) -> np.ndarray:
+    """sigma(x) = 1 / (1 + exp(-x)) in float32 with the written exp spec; one
+    rounded float32 add and one rounded float32 divide."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    one = np.float32(1.0)
+    for i in range(flat_in.size):
+        e = _exp_f32_spec(np.float32(-flat_in[i]))
+        with np.errstate(over="ignore"):
+            flat_out[i] = np.float32(one / np.float32(one + e))
+    return out
+
+
+def route_sigmoid_grouped(logits: np.ndarray, score_bias: np.ndarray, top_k: int,
+                          n_group: int, topk_group: int,
+                          routed_scaling_factor: float = 1.0):
+    """Sigmoid + bias router with grouped top-k (DeepSeek-V3's published rule).
+
+    s_e = sigmoid(l_e); b_e = s_e + bias_e (float32; the bias steers selection
+    only). The E experts form n_group contiguous groups; a group's score is
+    the float32 sum of its two largest b. The topk_group best groups are kept
+    (ties to the lower group id); among their experts the top_k largest b are
+    selected, ordered by b descending, ties to the lower expert id. The
+    weights are the unbiased s of the selected experts divided by their sum,
+    times the routed scale -- which is folded into the weights here, so the
+    caller's later routed scale is 1.0 (moe_output.py, ``MoEOutput``
+    ``routed_scaling_factor`` comment).
+    Returns (ids int32 [M, k], weights float64 [M, k]).
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    bias = np.asarray(score_bias, dtype=np.float32)
+    M, E = logits.shape
+    assert E % n_group == 0
+    G = E // n_group
+    s32 = sigmoid_f32_spec(logits)
+    b32 = (s32 + bias[None, :]).astype(np.float32)
+    ids = np.zeros((M, top_k), dtype=np.int32)
+    w = np.zeros((M, top_k), dtype=np.float64)
+    for t in range(M):
+        gscore = np.zeros(n_group, dtype=np.float32)
+        for g in range(n_group):
+            top2 = sorted(b32[t, g * G:(g + 1) * G].tolist(), reverse=True)[:2]
+            gscore[g] = np.float32(np.float32(top2[0]) + np.float32(top2[1]))
+        groups = _topk_desc(gscore, topk_group)
+        allowed = np.zeros(E, dtype=bool)
+        for g in groups:
+            allowed[g * G:(g + 1) * G] = True
+        sel = _topk_desc(b32[t], top_k, allowed)
+        s64 = 1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)))
+        ids[t] = sel
+        w[t] = s64[sel] / s64[sel].sum() * routed_scaling_factor
+    return ids, w
+
+
+# --------------------------------------------------------------------------
+# Permute (the permute map of moe_output.py ``UnfinalizedMoEOutput``)
+# --------------------------------------------------------------------------
+
+def permute(topk_ids: np.ndarray, E: int, expert_map=None):
+    """Group the M*k routes by local expert.
+
+    ``expert_map[e]`` gives the local id of global expert e, -1 if it is not
+    local; without a map every expert is local with its own id. Routes are
+    ordered expert-major and, within an expert, by expanded index t*k + j.
+    Returns (offsets int32 [E_local+1], map int32 [M, k] with -1 for masked
+    routes, inverse int32 [R] giving the expanded index of each permuted row,
+    E_local).
+    """
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    M, k = ids.shape
+    if expert_map is None:
+        emap = np.arange(E, dtype=np.int64)
+        E_local = E
+    else:
+        emap = np.asarray(expert_map, dtype=np.int64)
+        E_local = int(emap.max()) + 1 if (emap >= 0).any() else 0
+    local = emap[ids.reshape(-1)]                  # [M*k]
+    routes = [(int(local[i]), i) for i in range(M * k) if local[i] >= 0]
+    routes.sort()                                  # expert-major, then expanded index
+    counts = np.zeros(E_local, dtype=np.int64)
+    for le, _ in routes:
+        counts[le] += 1
+    offsets = np.zeros(E_local + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    pmap = np.full(M * k, -1, dtype=np.int32)
+    inverse = np.zeros(len(routes), dtype=np.int32)
+    for p, (_, i) in enumerate(routes):
+        pmap[i] = p
+        inverse[p] = i
+    return offsets, pmap.reshape(M, k), inverse, E_local
+
+
+# --------------------------------------------------------------------------
+# Experts (GEMM1 -> silu_and_mul -> GEMM2), unweighted and unreduced
+# --------------------------------------------------------------------------
+
+def expert_mlp(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
+    """One expert on token rows x [T, K]: h = x W1^T [T, 2N]; the first N
+    columns are the gate, the last N the up projection (``silu_and_mul``:
+    output width half the input width); a = silu(gate) * up with
+    silu(z) = z / (1 + e^-z); y = a W2^T [T, K]. Float64."""
+    x = np.asarray(x, dtype=np.float64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    N = w1.shape[0] // 2
+    h = x @ w1.T
+    gate, up = h[:, :N], h[:, N:]
+    with np.errstate(over="ignore"):
+        a = gate / (1.0 + np.exp(-gate)) * up
+    return a @ w2.T
+
+
+def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
+            inverse: np.ndarray, top_k: int) -> np.ndarray:
+    """``gemm2_permuted`` [R, K]: row p is the output of expert le (the p-th
+    row falls in [offsets[le], offsets[le+1])) on token inverse[p] // top_k.
+    ``w1``/``w2`` are the local experts' weights as float arrays."""
+    x = np.asarray(x, dtype=np.float64)
+    R = int(offsets[-1])
+    out = np.zeros((R, w2.shape[1]), dtype=np.float64)
+    for le in range(len(offsets) - 1):
+        r0, r1 = int(offsets[le]), int(offsets[le + 1])
+        if r1 > r0:
+            toks = np.asarray(inverse[r0:r1], dtype=np.int64) // top_k
+            out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le])
+    return out
+
+
+def shared_expert(x: np.ndarray, ws1: np.ndarray, ws2: np.ndarray) -> np.ndarray:
+    """The shared expert: the same gated MLP applied to every token."""
+    return expert_mlp(x, ws1, ws2)
+
+
+# --------------------------------------------------------------------------
+# Finalize (modular_kernel.py ``FusedMoEPrepareAndFinalize.finalize``;
+# moe_output.py ``MoEOutput``)
+# --------------------------------------------------------------------------
+
+def finalize(gemm2_permuted: np.ndarray, expert_weights: np.ndarray, pmap: np.ndarray,
+             shared=None, routed_scaling_factor: float = 1.0) -> np.ndarray:
+    """out[t] = rsf * sum_j w[t,j] * gemm2_permuted[map[t,j]] + shared[t], the
+    sum over the routes with map != -1 (a -1 route contributes nothing), in
+    j order; the shared output is added after the routed scale."""
+    g = np.asarray(gemm2_permuted, dtype=np.float64)
+    w = np.asarray(expert_weights, dtype=np.float64)
+    pmap = np.asarray(pmap)
+    M, k = pmap.shape
+    out = np.zeros((M, g.shape[1] if g.ndim == 2 else 0), dtype=np.float64)
+    for t in range(M):
+        acc = np.zeros(out.shape[1], dtype=np.float64)
+        for j in range(k):
+            p = int(pmap[t, j])
+            if p >= 0:
+                acc += w[t, j] * g[p]
+        out[t] = routed_scaling_factor * acc
+        if shared is not None:
+            out[t] += np.asarray(shared[t], dtype=np.float64)
+    return out
+
+
+def moe_forward(x, logits, w1, w2, top_k, route="softmax", score_bias=None,
+                n_group=1, topk_group=1, routed_scaling_factor=1.0,
+                expert_map=None, ws1=None, ws2=None):
+    """The whole layer: route -> permute -> experts -> finalize (+ shared).
+
+    ``w1``/``w2`` are float arrays of the local experts only ([E_local, 2N, K],
+    [E_local, K, N]). The routed scale of the sigmoid router is folded into
+    its weights, so finalize then uses 1.0. Returns a dict of every
+    intermediate (ids, weights, offsets, map, inverse, gemm2_permuted,
+    shared, out).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    logits = np.asarray(logits, dtype=np.float32)
+    E = logits.shape[1]
+    if route == "softmax":
+        ids, w = route_softmax_topk(logits, top_k, routed_scaling_factor)
+    else:
+        ids, w = route_sigmoid_grouped(logits, score_bias, top_k, n_group, topk_group,
+                                       routed_scaling_factor)
+    offsets, pmap, inverse, _ = permute(ids, E, expert_map)
+    g2 = experts(x, w1, w2, offsets, inverse, top_k)
+    shared = shared_expert(x, ws1, ws2) if ws1 is not None else None
+    out = finalize(g2, w, pmap, shared, 1.0)
+    return dict(ids=ids, weights=w, offsets=offsets, map=pmap, inverse=inverse,
+                gemm2_permuted=g2, shared=shared, out=out)

@@ -1,0 +1,364 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself:
+the e2m1 table printed on the page, closed forms, brute force over every
+subset / every expert, library routines for special cases, and invariants
+the pages state. CPU only."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _e2m1_from_bits(code: int) -> float:
+    """e2m1 by its bit fields (OCP MX v1.0): sign bit 3, exponent bits 2-1
+    (bias 1), mantissa bit 0; exponent 0 is subnormal (m * 0.5)."""
+    s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    mag = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1.0 + m / 2.0)
+    return -mag if s else mag
+
+
+# ---------------------------------------------------------------- MXFP4 decode
+
+def test_e2m1_table_matches_page():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_table.txt"))
+            if l.strip() and not l.startswith("#")]
+    page = {int(c): float(v) for c, v in rows}
+    assert len(page) == 16
+    for code in range(16):
+        got = O.e2m1_value(code)
+        assert got == page[code]
+        assert math.copysign(1.0, got) == math.copysign(1.0, page[code])
+
+
+def test_e2m1_table_matches_bitfield_definition():
+    for code in range(16):
+        got, want = O.e2m1_value(code), _e2m1_from_bits(code)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want)
+
+
+def test_ue8m0_closed_form():
+    s = np.arange(256)
+    got = O.ue8m0_scale(s)
+    assert got[0] == 0.0 and np.isinf(got[255])
+    for v in range(1, 255):
+        assert got[v] == math.ldexp(1.0, v - 127)
+
+
+def test_dequant_exhaustive_bytes_and_scales():
+    # every packed byte value, under every finite scale byte
+    packed = np.tile(np.arange(256, dtype=np.uint8), (254, 1))      # [254 rows, 256 bytes] -> C = 512
+    scales = np.repeat(np.arange(1, 255, dtype=np.uint8)[:, None], 16, axis=1)  # [254, 512/32]
+    got = O.dequant_mxfp4(packed, scales)
+
+    def f32(v):   # the page multiplies in float32: beyond its range the product is inf
+        return v if abs(v) <= 3.4028234663852886e38 else math.copysign(math.inf, v)
+
+    for r in range(254):
+        sc = math.ldexp(1.0, (r + 1) - 127)
+        for j in range(256):
+            assert got[r, 2 * j] == f32(_e2m1_from_bits(j & 0xF) * sc)
+            assert got[r, 2 * j + 1] == f32(_e2m1_from_bits(j >> 4) * sc)
+
+
+def test_dequant_scale_granularity_is_32():
+    rng = np.random.default_rng(5)
+    packed = rng.integers(0, 256, size=(3, 64), dtype=np.uint8)          # C = 128
+    scales = rng.integers(100, 140, size=(3, 4), dtype=np.uint8)
+    got = O.dequant_mxfp4(packed, scales)
+    for r in range(3):
+        for c in range(128):
+            byte = packed[r, c // 2]
+            code = (byte & 0xF) if c % 2 == 0 else (byte >> 4)
+            assert got[r, c] == _e2m1_from_bits(int(code)) * 2.0 ** (int(scales[r, c // 32]) - 127)
+
+
+def test_bf16_round_matches_torch():
+    x = np.random.default_rng(1).standard_normal(10000).astype(np.float32) * 37
+    x[:4] = [0.0, -0.0, 1e-40, 3.0e38]
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(O.bf16_round(x), want)
+
+
+# ---------------------------------------------------------------- sigmoid spec
+
+def test_sigmoid_spec_close_to_exact():
+    x = np.concatenate([np.linspace(-30, 30, 20001), np.linspace(-90, 90, 2001)]).astype(np.float32)
+    got = O.sigmoid_f32_spec(x).astype(np.float64)
+    exact = 1.0 / (1.0 + np.exp(-x.astype(np.float64)))
+    ulp = np.spacing(exact.astype(np.float32)).astype(np.float64)
+    normal = x > -88.0
+    assert np.all(np.abs(got - exact)[normal] <= 2 * ulp[normal])
+    # below -88 the true value is a float32 subnormal; the spec returns 0 there
+    assert np.all(got[~normal] == 0.0) and np.all(exact[~normal] < 2.0 ** -126)
+    assert O.sigmoid_f32_spec(np.float32(0.0)) == np.float32(0.5)
+    assert O.sigmoid_f32_spec(np.float32(100.0)) == 1.0
+    assert O.sigmoid_f32_spec(np.float32(-100.0)) == 0.0
+
+
+def test_sigmoid_spec_monotone():
+    x = np.sort(np.random.default_rng(2).standard_normal(20000).astype(np.float32) * 6)
+    y = O.sigmoid_f32_spec(x)
+    assert np.all(np.diff(y) >= 0)
+
+
+def test_exp_spec_constants():
+    # LN2_HI has at most 16 significant bits, and HI + LO is ln 2 to float64 rounding
+    hi = float(O.moe_oracle._LN2_HI)
+    m, e = math.frexp(hi)
+    assert (m * 2 ** 16) == int(m * 2 ** 16)
+    assert abs(hi + float(O.moe_oracle._LN2_LO) - math.log(2.0)) < 1e-13
+
+
+# ---------------------------------------------------------------- routers
+
+def _brute_best_subset(keys, k, allowed=None):
+    cand = [i for i in range(len(keys)) if allowed is None or allowed[i]]
+    best, best_s = None, None
+    for sub in itertools.combinations(cand, k):
+        s = sum(float(keys[i]) for i in sub)
+        if best_s is None or s > best_s:
+            best, best_s = set(sub), s
+    return best
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (9, 3), (12, 4)])
+def test_softmax_router_brute_force(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    logits = rng.standard_normal((40, E)).astype(np.float32)
+    ids, w = O.route_softmax_topk(logits, k, 1.0)
+    for t in range(40):
+        p = torch.softmax(torch.from_numpy(logits[t]).double(), 0).numpy()
+        assert set(ids[t].tolist()) == _brute_best_subset(p, k)
+        assert all(p[ids[t][i]] >= p[ids[t][i + 1]] for i in range(k - 1))
+        assert abs(w[t].sum() - 1.0) < 1e-12
+        # renormalised softmax: every ratio is exp of the logit difference
+        for a in range(k):
+            for b in range(k):
+                r = w[t, a] / w[t, b]
+                assert abs(r - math.exp(float(logits[t, ids[t, a]]) - float(logits[t, ids[t, b]]))) < 1e-9 * max(1, r)
+
+
+def test_softmax_router_ties_and_scale():
+    logits = np.array([[0.5, 1.0, 1.0, -2.0, 1.0, 0.0]], dtype=np.float32)
+    ids, w = O.route_softmax_topk(logits, 3, 2.5)
+    assert ids.tolist() == [[1, 2, 4]]
+    np.testing.assert_allclose(w, [[2.5 / 3] * 3], rtol=1e-12)
+    # -0.0 and +0.0 compare equal: lower id first
+    ids, _ = O.route_softmax_topk(np.array([[-0.0, 0.0, -1.0]], dtype=np.float32), 2)
+    assert ids.tolist() == [[0, 1]]
+
+
+def test_sigmoid_grouped_router_brute_force():
+    rng = np.random.default_rng(7)
+    E, n_group, topk_group, k = 16, 4, 2, 3
+    logits = rng.standard_normal((60, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    ids, w = O.route_sigmoid_grouped(logits, bias, k, n_group, topk_group, 2.5)
+    G = E // n_group
+    for t in range(60):
+        s = 1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)))
+        b = s + bias.astype(np.float64)
+        gs = [sum(sorted(b[g * G:(g + 1) * G], reverse=True)[:2]) for g in range(n_group)]
+        best_groups = _brute_best_subset(np.array(gs), topk_group)
+        allowed = np.zeros(E, bool)
+        for g in best_groups:
+            allowed[g * G:(g + 1) * G] = True
+        assert set(ids[t].tolist()) == _brute_best_subset(b, k, allowed)
+        assert all(allowed[i] for i in ids[t])
+        assert all(b[ids[t][i]] >= b[ids[t][i + 1]] for i in range(k - 1))
+        np.testing.assert_allclose(w[t], s[ids[t]] / s[ids[t]].sum() * 2.5, rtol=1e-12)
+        assert abs(w[t].sum() - 2.5) < 1e-12
+
+
+def test_sigmoid_grouped_single_group_is_plain_topk():
+    rng = np.random.default_rng(8)
+    logits = rng.standard_normal((20, 10)).astype(np.float32)
+    bias = np.zeros(10, np.float32)
+    ids, _ = O.route_sigmoid_grouped(logits, bias, 3, 1, 1)
+    ids2, _ = O.route_softmax_topk(logits, 3)        # sigmoid is increasing
+    assert (ids == ids2).all()
+
+
+# ---------------------------------------------------------------- permute
+
+def _check_permute(ids, E, emap=None):
+    offsets, pmap, inv, E_l = O.permute(ids, E, emap)
+    M, k = ids.shape
+    em = np.arange(E) if emap is None else np.asarray(emap)
+    local = em[ids.reshape(-1)]
+    masked = int((local < 0).sum())
+    R = int(offsets[-1])
+    assert R == M * k - masked                                   # counts sum
+    assert np.all(np.diff(offsets) >= 0) and offsets[0] == 0      # monotone offsets
+    flat = pmap.reshape(-1)
+    assert np.all((flat == -1) == (local < 0))                   # -1 exactly on masked routes
+    assert sorted(flat[flat >= 0].tolist()) == list(range(R))    # bijection onto [0, R)
+    for p in range(R):
+        assert flat[inv[p]] == p
+    # second formulation: stable argsort of the local ids
+    keep = np.nonzero(local >= 0)[0]
+    order = keep[np.argsort(local[keep], kind="stable")]
+    assert (inv == order).all()
+    for le in range(E_l):
+        assert offsets[le + 1] - offsets[le] == (local == le).sum()
+    return offsets, pmap, inv
+
+
+def test_permute_invariants():
+    rng = np.random.default_rng(3)
+    for E, k, M in [(8, 2, 16), (16, 4, 33), (5, 5, 7), (128, 8, 50)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+        _check_permute(ids, E)
+        emap = np.full(E, -1, np.int32)
+        keep = np.sort(rng.permutation(E)[: E // 2])
+        emap[keep] = np.arange(len(keep))
+        _check_permute(ids, E, emap)
+
+
+def test_permute_empty_and_all_masked():
+    offsets, pmap, inv, _ = O.permute(np.zeros((0, 2), np.int32), 4)
+    assert offsets.tolist() == [0, 0, 0, 0, 0] and pmap.shape == (0, 2) and len(inv) == 0
+    emap = np.array([-1, -1, 0, 1], np.int32)
+    offsets, pmap, inv, _ = O.permute(np.array([[0, 1]], np.int32), 4, emap)
+    assert offsets.tolist() == [0, 0, 0] and pmap.tolist() == [[-1, -1]]
+
+
+# ---------------------------------------------------------------- experts and finalize
+
+def _tiny_weights(rng, E, K, N):
+    w1 = rng.standard_normal((E, 2 * N, K)) / math.sqrt(K)
+    w2 = rng.standard_normal((E, K, N)) / math.sqrt(N)
+    return w1, w2
+
+
+def test_expert_mlp_matches_torch_swiglu():
+    rng = np.random.default_rng(4)
+    K, N = 24, 40
+    x = rng.standard_normal((9, K))
+    w1, w2 = _tiny_weights(rng, 1, K, N)
+    xt = torch.from_numpy(x)
+    g = xt @ torch.from_numpy(w1[0][:N]).T
+    u = xt @ torch.from_numpy(w1[0][N:]).T
+    want = (torch.nn.functional.silu(g) * u) @ torch.from_numpy(w2[0]).T
+    np.testing.assert_allclose(O.expert_mlp(x, w1[0], w2[0]), want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_top1_weight1_is_dense_mlp():
+    """top_k = 1 with weight 1 reproduces the single expert's dense MLP."""
+    rng = np.random.default_rng(6)
+    M, K, N, E = 12, 16, 32, 3
+    x = rng.standard_normal((M, K))
+    w1, w2 = _tiny_weights(rng, E, K, N)
+    ids = rng.integers(0, E, size=(M, 1)).astype(np.int32)
+    offsets, pmap, inv, _ = O.permute(ids, E)
+    g2 = O.experts(x, w1, w2, offsets, inv, 1)
+    out = O.finalize(g2, np.ones((M, 1)), pmap)
+    for t in range(M):
+        e = ids[t, 0]
+        xt = torch.from_numpy(x[t:t + 1])
+        h = xt @ torch.from_numpy(w1[e]).T
+        want = (torch.nn.functional.silu(h[:, :N]) * h[:, N:]) @ torch.from_numpy(w2[e]).T
+        np.testing.assert_allclose(out[t], want.numpy()[0], rtol=1e-12, atol=1e-12)
+
+
+def test_routed_equals_dense_brute_force():
+    """Every token through every expert, weighted by a dense [M, E] gate that
+    is zero off-route, equals the routed permute/experts/finalize result."""
+    rng = np.random.default_rng(9)
+    M, K, N, E, k = 10, 16, 24, 6, 3
+    x = rng.standard_normal((M, K))
+    w1, w2 = _tiny_weights(rng, E, K, N)
+    logits = rng.standard_normal((M, E)).astype(np.float32)
+    r = O.moe_forward(x, logits, w1, w2, k)
+    dense_gate = np.zeros((M, E))
+    for t in range(M):
+        dense_gate[t, r["ids"][t]] = r["weights"][t]
+    want = np.zeros((M, K))
+    for e in range(E):
+        xt = torch.from_numpy(x)
+        h = xt @ torch.from_numpy(w1[e]).T
+        ye = ((torch.nn.functional.silu(h[:, :N]) * h[:, N:]) @ torch.from_numpy(w2[e]).T).numpy()
+        want += dense_gate[:, e:e + 1] * ye
+    np.testing.assert_allclose(r["out"], want, rtol=1e-11, atol=1e-11)
+
+
+def test_masked_routes_contribute_zero_and_nan_does_not_leak():
+    rng = np.random.default_rng(10)
+    M, K, N, E, k = 8, 16, 16, 4, 2
+    x = rng.standard_normal((M, K))
+    w1, w2 = _tiny_weights(rng, E, K, N)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    emap = np.array([0, -1, 1, -1], np.int32)
+    offsets, pmap, inv, E_l = O.permute(ids, E, emap)
+    g2 = O.experts(x, w1[[0, 2]], w2[[0, 2]], offsets, inv, k)
+    w = rng.random((M, k))
+    w_poison = w.copy()
+    w_poison[pmap < 0] = np.nan
+    g2_pad = np.vstack([g2, np.full((M * k - len(g2), K), np.nan)])   # padded rows never referenced
+    a = O.finalize(g2, w, pmap)
+    b = O.finalize(g2_pad, w_poison, pmap)
+    assert np.isfinite(b).all()
+    np.testing.assert_array_equal(a, b)
+
+
+def test_complement_mask_additivity():
+    """out(map A) + out(map complement of A) = out(no map)."""
+    rng = np.random.default_rng(11)
+    M, K, N, E, k = 9, 16, 16, 6, 2
+    x = rng.standard_normal((M, K))
+    w1, w2 = _tiny_weights(rng, E, K, N)
+    logits = rng.standard_normal((M, E)).astype(np.float32)
+    full = O.moe_forward(x, logits, w1, w2, k)["out"]
+    sel = np.array([1, 0, 1, 1, 0, 0], bool)
+    emap_a = np.full(E, -1, np.int32); emap_a[sel] = np.arange(sel.sum())
+    emap_b = np.full(E, -1, np.int32); emap_b[~sel] = np.arange((~sel).sum())
+    out_a = O.moe_forward(x, logits, w1[sel], w2[sel], k, expert_map=emap_a)["out"]
+    out_b = O.moe_forward(x, logits, w1[~sel], w2[~sel], k, expert_map=emap_b)["out"]
+    np.testing.assert_allclose(out_a + out_b, full, rtol=1e-12, atol=1e-12)
+
+
+def test_finalize_scale_before_shared_add():
+    g2 = np.array([[1.0, 2.0], [3.0, 4.0]])
+    pmap = np.array([[0, 1]])
+    w = np.array([[0.25, 0.5]])
+    shared = np.array([[10.0, 20.0]])
+    out = O.finalize(g2, w, pmap, shared, routed_scaling_factor=2.0)
+    np.testing.assert_array_equal(out, [[2.0 * (0.25 + 1.5) + 10.0, 2.0 * (0.5 + 2.0) + 20.0]])
+
+
+def test_shared_expert_is_top1_mlp():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((5, 16))
+    w1, w2 = _tiny_weights(rng, 1, 16, 8)
+    np.testing.assert_array_equal(O.shared_expert(x, w1[0], w2[0]), O.expert_mlp(x, w1[0], w2[0]))
+
+
+def test_mxfp4_layer_equals_bf16_layer_on_dequantised_weights():
+    """The MXFP4 path is the bf16 path on the dequantised weights: dequantise,
+    then run the plain layer; compare with a layer whose weights are the
+    bit-field decode of the same bytes."""
+    rng = np.random.default_rng(13)
+    E, K, N, M, k = 3, 64, 64, 6, 2
+    p1 = rng.integers(0, 256, size=(E, 2 * N, K // 2), dtype=np.uint8)
+    s1 = rng.integers(118, 124, size=(E, 2 * N, K // 32), dtype=np.uint8)
+    p2 = rng.integers(0, 256, size=(E, K, N // 2), dtype=np.uint8)
+    s2 = rng.integers(118, 124, size=(E, K, N // 32), dtype=np.uint8)
+    w1 = np.stack([O.dequant_mxfp4(p1[e], s1[e]) for e in range(E)])
+    w2 = np.stack([O.dequant_mxfp4(p2[e], s2[e]) for e in range(E)])
+    lut = np.array([_e2m1_from_bits(c) for c in range(16)])
+    def bitdec(p, s):
+        v = np.empty(p.shape[:-1] + (p.shape[-1] * 2,))
+        v[..., 0::2] = lut[p & 15]; v[..., 1::2] = lut[p >> 4]
+        return v * np.repeat(2.0 ** (s.astype(np.float64) - 127), 32, axis=-1)
+    np.testing.assert_array_equal(w1, bitdec(p1, s1))
+    np.testing.assert_array_equal(w2, bitdec(p2, s2))
+    x = rng.standard_normal((M, K))
+    logits = rng.standard_normal((M, E)).astype(np.float32)
+    r = O.moe_forward(x, logits, w1, w2, k)
+    assert np.isfinite(r["out"]).all()
