@@ -1,0 +1,289 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer forward.
+ *
+ * The layer is the pipeline [Router] -> [Quantize-Dispatch] ->
+ * [Permute-Experts-Unpermute] -> [Combine] laid out in the module header of
+ * vllm/model_executor/layers/fused_moe/modular_kernel.py. On one GPU with all
+ * experts local the dispatch and combine are no-ops, so the calls are:
+ *
+ *   moe_route     logits -> topk_ids, topk_weights                  [Router]
+ *   moe_permute   topk_ids -> expert_offsets, expanded_idx_to_permuted_idx,
+ *                 permuted_to_expanded, x_perm                        (permute)
+ *   moe_experts   x_perm -> gemm2_permuted (GEMM1, silu_and_mul, GEMM2;
+ *                 unweighted, unreduced), optionally finalized   (experts)
+ *   moe_finalize  gemm2_permuted, weights, map, shared -> out    (unpermute+reduce)
+ *
+ * Conventions that hold for every call:
+ *  - Every pointer argument is a DEVICE pointer to a dense row-major
+ *    (contiguous) array, unless it is documented as a host pointer. The
+ *    deferred-finalize contract requires contiguous buffers
+ *    (moe_output.py, convert_flashinfer_moe_output).
+ *  - The caller owns and allocates every buffer. The library never
+ *    allocates device memory, never synchronizes, and enqueues all work on
+ *    `stream` (asynchronous).
+ *  - Every call returns a moe_status. Nothing throws across the ABI.
+ *    Argument validation runs on the host before anything is enqueued; a
+ *    call that fails validation enqueues nothing.
+ *  - Problems found on the device (an expert id or a map entry out of range,
+ *    a pipeline wait that ran out) do not trap: the offending route is
+ *    skipped and a device error word is set, which moe_get_error() returns.
+ *  - The device must have compute capability 10.3 (GB300); other devices get
+ *    MOE_ERR_UNSUPPORTED_ARCH (flashinfer_moe_ep.py,
+ *    validate_fi_moe_ep_config: the mega MoE kernels are Blackwell-only and
+ *    fail loudly elsewhere).
+ *  - bf16 means IEEE bfloat16 stored as 16-bit words; f32 is IEEE binary32.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* a size, range, NULL or dtype rule is broken   */
+    MOE_ERR_ALIGNMENT = 2,         /* K or N not a multiple of 128; a pointer not 16-byte aligned */
+    MOE_ERR_UNSUPPORTED = 3,       /* a combination this library does not implement */
+    MOE_ERR_UNSUPPORTED_ARCH = 4,  /* the current device is not compute capability 10.3 */
+    MOE_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than the *_workspace_size() */
+    MOE_ERR_CUDA = 6,              /* a CUDA runtime call (launch, attribute, no device) failed */
+    MOE_ERR_DEVICE_INDEX = 7,      /* device-detected: an expert id or map entry out of range */
+    MOE_ERR_DEVICE_TIMEOUT = 8     /* device-detected: a pipeline wait exceeded its limit */
+} moe_status;
+
+typedef enum moe_dtype {
+    MOE_DTYPE_BF16 = 0,
+    MOE_DTYPE_F32 = 1
+} moe_dtype;
+
+typedef enum moe_route_method {
+    /* softmax over the E logits, top_k largest, renormalised to sum 1, x scale */
+    MOE_ROUTE_SOFTMAX_TOPK = 0,
+    /* sigmoid scores + selection bias, grouped top-k, renormalised, x scale */
+    MOE_ROUTE_SIGMOID_GROUPED_TOPK = 1
+} moe_route_method;
+
+typedef enum moe_weight_format {
+    MOE_WEIGHTS_BF16 = 0,          /* bf16 weights                                     */
+    MOE_WEIGHTS_MXFP4 = 1          /* e2m1 codes, two per byte, + one E8M0 byte per 32 */
+} moe_weight_format;
+
+/*
+ * Expert weights of the E_local local experts (modular_kernel.py,
+ * _moe_problem_size: w1 is [E, 2N, .], w2 is [., K, .]; for packed formats the
+ * trailing dimension is halved, so K and N are given explicitly here).
+ *
+ *   BF16:  w1 bf16 [E_local, 2N, K]; rows 0..N-1 of each expert are the gate
+ *          projection, rows N..2N-1 the up projection (silu_and_mul multiplies
+ *          silu(first half) by the second half).
+ *          w2 bf16 [E_local, K, N].
+ *   MXFP4: w1 u8 [E_local, 2N, K/2] and w1_scale u8 [E_local, 2N, K/32];
+ *          w2 u8 [E_local, K, N/2] and w2_scale u8 [E_local, K, N/32].
+ *          Byte j of a row holds element 2j in its low nibble and element
+ *          2j+1 in its high nibble; scale byte b of a row scales elements
+ *          32b..32b+31 by the float whose bits are (b << 23), i.e. 2^(b-127)
+ *          (flashinfer_moe_ep.py, _E2M1_LUT and _dequant_fp4_ue8m0_gran32).
+ *          Scale bytes must lie in 1..254 and every decoded value must be a
+ *          normal bf16 or zero (the kernels decode to bf16 before the MMA).
+ *
+ * K and N must be multiples of 128. All pointers 16-byte aligned.
+ */
+typedef struct moe_weights {
+    moe_weight_format format;
+    int E_local;
+    int K;                 /* hidden size                 */
+    int N;                 /* expert intermediate size    */
+    const void* w1;
+    const uint8_t* w1_scale;   /* MXFP4 only, else NULL */
+    const void* w2;
+    const uint8_t* w2_scale;   /* MXFP4 only, else NULL */
+} moe_weights;
+
+/* ------------------------------------------------------------------------
+ * moe_route -- the [Router] step (modular_kernel.py module header; its
+ * outputs are FusedMoEModularKernel.forward's topk_ids / topk_weights).
+ *
+ *   logits        f32 [M, E] router logits.
+ *   method        MOE_ROUTE_SOFTMAX_TOPK: select the top_k largest logits,
+ *                 ordered by logit descending, equal logits to the lower
+ *                 expert id; weight_j = exp(l_j - l_max) / sum over the
+ *                 selected of exp(l_i - l_max), times routed_scaling_factor.
+ *                 MOE_ROUTE_SIGMOID_GROUPED_TOPK: s_e = sigmoid(l_e) computed
+ *                 by a fixed float32 spec (see moe_debug_sigmoid),
+ *                 b_e = s_e + score_bias[e]; the experts form n_group
+ *                 contiguous groups of E/n_group; a group's score is the
+ *                 float32 sum of its two largest b; the topk_group best groups
+ *                 are kept (ties to the lower group); the top_k largest b
+ *                 among their experts are selected, ordered by b descending
+ *                 (ties to the lower id); weight_j = s_j / sum_selected s,
+ *                 times routed_scaling_factor (the scale is then folded:
+ *                 moe_output.py, UnfinalizedMoEOutput expert_weights comment).
+ *   score_bias    f32 [E]; required for the sigmoid method, must be NULL for softmax.
+ *   n_group, topk_group   sigmoid method only (E % n_group == 0,
+ *                 E/n_group >= 2, 1 <= topk_group <= n_group,
+ *                 top_k <= topk_group * E/n_group); pass 1, 1 for softmax.
+ *   topk_ids      out, i32 [M, top_k], global expert ids.
+ *   topk_weights  out, [M, top_k] in weights_dtype (bf16 or f32).
+ * Limits: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), M >= 0 (M = 0: no work).
+ * Logits must be finite (NaN gives an unspecified but in-range selection).
+ * ---------------------------------------------------------------------- */
+moe_status moe_route(const float* logits, int M, int E, int top_k,
+                     moe_route_method method, const float* score_bias,
+                     int n_group, int topk_group, float routed_scaling_factor,
+                     int32_t* topk_ids, void* topk_weights, moe_dtype weights_dtype,
+                     cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_permute -- group the M*top_k routes by local expert (the permute half
+ * of [Permute-Experts-Unpermute]; the map is UnfinalizedMoEOutput's
+ * expanded_idx_to_permuted_idx, moe_output.py).
+ *
+ *   topk_ids      i32 [M, top_k] global expert ids in [0, E).
+ *   expert_map    i32 [E] or NULL. expert_map[e] is the local id of global
+ *                 expert e, or -1 when e is not local (modular_kernel.py,
+ *                 prepare/apply expert_map). Local ids must be < E_local and
+ *                 no two global experts may share one. NULL = identity
+ *                 (then E_local must equal E).
+ *   x             bf16 [M, K] token activations; may be NULL iff x_perm is NULL.
+ *
+ * Outputs. Routes are ordered expert-major, and within an expert by their
+ * expanded index t*top_k + j (a canonical order that does not depend on any
+ * tiling). R = number of routes to local experts.
+ *   expert_offsets               i32 [E_local+1]: rows of local expert le are
+ *                                [offsets[le], offsets[le+1]); offsets[E_local] = R.
+ *   expanded_idx_to_permuted_idx i32 [M, top_k]: permuted row of route (t, j),
+ *                                -1 for a route to a non-local expert.
+ *   permuted_to_expanded         i32 [M*top_k]: entries [0, R) give the expanded
+ *                                index of each permuted row; the rest are not written.
+ *   x_perm                       bf16 [M*top_k, K] or NULL: row p = x[inverse[p] / top_k]
+ *                                for p < R; rows >= R are not written.
+ *   workspace                    device scratch of moe_permute_workspace_size() bytes
+ *                                (contents on entry do not matter).
+ * Out-of-range ids or map entries set MOE_ERR_DEVICE_INDEX and the route is
+ * treated as non-local.
+ * ---------------------------------------------------------------------- */
+size_t moe_permute_workspace_size(int M, int top_k, int E_local);
+
+moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E,
+                       const int32_t* expert_map, int E_local,
+                       const void* x, int K,
+                       int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
+                       int32_t* permuted_to_expanded, void* x_perm,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_experts -- the experts: GEMM1, silu_and_mul, GEMM2, per local expert on
+ * its rows of x_perm (modular_kernel.py, FusedMoEPermuteExpertsUnpermute.apply
+ * and .activation). The result is unweighted and unreduced.
+ *
+ *   x_perm           bf16 [M*top_k, K] (rows [0, R) valid, from moe_permute).
+ *   expert_offsets   i32 [E_local+1] (from moe_permute); read on the device, so
+ *                    the host never learns R.
+ *   gemm2_permuted   out, [M*top_k, K] in gemm2_dtype (bf16 or f32): row p is
+ *                    W2[le] . (silu(W1g[le] x) * (W1u[le] x)) for the token of
+ *                    permuted row p, densely packed at K; rows >= R are not
+ *                    written (UnfinalizedMoEOutput: indexed by row, padded row
+ *                    count never referenced).
+ *   do_finalize      0: stop after GEMM2 (the deferred output is gemm2_permuted,
+ *                    expert_weights and expanded_idx_to_permuted_idx); `out`
+ *                    must be NULL -- a deferred output has no destination
+ *                    (convert_flashinfer_moe_output).
+ *                    1: also run moe_finalize into `out`, with the same
+ *                    result bit for bit as a separate moe_finalize call.
+ *   expert_weights, weights_dtype, expanded_idx_to_permuted_idx, shared_out,
+ *   shared_dtype, routed_scaling_factor, out, out_dtype:
+ *                    as in moe_finalize (ignored when do_finalize = 0; pass NULL).
+ *   workspace        device scratch of at least moe_experts_workspace_size()
+ *                    bytes, ZERO-FILLED BEFORE ITS FIRST USE. Every completed
+ *                    call leaves its synchronisation counters at zero again, so
+ *                    a workspace is zeroed once, and again only after a call
+ *                    that reported MOE_ERR_DEVICE_TIMEOUT. Calls that share a
+ *                    workspace must not overlap on the GPU.
+ * ---------------------------------------------------------------------- */
+size_t moe_experts_workspace_size(const moe_weights* w, int M, int top_k);
+
+moe_status moe_experts(const moe_weights* w,
+                       const void* x_perm, const int32_t* expert_offsets,
+                       int M, int top_k,
+                       void* gemm2_permuted, moe_dtype gemm2_dtype,
+                       int do_finalize,
+                       const void* expert_weights, moe_dtype weights_dtype,
+                       const int32_t* expanded_idx_to_permuted_idx,
+                       const void* shared_out, moe_dtype shared_dtype,
+                       float routed_scaling_factor,
+                       void* out, moe_dtype out_dtype,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_finalize -- apply the routing weights and reduce over top_k
+ * (modular_kernel.py, FusedMoEPrepareAndFinalize.finalize), then the routed
+ * scale and the shared-expert add (moe_output.py, MoEOutput: the shared
+ * output is folded in by whoever finalizes; the routed scale is applied to
+ * the routed sum before the shared add and is 1.0 when folded):
+ *
+ *   out[t] = routed_scaling_factor * sum_{j : map[t,j] != -1}
+ *                 expert_weights[t,j] * gemm2_permuted[map[t,j]]
+ *            + shared_out[t]
+ *
+ * accumulated in float32 in j order, then rounded once to out_dtype.
+ *   gemm2_permuted     [num_permuted_rows, K] in gemm2_dtype.
+ *   num_permuted_rows  rows allocated in gemm2_permuted (for the device bounds
+ *                      check only; map entries >= it set MOE_ERR_DEVICE_INDEX
+ *                      and are skipped).
+ *   expert_weights     [M, top_k] in weights_dtype.
+ *   expanded_idx_to_permuted_idx  i32 [M, top_k].
+ *   shared_out         [M, K] in shared_dtype, or NULL.
+ *   out                out, [M, K] in out_dtype; may not alias any input.
+ * ---------------------------------------------------------------------- */
+moe_status moe_finalize(const void* gemm2_permuted, moe_dtype gemm2_dtype, int num_permuted_rows,
+                        const void* expert_weights, moe_dtype weights_dtype,
+                        const int32_t* expanded_idx_to_permuted_idx, int M, int top_k, int K,
+                        const void* shared_out, moe_dtype shared_dtype,
+                        float routed_scaling_factor,
+                        void* out, moe_dtype out_dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_shared_expert -- the shared expert: the same gated MLP on every token
+ * (its output is MoEOutput.shared_output, moe_output.py), run by the same
+ * grouped GEMM kernels with one group of M rows.
+ *   ws1 bf16 [2*Ns, K] (gate rows then up rows), ws2 bf16 [K, Ns], x bf16 [M, K],
+ *   shared_out out [M, K] in shared_dtype. K, Ns multiples of 128.
+ *   workspace: moe_shared_expert_workspace_size() bytes, zero-filled before
+ *   first use (same rule as moe_experts).
+ * ---------------------------------------------------------------------- */
+size_t moe_shared_expert_workspace_size(int M, int K, int Ns);
+
+moe_status moe_shared_expert(const void* ws1, const void* ws2, int K, int Ns,
+                             const void* x, int M,
+                             void* shared_out, moe_dtype shared_dtype,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * ---------------------------------------------------------------------- */
+/* Static text for a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* Synchronizes `stream`, then returns and clears the device error word of the
+ * current device: MOE_OK, MOE_ERR_DEVICE_INDEX or MOE_ERR_DEVICE_TIMEOUT
+ * (MOE_ERR_CUDA if the synchronization itself failed). Not for the hot path. */
+moe_status moe_get_error(cudaStream_t stream);
+
+/* MOE_OK if the current device has compute capability 10.3. */
+moe_status moe_device_check(void);
+
+/* The float32 sigmoid spec the sigmoid router selects with, applied to
+ * x f32 [n] -> y f32 [n] (a test hook: the CPU oracle implements the same
+ * written spec independently, and the two must agree bit for bit). */
+moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

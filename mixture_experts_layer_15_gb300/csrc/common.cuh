@@ -1,0 +1,108 @@
+// Device helpers shared by the kernels of the MoE library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// ---- device error word -------------------------------------------------------
+// Kernels never trap: a detected problem records its status code here (first
+// writer wins) and the kernel skips the offending item.
+__device__ __forceinline__ void set_error(int* err, int code) {
+    if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// ---- dtype helpers -------------------------------------------------------------
+__device__ __forceinline__ float load_as_f32(const void* p, size_t i, int dtype) {
+    if (dtype == MOE_DTYPE_F32) return static_cast<const float*>(p)[i];
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+__device__ __forceinline__ void store_from_f32(void* p, size_t i, float v, int dtype) {
+    if (dtype == MOE_DTYPE_F32) static_cast<float*>(p)[i] = v;
+    else static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// 8 consecutive elements as float (16-byte aligned source for bf16, 32 for f32).
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
+        float4 a = reinterpret_cast<const float4*>(p)[0];
+        float4 b = reinterpret_cast<const float4*>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float (&v)[8]) {
+        reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+};
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Block-wide in-place exclusive scan of data[0..n); returns the total.
+// `tmp` holds >= 33 ints. Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* tmp) {
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int per = (n + nt - 1) / nt;
+    const int b = tid * per, e = min(n, b + per);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += data[i];
+    // inclusive warp scan of the per-thread sums
+    const int lane = tid & 31, warp = tid >> 5;
+    int v = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+    }
+    if (lane == 31) tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += u;
+        }
+        if (lane < nw) tmp[lane] = w;            // inclusive warp totals
+        if (lane == 31) tmp[32] = w;             // block total
+    }
+    __syncthreads();
+    int run = v - local + (warp > 0 ? tmp[warp - 1] : 0);
+    for (int i = b; i < e; ++i) {
+        const int d = data[i];
+        data[i] = run;
+        run += d;
+    }
+    const int total = tmp[32];
+    __syncthreads();
+    return total;
+}
+
+
+}  // namespace moe

@@ -1,0 +1,352 @@
+// C ABI of the MoE layer forward (declared in include/moe.h): argument
+// validation on the host, then the launchers of the kernel translation units.
+//
+// Validation mirrors the checks of vllm/model_executor/layers/fused_moe/
+// moe_output.py, convert_flashinfer_moe_output (num_tokens >= 0, top_k > 0,
+// a finalized result goes to the given destination, a deferred result has
+// none, the permute map is int32, contiguous buffers) and the arch allowlist
+// of vllm/utils/flashinfer_moe_ep.py, validate_fi_moe_ep_config. Every check
+// runs before anything is enqueued; no call allocates or synchronizes (except
+// moe_get_error, which is documented to).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+__device__ int g_error_word;     // first device-detected error since the last moe_get_error
+
+constexpr int kMaxDevices = 64;
+struct DevSlot {
+    std::once_flag once;
+    bool ok = false;
+    DeviceInfo info;
+    int* err = nullptr;
+};
+DevSlot g_dev[kMaxDevices];
+
+DevSlot* current_slot() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    DevSlot* s = &g_dev[d];
+    std::call_once(s->once, [s, d] {
+        DeviceInfo i;
+        if (cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return;
+        cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, d);
+        cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
+        cudaDeviceGetAttribute(&i.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return;
+        s->info = i;
+        s->err = static_cast<int*>(p);
+        s->ok = true;
+    });
+    cudaGetLastError();   // clear any sticky-free error left by the queries
+    return s->ok ? s : nullptr;
+}
+}  // namespace
+
+bool current_device_info(DeviceInfo* info) {
+    DevSlot* s = current_slot();
+    if (!s) return false;
+    *info = s->info;
+    return true;
+}
+
+int* device_error_word() {
+    DevSlot* s = current_slot();
+    return s ? s->err : nullptr;
+}
+
+}  // namespace moe
+
+using moe::DeviceInfo;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool valid_dtype(int d) { return d == MOE_DTYPE_BF16 || d == MOE_DTYPE_F32; }
+
+// Device gate: a cc 10.3 device must be current.
+moe_status device_gate(DeviceInfo* info, int** err) {
+    if (!moe::current_device_info(info)) return MOE_ERR_CUDA;
+    if (info->cc_major != 10 || info->cc_minor != 3) return MOE_ERR_UNSUPPORTED_ARCH;
+    *err = moe::device_error_word();
+    return MOE_OK;
+}
+
+inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_weights(const moe_weights* w) {
+    if (w == nullptr || w->w1 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
+    if (w->E_local < 1 || w->E_local > 1024 || w->K <= 0 || w->N <= 0) return MOE_ERR_INVALID_ARG;
+    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (w->K % 128 != 0 || w->N % 128 != 0) return MOE_ERR_ALIGNMENT;
+    if (!aligned16(w->w1) || !aligned16(w->w2)) return MOE_ERR_ALIGNMENT;
+    if (w->format == MOE_WEIGHTS_MXFP4) {
+        if (w->w1_scale == nullptr || w->w2_scale == nullptr) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(w->w1_scale) || !aligned16(w->w2_scale)) return MOE_ERR_ALIGNMENT;
+    } else if (w->w1_scale != nullptr || w->w2_scale != nullptr) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    // the largest row index a TMA coordinate can address is 2^31 - 1
+    if (static_cast<long long>(w->E_local) * 2 * w->N >= (1LL << 31) ||
+        static_cast<long long>(w->E_local) * w->K >= (1LL << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// Shared checks of the finalize arguments (moe_finalize and moe_experts with
+// do_finalize = 1).
+moe_status check_finalize_args(const void* weights, int wdtype, const int32_t* map, const void* shared,
+                               int sdtype, void* out, int odtype) {
+    if (weights == nullptr || map == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!valid_dtype(wdtype) || !valid_dtype(odtype)) return MOE_ERR_INVALID_ARG;
+    if (shared != nullptr && !valid_dtype(sdtype)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out) || (shared != nullptr && !aligned16(shared))) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_ALIGNMENT: return "size or pointer alignment";
+        case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+        case MOE_ERR_UNSUPPORTED_ARCH: return "device is not compute capability 10.3";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_INDEX: return "device: expert id or map entry out of range";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device: pipeline wait exceeded its limit";
+        default: return "unknown status";
+    }
+}
+
+moe_status moe_device_check(void) {
+    DeviceInfo info;
+    int* err = nullptr;
+    return device_gate(&info, &err);
+}
+
+moe_status moe_get_error(cudaStream_t stream) {
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return static_cast<moe_status>(v);
+}
+
+moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream) {
+    if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_debug_sigmoid(x, y, n, stream));
+}
+
+moe_status moe_route(const float* logits, int M, int E, int top_k, moe_route_method method,
+                     const float* score_bias, int n_group, int topk_group, float routed_scaling_factor,
+                     int32_t* topk_ids, void* topk_weights, moe_dtype weights_dtype, cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;                               // num_tokens >= 0
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;                          // top_k > 0
+    if (E < 1 || E > 1024 || top_k > E || top_k > 32) return MOE_ERR_INVALID_ARG;
+    if (!valid_dtype(weights_dtype)) return MOE_ERR_INVALID_ARG;
+    if (method == MOE_ROUTE_SOFTMAX_TOPK) {
+        if (score_bias != nullptr) return MOE_ERR_INVALID_ARG;
+    } else if (method == MOE_ROUTE_SIGMOID_GROUPED_TOPK) {
+        if (score_bias == nullptr) return MOE_ERR_INVALID_ARG;
+        if (n_group < 1 || n_group > 32 || E % n_group != 0 || E / n_group < 2) return MOE_ERR_INVALID_ARG;
+        if (topk_group < 1 || topk_group > n_group) return MOE_ERR_INVALID_ARG;
+        if (top_k > topk_group * (E / n_group)) return MOE_ERR_INVALID_ARG;
+    } else {
+        return MOE_ERR_INVALID_ARG;
+    }
+    if (M == 0) return MOE_OK;
+    if (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr) return MOE_ERR_INVALID_ARG;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_route(logits, M, E, top_k, method, score_bias, n_group, topk_group,
+                                       routed_scaling_factor, topk_ids, topk_weights, weights_dtype, err,
+                                       stream));
+}
+
+size_t moe_permute_workspace_size(int M, int top_k, int E_local) {
+    if (M <= 0 || top_k <= 0 || E_local <= 0) return 0;
+    return moe::permute_workspace_bytes(M, top_k, E_local);
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E, const int32_t* expert_map,
+                       int E_local, const void* x, int K, int32_t* expert_offsets,
+                       int32_t* expanded_idx_to_permuted_idx, int32_t* permuted_to_expanded, void* x_perm,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0 || top_k <= 0 || E < 1 || E_local < 1 || E_local > 1024 || top_k > E) return MOE_ERR_INVALID_ARG;
+    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (x_perm != nullptr) {
+        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
+        if (K % 8 != 0 || !aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+    }
+    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (M > 0 && (topk_ids == nullptr || expanded_idx_to_permuted_idx == nullptr ||
+                  permuted_to_expanded == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    const size_t need = moe::permute_workspace_bytes(M > 0 ? M : 1, top_k, E_local);
+    if (M > 0 && need > 0 && (workspace == nullptr || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    if (M == 0) {
+        // no routes: every expert is empty
+        return from_cuda(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E_local + 1), stream));
+    }
+    return from_cuda(moe::launch_permute(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                                         expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm,
+                                         workspace, err, info, stream));
+}
+
+size_t moe_experts_workspace_size(const moe_weights* w, int M, int top_k) {
+    if (check_weights(w) != MOE_OK || M < 0 || top_k <= 0) return 0;
+    DeviceInfo info;
+    if (!moe::current_device_info(&info)) info.sm_count = 152;
+    const int rows = M * top_k > 0 ? M * top_k : 1;
+    return moe::experts_workspace_bytes(w, rows, M > 0 ? M : 1, info);
+}
+
+moe_status moe_finalize(const void* gemm2_permuted, moe_dtype gemm2_dtype, int num_permuted_rows,
+                        const void* expert_weights, moe_dtype weights_dtype,
+                        const int32_t* expanded_idx_to_permuted_idx, int M, int top_k, int K,
+                        const void* shared_out, moe_dtype shared_dtype, float routed_scaling_factor, void* out,
+                        moe_dtype out_dtype, cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    if (K <= 0 || num_permuted_rows < 0 || !valid_dtype(gemm2_dtype)) return MOE_ERR_INVALID_ARG;
+    if (M == 0) return MOE_OK;
+    if (K % 8 != 0) return MOE_ERR_ALIGNMENT;
+    const moe_status a = check_finalize_args(expert_weights, weights_dtype, expanded_idx_to_permuted_idx,
+                                             shared_out, shared_dtype, out, out_dtype);
+    if (a != MOE_OK) return a;
+    if (num_permuted_rows > 0 && gemm2_permuted == nullptr) return MOE_ERR_INVALID_ARG;
+    if (gemm2_permuted != nullptr && !aligned16(gemm2_permuted)) return MOE_ERR_ALIGNMENT;
+    if (out == gemm2_permuted || out == shared_out || out == expert_weights) return MOE_ERR_INVALID_ARG;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_finalize(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights,
+                                          weights_dtype, expanded_idx_to_permuted_idx, M, top_k, K, shared_out,
+                                          shared_dtype, routed_scaling_factor, out, out_dtype, err, stream));
+}
+
+moe_status moe_experts(const moe_weights* w, const void* x_perm, const int32_t* expert_offsets, int M,
+                       int top_k, void* gemm2_permuted, moe_dtype gemm2_dtype, int do_finalize,
+                       const void* expert_weights, moe_dtype weights_dtype,
+                       const int32_t* expanded_idx_to_permuted_idx, const void* shared_out,
+                       moe_dtype shared_dtype, float routed_scaling_factor, void* out, moe_dtype out_dtype,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    const moe_status ws_ok = check_weights(w);
+    if (ws_ok != MOE_OK) return ws_ok;
+    if (do_finalize != 0 && do_finalize != 1) return MOE_ERR_INVALID_ARG;
+    if (!do_finalize && out != nullptr) return MOE_ERR_INVALID_ARG;     // a deferred output has no destination
+    if (!valid_dtype(gemm2_dtype)) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (do_finalize) {
+        const moe_status a = check_finalize_args(expert_weights, weights_dtype, expanded_idx_to_permuted_idx,
+                                                 shared_out, shared_dtype, out, out_dtype);
+        if (a != MOE_OK) return a;
+        if (out == gemm2_permuted || out == shared_out || out == expert_weights) return MOE_ERR_INVALID_ARG;
+    }
+    if (M == 0) return MOE_OK;                                          // nothing arrives: empty output
+    if (x_perm == nullptr || expert_offsets == nullptr || gemm2_permuted == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(gemm2_permuted)) return MOE_ERR_ALIGNMENT;
+    if (w->format != MOE_WEIGHTS_BF16) return MOE_ERR_UNSUPPORTED;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    const int rows = M * top_k;
+    const size_t need = moe::experts_workspace_bytes(w, rows, M, info);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    moe::ExpertsProblem p;
+    p.w = w;
+    p.x = x_perm;
+    p.rows_alloc = rows;
+    p.M = M;
+    p.offsets = expert_offsets;
+    p.single_rows = 0;
+    p.y = gemm2_permuted;
+    p.y_dtype = gemm2_dtype;
+    cudaError_t e = moe::launch_experts(p, workspace, workspace_bytes, err, info, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (!do_finalize) return MOE_OK;
+    return from_cuda(moe::launch_finalize(gemm2_permuted, gemm2_dtype, rows, expert_weights, weights_dtype,
+                                          expanded_idx_to_permuted_idx, M, top_k, w->K, shared_out,
+                                          shared_dtype, routed_scaling_factor, out, out_dtype, err, stream));
+}
+
+size_t moe_shared_expert_workspace_size(int M, int K, int Ns) {
+    if (M <= 0 || K <= 0 || Ns <= 0 || K % 128 != 0 || Ns % 128 != 0) return 0;
+    moe_weights w{};
+    w.format = MOE_WEIGHTS_BF16;
+    w.E_local = 1;
+    w.K = K;
+    w.N = Ns;
+    DeviceInfo info;
+    if (!moe::current_device_info(&info)) info.sm_count = 152;
+    return moe::experts_workspace_bytes(&w, M, M, info);
+}
+
+moe_status moe_shared_expert(const void* ws1, const void* ws2, int K, int Ns, const void* x, int M,
+                             void* shared_out, moe_dtype shared_dtype, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    if (M < 0 || K <= 0 || Ns <= 0 || !valid_dtype(shared_dtype)) return MOE_ERR_INVALID_ARG;
+    if (K % 128 != 0 || Ns % 128 != 0) return MOE_ERR_ALIGNMENT;
+    if (M == 0) return MOE_OK;
+    if (ws1 == nullptr || ws2 == nullptr || x == nullptr || shared_out == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws1) || !aligned16(ws2) || !aligned16(x) || !aligned16(shared_out)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    moe_weights w{};
+    w.format = MOE_WEIGHTS_BF16;
+    w.E_local = 1;
+    w.K = K;
+    w.N = Ns;
+    w.w1 = ws1;
+    w.w2 = ws2;
+    const size_t need = moe::experts_workspace_bytes(&w, M, M, info);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    moe::ExpertsProblem p;
+    p.w = &w;
+    p.x = x;
+    p.rows_alloc = M;
+    p.M = M;
+    p.offsets = nullptr;
+    p.single_rows = M;
+    p.y = shared_out;
+    p.y_dtype = shared_dtype;
+    return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Internal host-side interfaces between the C ABI (moe_abi.cu) and the kernel
+// translation units. Arguments are validated by the ABI layer before any of
+// these is called; launchers only configure and enqueue.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int max_smem_optin = 0;
+};
+
+// Cached properties of the current device; returns false if there is none.
+bool current_device_info(DeviceInfo* info);
+
+// Address (device pointer) of the current device's error word.
+int* device_error_word();
+
+// ---- router (router.cu) --------------------------------------------------------
+cudaError_t launch_route(const float* logits, int M, int E, int top_k, int method,
+                         const float* score_bias, int n_group, int topk_group, float rsf,
+                         int32_t* topk_ids, void* topk_weights, int weights_dtype,
+                         int* err, cudaStream_t stream);
+cudaError_t launch_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream);
+
+// ---- permute (permute.cu) ------------------------------------------------------
+size_t permute_workspace_bytes(int M, int top_k, int E_local);
+cudaError_t launch_permute(const int32_t* topk_ids, int M, int top_k, int E,
+                           const int32_t* expert_map, int E_local, const void* x, int K,
+                           int32_t* expert_offsets, int32_t* map, int32_t* inverse,
+                           void* x_perm, void* workspace, int* err, const DeviceInfo& dev,
+                           cudaStream_t stream);
+
+// ---- finalize (finalize.cu) ----------------------------------------------------
+cudaError_t launch_finalize(const void* gemm2, int gemm2_dtype, int num_rows,
+                            const void* weights, int weights_dtype, const int32_t* map,
+                            int M, int top_k, int K, const void* shared, int shared_dtype,
+                            float rsf, void* out, int out_dtype, int* err, cudaStream_t stream);
+
+// ---- grouped expert GEMMs (gemm.cu) --------------------------------------------
+// One grouped "gated MLP" problem: E groups of rows of `x` (bf16 [rows_alloc, K]),
+// group g = rows [offsets[g], offsets[g+1]) (or one group of `single_rows`
+// rows when offsets == nullptr), weights per group W1 [2N, K], W2 [K, N].
+struct ExpertsProblem {
+    const moe_weights* w;
+    const void* x;
+    int rows_alloc;              // rows allocated in x / act / y (M * top_k)
+    int M;                       // tokens (bounds the rows one group can have)
+    const int32_t* offsets;      // [E+1] device, or nullptr
+    int single_rows;             // rows of the single group when offsets == nullptr
+    void* y;                     // [rows_alloc, K] output (bf16 or f32)
+    int y_dtype;
+};
+
+size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev);
+cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t workspace_bytes,
+                           int* err, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace moe

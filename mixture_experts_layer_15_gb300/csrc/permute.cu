@@ -1,0 +1,243 @@
+// Permute: group the M*top_k routes by local expert and build the permute map
+// expanded_idx_to_permuted_idx (-1 = expert not local) of
+// vllm/model_executor/layers/fused_moe/moe_output.py, UnfinalizedMoEOutput,
+// plus the per-expert offsets (the "expert_num_tokens" of modular_kernel.py,
+// FusedMoEPrepareAndFinalize.prepare), the inverse map and the row gather
+// x_perm[p] = x[token of row p].
+//
+// The order is canonical: expert-major, then expanded index t*top_k + j. It is
+// a stable counting sort. Routes are cut into chunks of 32*W (one route per
+// thread, warp w owns 32 consecutive routes). Inside a warp, __match_any_sync
+// gives each route its rank among the warp's routes to the same expert; a
+// per-warp histogram and an exclusive scan over warps give the rank inside
+// the chunk; an exclusive scan over chunks (per expert) and over experts
+// gives the global row. No atomics decide an order, so the result is
+// deterministic.
+//
+// One chunk (M*top_k <= 32*W): a single kernel; every CTA recomputes the tiny
+// sort in shared memory and copies its share of the rows.
+// Several chunks: count -> scan -> scatter -> gather (4 launches).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// Warps per chunk: per-warp histograms are W x E_local ints in shared memory;
+// keep them within 32 KB.
+__host__ __device__ inline int warps_per_chunk(int E_local) {
+    int w = 8192 / (E_local > 0 ? E_local : 1);
+    return w < 1 ? 1 : (w > 32 ? 32 : w);
+}
+
+__device__ __forceinline__ int local_expert(const int32_t* __restrict__ ids,
+                                            const int32_t* __restrict__ emap,
+                                            int i, int n, int E, int E_l, int* err) {
+    if (i >= n) return -2;                 // padding lane: in no group
+    const int id = __ldg(ids + i);
+    if (id < 0 || id >= E) { set_error(err, MOE_ERR_DEVICE_INDEX); return -1; }
+    if (emap == nullptr) return id;
+    const int le = __ldg(emap + id);
+    if (le < -1 || le >= E_l) { set_error(err, MOE_ERR_DEVICE_INDEX); return -1; }
+    return le;
+}
+
+// Per-warp histograms of one chunk -> exclusive scan over warps, in place.
+// hist is [W][E_l]; on return hist[w][le] = routes to le in warps < w, and
+// chunk_total[le] = routes to le in the whole chunk. Also returns, per
+// thread, the route's local expert and its rank within its warp.
+__device__ void chunk_ranks(const int32_t* ids, const int32_t* emap, int chunk_base, int n,
+                            int E, int E_l, int* hist, int* chunk_total, int* err,
+                            int& le, int& rank) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, W = blockDim.x >> 5;
+    for (int i = tid; i < W * E_l; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    le = local_expert(ids, emap, chunk_base + tid, n, E, E_l, err);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    rank = __popc(peers & ((1u << lane) - 1u));
+    if (rank == 0 && le >= 0) hist[warp * E_l + le] = __popc(peers);
+    __syncthreads();
+    for (int e = tid; e < E_l; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            const int c = hist[w * E_l + e];
+            hist[w * E_l + e] = run;
+            run += c;
+        }
+        chunk_total[e] = run;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                         int n16, int lane) {
+    int c = lane;
+    for (; c + 96 < n16; c += 128) {
+        const uint4 a = __ldg(src + c), b = __ldg(src + c + 32);
+        const uint4 d = __ldg(src + c + 64), e = __ldg(src + c + 96);
+        dst[c] = a; dst[c + 32] = b; dst[c + 64] = d; dst[c + 96] = e;
+    }
+    for (; c < n16; c += 32) dst[c] = __ldg(src + c);
+}
+
+// ---- single chunk: one kernel ------------------------------------------------
+__global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int top_k, int E,
+                                     const int32_t* __restrict__ emap, int E_l,
+                                     const __nv_bfloat16* __restrict__ x, int K,
+                                     int32_t* __restrict__ offsets, int32_t* __restrict__ map,
+                                     int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
+                                     int* err) {
+    extern __shared__ int sm[];
+    const int W = blockDim.x >> 5;
+    int* hist = sm;                          // [W][E_l]
+    int* total = hist + W * E_l;             // [E_l + 1]
+    int* pos = total + E_l + 1;              // [32 W] permuted row of each route
+    int* tmp = pos + blockDim.x;             // [33]
+    int le, rank;
+    // Only CTA 0 reports device errors (all CTAs see the same ids).
+    chunk_ranks(ids, emap, 0, n, E, E_l, hist, total, blockIdx.x == 0 ? err : nullptr, le, rank);
+    const int R = block_exclusive_scan(total, E_l, tmp);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int p = le >= 0 ? total[le] + hist[warp * E_l + le] + rank : -1;
+    pos[tid] = p;
+    if (blockIdx.x == 0) {
+        for (int e = tid; e < E_l; e += blockDim.x) offsets[e] = total[e];
+        if (tid == 0) offsets[E_l] = R;
+        if (tid < n) {
+            map[tid] = p;
+            if (p >= 0) inverse[p] = tid;
+        }
+    }
+    if (x_perm == nullptr) return;
+    __syncthreads();
+    // rows: route i (< n, local) is copied by global warp i % (grid * W)
+    const int gw = blockIdx.x * W + warp, nw = gridDim.x * W, n16 = K / 8;
+    for (int i = gw; i < n; i += nw) {
+        const int pi = pos[i];
+        if (pi < 0) continue;
+        copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(i / top_k) * K),
+                 reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(pi) * K), n16, tid & 31);
+    }
+}
+
+// ---- several chunks ------------------------------------------------------------
+__global__ void permute_count_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                     const int32_t* __restrict__ emap, int E_l,
+                                     int32_t* __restrict__ chunk_counts, int* err) {
+    extern __shared__ int sm[];
+    const int W = blockDim.x >> 5;
+    int* hist = sm;
+    int* total = hist + W * E_l;
+    int le, rank;
+    chunk_ranks(ids, emap, blockIdx.x * blockDim.x, n, E, E_l, hist, total, err, le, rank);
+    for (int e = threadIdx.x; e < E_l; e += blockDim.x)
+        chunk_counts[static_cast<size_t>(blockIdx.x) * E_l + e] = total[e];
+}
+
+// chunk_counts[c][e] -> global first row of (chunk c, expert e); offsets.
+__global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E_l,
+                                    int32_t* __restrict__ offsets) {
+    extern __shared__ int sm[];
+    int* total = sm;                         // [E_l]
+    int* tmp = total + E_l;                  // [33]
+    for (int e = threadIdx.x; e < E_l; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const size_t o = static_cast<size_t>(c) * E_l + e;
+            const int v = chunk_counts[o];
+            chunk_counts[o] = run;
+            run += v;
+        }
+        total[e] = run;
+    }
+    __syncthreads();
+    const int R = block_exclusive_scan(total, E_l, tmp);
+    for (int e = threadIdx.x; e < E_l; e += blockDim.x) {
+        const int base = total[e];
+        offsets[e] = base;
+        for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<size_t>(c) * E_l + e] += base;
+    }
+    if (threadIdx.x == 0) offsets[E_l] = R;
+}
+
+__global__ void permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                       const int32_t* __restrict__ emap, int E_l,
+                                       const int32_t* __restrict__ chunk_base,
+                                       int32_t* __restrict__ map, int32_t* __restrict__ inverse) {
+    extern __shared__ int sm[];
+    const int W = blockDim.x >> 5;
+    int* hist = sm;
+    int* total = hist + W * E_l;
+    int le, rank;
+    const int base = blockIdx.x * blockDim.x;
+    chunk_ranks(ids, emap, base, n, E, E_l, hist, total, nullptr, le, rank);
+    const int i = base + threadIdx.x;
+    if (i >= n) return;
+    int p = -1;
+    if (le >= 0)
+        p = chunk_base[static_cast<size_t>(blockIdx.x) * E_l + le] + hist[(threadIdx.x >> 5) * E_l + le] + rank;
+    map[i] = p;
+    if (p >= 0) inverse[p] = i;
+}
+
+// x_perm[p] = x[inverse[p] / top_k] for p < offsets[E_l]; one warp per row.
+__global__ void permute_gather_kernel(const int32_t* __restrict__ offsets, int E_l,
+                                      const int32_t* __restrict__ inverse, int top_k,
+                                      const __nv_bfloat16* __restrict__ x, int K,
+                                      __nv_bfloat16* __restrict__ x_perm) {
+    const int R = __ldg(offsets + E_l);
+    const int warps = blockDim.x >> 5;
+    const int n16 = K / 8;
+    for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < R; p += gridDim.x * warps) {
+        const int t = __ldg(inverse + p) / top_k;
+        copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * K),
+                 reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(p) * K), n16, threadIdx.x & 31);
+    }
+}
+
+}  // namespace
+
+size_t permute_workspace_bytes(int M, int top_k, int E_local) {
+    const long long n = static_cast<long long>(M) * top_k;
+    const int chunk = 32 * warps_per_chunk(E_local);
+    const long long nchunks = (n + chunk - 1) / chunk;
+    if (nchunks <= 1) return 0;
+    return static_cast<size_t>(nchunks) * E_local * sizeof(int32_t);
+}
+
+cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const int32_t* emap,
+                           int E_l, const void* x, int K, int32_t* offsets, int32_t* map,
+                           int32_t* inverse, void* x_perm, void* ws, int* err,
+                           const DeviceInfo& dev, cudaStream_t s) {
+    const int n = M * top_k;
+    const int W = warps_per_chunk(E_l);
+    const int threads = 32 * W;
+    const int nchunks = ceil_div(n, threads);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
+    if (nchunks <= 1) {
+        const size_t smem = sizeof(int) * (W * E_l + E_l + 1 + threads + 33);
+        int grid = 1;
+        if (x_perm != nullptr) {
+            // enough warps to copy every row in about one pass, at most 2 per SM
+            grid = ceil_div(n, W);
+            grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
+        }
+        permute_fused_kernel<<<grid, threads, smem, s>>>(ids, n, top_k, E, emap, E_l, xb, K,
+                                                        offsets, map, inverse, xp, err);
+        return cudaGetLastError();
+    }
+    int32_t* chunk = static_cast<int32_t*>(ws);
+    const size_t smem_h = sizeof(int) * (W * E_l + E_l);
+    permute_count_kernel<<<nchunks, threads, smem_h, s>>>(ids, n, E, emap, E_l, chunk, err);
+    permute_scan_kernel<<<1, 1024, sizeof(int) * (E_l + 33), s>>>(chunk, nchunks, E_l, offsets);
+    permute_scatter_kernel<<<nchunks, threads, smem_h, s>>>(ids, n, E, emap, E_l, chunk, map, inverse);
+    if (x_perm != nullptr) {
+        const int rows_per_block = 8;   // 256 threads, one warp per row
+        int grid = ceil_div(n, rows_per_block);
+        if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+        permute_gather_kernel<<<grid, 32 * rows_per_block, 0, s>>>(offsets, E_l, inverse, top_k, xb, K, xp);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

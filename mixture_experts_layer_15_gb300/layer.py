@@ -1,0 +1,141 @@
+"""The whole MoE layer forward as a sequence of C-ABI calls.
+
+``MoELayer`` holds device weights and reusable device buffers (allocated with
+torch, which is only the allocator and stream provider here) and runs
+moe_route -> moe_permute -> [moe_shared_expert] -> moe_experts(+finalize), the
+order of vllm/model_executor/layers/fused_moe/modular_kernel.py,
+FusedMoEModularKernel.forward with the dispatch/combine being no-ops on one
+GPU. Every arithmetic step runs in the CUDA library.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+_TORCH = {L.MOE_DTYPE_BF16: torch.bfloat16, L.MOE_DTYPE_F32: torch.float32}
+
+
+@dataclasses.dataclass
+class Buffers:
+    M: int
+    topk_ids: torch.Tensor
+    topk_weights: torch.Tensor
+    offsets: torch.Tensor
+    pmap: torch.Tensor
+    inverse: torch.Tensor
+    x_perm: torch.Tensor
+    gemm2: torch.Tensor
+    out: torch.Tensor
+    shared: Optional[torch.Tensor]
+    perm_ws: torch.Tensor
+    exp_ws: torch.Tensor
+    shared_ws: Optional[torch.Tensor]
+
+
+class MoELayer:
+    """One MoE layer on the current CUDA device.
+
+    w1/w2 (and scales) hold the E_local local experts; ``expert_map`` (int32
+    [E]) maps global expert ids to local ids (-1 = not local). Routing weights,
+    gemm2_permuted and the output are stored in the given dtypes (float32 by
+    default: see the precision notes of the C ABI).
+    """
+
+    def __init__(self, *, K, N, E, top_k, w1, w2, w1_scale=None, w2_scale=None,
+                 fmt=L.MOE_WEIGHTS_BF16, route="softmax", score_bias=None, n_group=1, topk_group=1,
+                 routed_scaling_factor=1.0, expert_map=None, E_local=None, ws1=None, ws2=None,
+                 weights_dtype=L.MOE_DTYPE_F32, gemm2_dtype=L.MOE_DTYPE_F32,
+                 out_dtype=L.MOE_DTYPE_F32):
+        self.K, self.N, self.E, self.top_k = K, N, E, top_k
+        self.E_local = E if E_local is None else E_local
+        self.w1, self.w2, self.w1_scale, self.w2_scale = w1, w2, w1_scale, w2_scale
+        self.fmt = fmt
+        self.method = (L.MOE_ROUTE_SOFTMAX_TOPK if route == "softmax"
+                       else L.MOE_ROUTE_SIGMOID_GROUPED_TOPK)
+        self.score_bias = score_bias
+        self.n_group, self.topk_group = n_group, topk_group
+        self.rsf = float(routed_scaling_factor)
+        self.expert_map = expert_map
+        self.ws1, self.ws2 = ws1, ws2
+        self.Ns = 0 if ws1 is None else ws1.shape[0] // 2
+        self.weights_dtype, self.gemm2_dtype, self.out_dtype = weights_dtype, gemm2_dtype, out_dtype
+        self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale)
+        self._bufs = {}
+
+    def buffers(self, M: int) -> Buffers:
+        b = self._bufs.get(M)
+        if b is not None:
+            return b
+        dev = self.w1.device
+        R = max(M * self.top_k, 1)
+        i32 = dict(dtype=torch.int32, device=dev)
+        pws = L.moe_permute_workspace_size(M, self.top_k, self.E_local)
+        ews = L.moe_experts_workspace_size(self.cw, M, self.top_k)
+        shared = shared_ws = None
+        if self.ws1 is not None:
+            shared = torch.empty(M, self.K, dtype=_TORCH[self.gemm2_dtype], device=dev)
+            sws = L.moe_shared_expert_workspace_size(M, self.K, self.Ns)
+            shared_ws = torch.zeros(max(sws, 16), dtype=torch.uint8, device=dev)
+        b = Buffers(
+            M=M,
+            topk_ids=torch.empty(M, self.top_k, **i32),
+            topk_weights=torch.empty(M, self.top_k, dtype=_TORCH[self.weights_dtype], device=dev),
+            offsets=torch.empty(self.E_local + 1, **i32),
+            pmap=torch.empty(M, self.top_k, **i32),
+            inverse=torch.empty(R, **i32),
+            x_perm=torch.empty(R, self.K, dtype=torch.bfloat16, device=dev),
+            gemm2=torch.empty(R, self.K, dtype=_TORCH[self.gemm2_dtype], device=dev),
+            out=torch.empty(M, self.K, dtype=_TORCH[self.out_dtype], device=dev),
+            shared=shared,
+            perm_ws=torch.empty(max(pws, 16), dtype=torch.uint8, device=dev),
+            # zero-filled once: the split-K counters in it start at zero
+            exp_ws=torch.zeros(max(ews, 16), dtype=torch.uint8, device=dev),
+            shared_ws=shared_ws,
+        )
+        self._bufs[M] = b
+        return b
+
+    def route(self, logits, b: Buffers, stream=None):
+        M = logits.shape[0]
+        L.moe_route(logits, M, self.E, self.top_k, self.method, self.score_bias, self.n_group,
+                    self.topk_group, self.rsf if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0,
+                    b.topk_ids, b.topk_weights, self.weights_dtype, stream)
+
+    def forward(self, x, logits, do_finalize=True, stream=None, topk_ids=None, topk_weights=None) -> Buffers:
+        """Run the layer on x bf16 [M, K] and logits f32 [M, E]; returns the
+        buffers (out, gemm2_permuted, map, ...). ``topk_ids``/``topk_weights``
+        skip the router and use the given routing instead."""
+        M = x.shape[0]
+        b = self.buffers(M)
+        if topk_ids is None:
+            self.route(logits, b, stream)
+            ids, wts = b.topk_ids, b.topk_weights
+        else:
+            ids, wts = topk_ids, topk_weights
+        L.moe_permute(ids, M, self.top_k, self.E, self.expert_map, self.E_local, x, self.K, b.offsets,
+                      b.pmap, b.inverse, b.x_perm, b.perm_ws, b.perm_ws.numel(), stream)
+        if self.ws1 is not None:
+            L.moe_shared_expert(self.ws1, self.ws2, self.K, self.Ns, x, M, b.shared, self.gemm2_dtype,
+                                b.shared_ws, b.shared_ws.numel(), stream)
+        # the sigmoid router folds the routed scale into its weights
+        rsf = 1.0 if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else self.rsf
+        wdt = L.MOE_DTYPE_F32 if wts.dtype == torch.float32 else L.MOE_DTYPE_BF16
+        L.moe_experts(self.cw, b.x_perm, b.offsets, M, self.top_k, b.gemm2, self.gemm2_dtype,
+                      1 if do_finalize else 0,
+                      wts if do_finalize else None, wdt, b.pmap if do_finalize else None,
+                      b.shared if do_finalize else None, self.gemm2_dtype, rsf,
+                      b.out if do_finalize else None, self.out_dtype,
+                      b.exp_ws, b.exp_ws.numel(), stream)
+        return b
+
+    def finalize(self, b: Buffers, stream=None):
+        """The deferred finalize: moe_finalize on the buffers of a forward
+        that ran with do_finalize=False."""
+        rsf = 1.0 if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else self.rsf
+        wdt = L.MOE_DTYPE_F32 if b.topk_weights.dtype == torch.float32 else L.MOE_DTYPE_BF16
+        L.moe_finalize(b.gemm2, self.gemm2_dtype, b.gemm2.shape[0], b.topk_weights, wdt, b.pmap, b.M,
+                       self.top_k, self.K, b.shared, self.gemm2_dtype, rsf, b.out, self.out_dtype, stream)

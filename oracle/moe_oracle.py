@@ -162,9 +162,9 @@ _LN2_LO = np.float32(1.4286068203094173e-06)
 _INV_FACT = [np.float32(1.0 / math.factorial(i)) for i in range(8)]   # 1/0! .. 1/7!
 
 
-def _exp_f32_spec(t: np.float32) -> np.float32:
-    """exp(t) in float32 by the written spec: every step one IEEE float32
-    operation rounded to nearest (no fused multiply-add).
+def _exp_f32_spec(t) -> np.ndarray:
+    """exp(t) in float32 by the written spec, elementwise: every step one IEEE
+    float32 operation rounded to nearest (no fused multiply-add).
 
       t > 88      -> +inf            t < -80 -> 0
       n = rint(t * LOG2E)            (float32 product, round half to even)
@@ -172,35 +172,30 @@ def _exp_f32_spec(t: np.float32) -> np.float32:
       p = ((((((c7 r + c6) r + c5) r + c4) r + c3) r + c2) r + c1) r + c0,  c_i = fl32(1/i!)
       exp = p * 2^n                  (exact: 2^n is built from its bits)
     """
-    t = np.float32(t)
-    if np.isnan(t):
-        return np.float32(np.nan)
-    if t > np.float32(88.0):
-        return np.float32(np.inf)
-    if t < np.float32(-80.0):
-        return np.float32(0.0)
-    n = np.rint(np.float32(t * _LOG2E))
-    r = np.float32(t - np.float32(n * _LN2_HI))
-    r = np.float32(r - np.float32(n * _LN2_LO))
-    p = _INV_FACT[7]
+    t = np.asarray(t, dtype=np.float32)
+    inner = (t <= np.float32(88.0)) & (t >= np.float32(-80.0))
+    ti = np.where(inner, t, np.float32(0.0)).astype(np.float32)
+    n = np.rint((ti * _LOG2E).astype(np.float32)).astype(np.float32)
+    r = (ti - (n * _LN2_HI).astype(np.float32)).astype(np.float32)
+    r = (r - (n * _LN2_LO).astype(np.float32)).astype(np.float32)
+    p = np.full_like(r, _INV_FACT[7])
     for c in reversed(_INV_FACT[:7]):
-        p = np.float32(np.float32(p * r) + c)
-    two_n = np.array([(int(n) + 127) << 23], dtype=np.uint32).view(np.float32)[0]
-    return np.float32(p * two_n)
+        p = ((p * r).astype(np.float32) + c).astype(np.float32)
+    two_n = ((n.astype(np.int32) + 127) << 23).astype(np.uint32).view(np.float32)
+    e = (p * two_n).astype(np.float32)
+    e = np.where(t > np.float32(88.0), np.float32(np.inf), e)
+    e = np.where(t < np.float32(-80.0), np.float32(0.0), e)
+    return np.where(np.isnan(t), t, e).astype(np.float32)
 
 
 def sigmoid_f32_spec(x) -> np.ndarray:
     """sigma(x) = 1 / (1 + exp(-x)) in float32 with the written exp spec; one
-    rounded float32 add and one rounded float32 divide."""
+    rounded float32 add and one rounded float32 divide (elementwise)."""
     x = np.asarray(x, dtype=np.float32)
-    out = np.empty_like(x)
-    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    e = _exp_f32_spec(-x)
     one = np.float32(1.0)
-    for i in range(flat_in.size):
-        e = _exp_f32_spec(np.float32(-flat_in[i]))
-        with np.errstate(over="ignore"):
-            flat_out[i] = np.float32(one / np.float32(one + e))
-    return out
+    with np.errstate(over="ignore"):
+        return (one / (one + e).astype(np.float32)).astype(np.float32)
 
 
 def route_sigmoid_grouped(logits: np.ndarray, score_bias: np.ndarray, top_k: int,

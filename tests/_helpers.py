@@ -1,0 +1,92 @@
+"""Test helpers: build/import the library, per-expert float64 views of device
+weights for the oracle, and the oracle's output on a sample of tokens."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+
+
+def lib():
+    from mixture_experts_layer_15_gb300 import build
+    build.build()
+    import mixture_experts_layer_15_gb300 as m
+    return m
+
+
+def tol(ref, rel=1e-2, abs_=1e-3):
+    """The value bar: max |gpu - ref| <= rel * RMS(ref) + abs."""
+    rms = float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2)))
+    return rel * rms + abs_
+
+
+def max_err(got, ref):
+    return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))))
+
+
+class ExpertsF64:
+    """``[e]`` -> float64 numpy weights of local expert e, converted lazily
+    (bf16 tensors, or MXFP4 bytes dequantised by the oracle)."""
+
+    def __init__(self, w, scale=None):
+        self.w, self.scale = w, scale
+
+    def __len__(self):
+        return self.w.shape[0]
+
+    def __getitem__(self, e):
+        if self.scale is None:
+            return self.w[e].to(torch.float64).cpu().numpy()
+        return O.dequant_mxfp4(self.w[e].cpu().numpy(), self.scale[e].cpu().numpy())
+
+    @property
+    def shape(self):
+        s = tuple(self.w.shape)
+        return s if self.scale is None else s[:-1] + (s[-1] * 2,)
+
+
+def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None, rsf=1.0):
+    """Oracle output rows for ``tokens`` (and the expert output y of each of
+    their routes): the experts and finalize of the oracle applied to the
+    sub-problem made of those tokens' routes.
+
+    x: float64 [M, K]; ids int [M, k]; weights float64 [M, k]; w1/w2 indexable
+    per local expert; shared: float64 [M, K] or None.
+    Returns (out [T, K], y dict {(t, j): [K]}).
+    """
+    tokens = list(tokens)
+    k = ids.shape[1]
+    emap = None if expert_map is None else np.asarray(expert_map)
+    sub_ids = ids[tokens]
+    local = sub_ids if emap is None else emap[sub_ids]
+    by_expert = {}
+    for a, t in enumerate(tokens):
+        for j in range(k):
+            le = int(local[a, j])
+            if le >= 0:
+                by_expert.setdefault(le, []).append((a, j))
+    ys = {}
+    for le, routes in by_expert.items():
+        xt = x[[tokens[a] for a, _ in routes]]
+        y = O.expert_mlp(xt, w1[le], w2[le])
+        for r, (a, j) in enumerate(routes):
+            ys[(a, j)] = y[r]
+    # sub-problem gemm2 rows and map, then the oracle's finalize
+    rows, pmap = [], np.full((len(tokens), k), -1, np.int32)
+    for (a, j), y in ys.items():
+        pmap[a, j] = len(rows)
+        rows.append(y)
+    K = x.shape[1]
+    g2 = np.stack(rows) if rows else np.zeros((0, K))
+    sh = None if shared is None else shared[tokens]
+    out = O.finalize(g2, weights[tokens], pmap, sh, rsf)
+    return out, {(tokens[a], j): y for (a, j), y in ys.items()}
+
+
+def sample_tokens(M, n=256, seed=0):
+    if M <= n:
+        return list(range(M))
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(M, size=n - 2, replace=False).tolist()) | {0, M - 1}
+    return sorted(s)

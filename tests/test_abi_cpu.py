@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and its
+host-side validation rejects bad arguments before touching a device. CPU only:
+no call here reaches a kernel launch."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_15_gb300 import build
+    build.build()
+    import mixture_experts_layer_15_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("moe_route", "moe_permute", "moe_experts", "moe_finalize"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = _declared()
+    assert set(names) == set(moe.EXPORTS)
+    for n in names:
+        assert hasattr(moe.lib, n), n
+
+
+def test_status_strings(moe):
+    for code in range(9):
+        assert moe.status_string(code)
+    assert moe.status_string(0) == "ok"
+    assert moe.status_string(123) == "unknown status"
+
+
+def _status(fn, *a):
+    import mixture_experts_layer_15_gb300 as m
+    try:
+        fn(*a)
+        return 0
+    except m.MoEError as e:
+        return e.status
+
+
+def test_route_validation(moe):
+    P = 0x1000  # never dereferenced: validation fails first
+    S = moe.MOE_ROUTE_SOFTMAX_TOPK
+    # num_tokens must be non-negative, top_k positive (convert_flashinfer_moe_output)
+    assert _status(moe.moe_route, P, -1, 8, 2, S, None, 1, 1, 1.0, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 8, 0, S, None, 1, 1, 1.0, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 8, 9, S, None, 1, 1, 1.0, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 8, 2, S, P, 1, 1, 1.0, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 8, 2, S, None, 1, 1, 1.0, P, P, 7, 0) == moe.MOE_ERR_INVALID_ARG
+    G = moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK
+    assert _status(moe.moe_route, P, 4, 256, 8, G, None, 8, 4, 2.5, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 256, 8, G, P, 7, 4, 2.5, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 256, 8, G, P, 8, 9, 2.5, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_route, P, 4, 16, 9, G, P, 8, 4, 2.5, P, P, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    # M = 0 is a valid no-op that needs no device
+    assert _status(moe.moe_route, None, 0, 8, 2, S, None, 1, 1, 1.0, None, None, 1, 0) == 0
+
+
+def _weights(moe, K=256, N=256, E=8, fmt=0, scales=False):
+    P = 0x1000
+    return moe.make_weights(fmt, E, K, N, P, P, P if scales else None, P if scales else None)
+
+
+def test_experts_validation(moe):
+    P = 0x1000
+    w = _weights(moe)
+    B, F = moe.MOE_DTYPE_BF16, moe.MOE_DTYPE_F32
+    call = lambda w, M, k, fin, out, **kw: _status(
+        moe.moe_experts, w, P, P, M, k, P, F, fin, P, F, P, None, F, 1.0, out, F, P, 1 << 30, 0)
+    # a deferred output cannot have a destination (convert_flashinfer_moe_output)
+    O = P + 4096
+    assert call(w, 4, 2, 0, O) == moe.MOE_ERR_INVALID_ARG
+    assert call(w, -1, 2, 1, O) == moe.MOE_ERR_INVALID_ARG
+    assert call(w, 4, 0, 1, O) == moe.MOE_ERR_INVALID_ARG
+    assert call(w, 4, 2, 2, O) == moe.MOE_ERR_INVALID_ARG
+    assert call(_weights(moe, K=200), 4, 2, 1, O) == moe.MOE_ERR_ALIGNMENT
+    assert call(_weights(moe, N=192), 4, 2, 1, O) == moe.MOE_ERR_ALIGNMENT
+    assert call(_weights(moe, E=0), 4, 2, 1, O) == moe.MOE_ERR_INVALID_ARG
+    assert call(_weights(moe, fmt=1), 4, 2, 1, O) == moe.MOE_ERR_INVALID_ARG      # MXFP4 needs scales
+    assert call(_weights(moe, scales=True), 4, 2, 1, O) == moe.MOE_ERR_INVALID_ARG  # bf16 takes none
+    # finalized output to its own destination only: out may not alias gemm2
+    assert _status(moe.moe_experts, w, P, P, 4, 2, P, F, 1, P + 64, F, P + 128, None, F, 1.0, P, F,
+                   P, 1 << 30, 0) == moe.MOE_ERR_INVALID_ARG
+    # M = 0: nothing arrives, nothing to do
+    assert call(w, 0, 2, 1, P + 4096) == 0
+    assert call(w, 0, 2, 0, None) == 0
+
+
+def test_finalize_and_permute_validation(moe):
+    P = 0x1000
+    F = moe.MOE_DTYPE_F32
+    fin = lambda M, k, K, out, g2=P: _status(moe.moe_finalize, g2, F, 8, P, F, P, M, k, K, None, F, 1.0,
+                                            out, F, 0)
+    assert fin(-1, 2, 128, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert fin(4, 0, 128, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert fin(4, 2, 100, P + 4096) == moe.MOE_ERR_ALIGNMENT
+    assert fin(4, 2, 128, None) == moe.MOE_ERR_INVALID_ARG
+    assert fin(4, 2, 128, P) == moe.MOE_ERR_INVALID_ARG          # out aliases gemm2_permuted
+    assert fin(0, 2, 128, None) == 0
+    perm = lambda M, k, E, emap, El: _status(moe.moe_permute, P, M, k, E, emap, El, P, 128, P, P, P, P,
+                                             P, 1 << 20, 0)
+    assert perm(-1, 2, 8, None, 8) == moe.MOE_ERR_INVALID_ARG
+    assert perm(4, 0, 8, None, 8) == moe.MOE_ERR_INVALID_ARG
+    assert perm(4, 2, 8, None, 4) == moe.MOE_ERR_INVALID_ARG     # no map: E_local must be E
+    assert perm(4, 9, 8, None, 8) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_host_computable(moe):
+    w = moe.make_weights(0, 8, 4096, 14336, 0x1000, 0x1000)
+    small = moe.moe_experts_workspace_size(w, 1, 2)
+    big = moe.moe_experts_workspace_size(w, 8192, 2)
+    assert small > 0 and big > 8192 * 2 * 14336 * 2      # holds the bf16 activations
+    assert moe.moe_permute_workspace_size(16, 2, 8) == 0     # one chunk: no scratch
+    assert moe.moe_permute_workspace_size(8192, 8, 128) > 0
+    assert moe.moe_shared_expert_workspace_size(64, 7168, 2048) > 64 * 2048 * 2

@@ -1,0 +1,351 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer results (routing ids, permute map, offsets, inverse map, the gathered
+rows) must match bit for bit; values must satisfy
+    max |gpu - oracle| <= 1e-2 * RMS(oracle) + 1e-3
+with routing weights, gemm2_permuted and the output stored as float32 (the
+bf16-activation pipeline: bf16 x, weights and act, fp32 accumulation). With
+the pages' bf16 storage of those three tensors the bar is the same plus one
+bf16 ulp of the reference value, compared with the oracle rounded to bf16
+(the stored dtype's own rounding is not an error of the computation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from _helpers import ExpertsF64, lib, max_err, oracle_tokens, sample_tokens, tol
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    m = lib()
+    assert m.moe_device_check() == 0, "needs a compute capability 10.3 device"
+    return m
+
+
+_LAYERS = {}
+
+
+def layer_inputs(name):
+    if name not in _LAYERS:
+        _LAYERS.clear()
+        torch.cuda.empty_cache()
+        _LAYERS[name] = synth.make_layer(synth.CONFIGS[name], DEV)
+    return _LAYERS[name]
+
+
+def make_layer(moe, name, li, **kw):
+    cfg = li.cfg
+    args = dict(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
+                w1_scale=li.w1_scale, w2_scale=li.w2_scale,
+                fmt=moe.MOE_WEIGHTS_MXFP4 if cfg.weight_format == "mxfp4" else moe.MOE_WEIGHTS_BF16,
+                route="softmax" if cfg.route == "softmax" else "sigmoid",
+                score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2)
+    args.update(kw)
+    return moe.MoELayer(**args)
+
+
+def check_no_device_error(moe):
+    st = moe.moe_get_error()
+    assert st == 0, moe.status_string(st)
+
+
+# ------------------------------------------------------------------ sigmoid spec
+
+def test_sigmoid_spec_bitexact(moe):
+    x = np.concatenate([np.linspace(-100, 100, 200001),
+                        np.random.default_rng(0).standard_normal(100000) * 4,
+                        [0.0, -0.0, 88.0, -88.0, 80.0, -80.0, 87.99, -79.99]]).astype(np.float32)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.empty_like(xd)
+    moe.moe_debug_sigmoid(xd, y, x.size)
+    got = y.cpu().numpy()
+    want = O.sigmoid_f32_spec(x)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("name,M", [("tiny", 16), ("mixtral", 8192), ("qwen3", 8192), ("qwen3", 1),
+                                    ("mixtral", 3)])
+def test_router_softmax(moe, name, M):
+    cfg = synth.CONFIGS[name]
+    li = synth.make_layer(cfg, "cpu", experts=[]) if cfg.logit_bias_std else None
+    _, logits = synth.make_tokens(cfg, M, DEV, li)
+    ids = torch.empty(M, cfg.top_k, dtype=torch.int32, device=DEV)
+    for wdt, tdt in ((moe.MOE_DTYPE_F32, torch.float32), (moe.MOE_DTYPE_BF16, torch.bfloat16)):
+        w = torch.empty(M, cfg.top_k, dtype=tdt, device=DEV)
+        moe.moe_route(logits, M, cfg.E, cfg.top_k, moe.MOE_ROUTE_SOFTMAX_TOPK, None, 1, 1, 1.0, ids, w, wdt)
+        rid, rw = O.route_softmax_topk(logits.cpu().numpy(), cfg.top_k)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        got = w.float().cpu().numpy()
+        if wdt == moe.MOE_DTYPE_F32:
+            np.testing.assert_allclose(got, rw, rtol=2e-6, atol=1e-7)
+        else:
+            np.testing.assert_allclose(got, O.bf16_round(rw), rtol=2 ** -8, atol=0)
+    check_no_device_error(moe)
+
+
+@pytest.mark.parametrize("M", [1, 64, 8192])
+def test_router_sigmoid_grouped(moe, M):
+    cfg = synth.CONFIGS["deepseek"]
+    li = synth.make_layer(cfg, "cpu", experts=[])
+    _, logits = synth.make_tokens(cfg, M, DEV)
+    bias = li.score_bias.to(DEV)
+    ids = torch.empty(M, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(M, cfg.top_k, dtype=torch.float32, device=DEV)
+    moe.moe_route(logits, M, cfg.E, cfg.top_k, moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK, bias, cfg.n_group,
+                  cfg.topk_group, cfg.routed_scaling_factor, ids, w, moe.MOE_DTYPE_F32)
+    rid, rw = O.route_sigmoid_grouped(logits.cpu().numpy(), li.score_bias.numpy(), cfg.top_k, cfg.n_group,
+                                      cfg.topk_group, cfg.routed_scaling_factor)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=5e-6, atol=1e-7)
+    check_no_device_error(moe)
+
+
+def test_router_ties_lower_id_first(moe):
+    logits = torch.tensor([[0.5, 1.0, 1.0, -2.0, 1.0, 0.0, 1.0, -0.0]] * 3, device=DEV)
+    ids = torch.empty(3, 3, dtype=torch.int32, device=DEV)
+    w = torch.empty(3, 3, dtype=torch.float32, device=DEV)
+    moe.moe_route(logits, 3, 8, 3, moe.MOE_ROUTE_SOFTMAX_TOPK, None, 1, 1, 1.0, ids, w, moe.MOE_DTYPE_F32)
+    assert ids.cpu().tolist() == [[1, 2, 4]] * 3
+
+
+# ------------------------------------------------------------------ permute
+
+def _permute(moe, ids_np, E, K, emap=None, E_l=None, x=None):
+    M, k = ids_np.shape
+    E_l = E if E_l is None else E_l
+    ids = torch.from_numpy(ids_np).to(DEV)
+    if x is None:
+        x = torch.randn(M, K, device=DEV).to(torch.bfloat16)
+    offs = torch.empty(E_l + 1, dtype=torch.int32, device=DEV)
+    pmap = torch.empty(M, k, dtype=torch.int32, device=DEV)
+    inv = torch.full((max(M * k, 1),), -7, dtype=torch.int32, device=DEV)
+    xp = torch.zeros(max(M * k, 1), K, dtype=torch.bfloat16, device=DEV)
+    wsb = moe.moe_permute_workspace_size(M, k, E_l)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    em = None if emap is None else torch.from_numpy(np.asarray(emap, np.int32)).to(DEV)
+    moe.moe_permute(ids, M, k, E, em, E_l, x, K, offs, pmap, inv, xp, ws, ws.numel())
+    return x, offs.cpu().numpy(), pmap.cpu().numpy(), inv.cpu().numpy(), xp
+
+
+@pytest.mark.parametrize("name,M,masked", [("tiny", 16, False), ("mixtral", 1, False), ("mixtral", 8192, False),
+                                           ("qwen3", 8192, False), ("qwen3", 4096, True), ("qwen3", 33, True),
+                                           ("deepseek", 1024, False)])
+def test_permute_bitexact(moe, name, M, masked):
+    cfg = synth.CONFIGS[name]
+    rng = np.random.default_rng(M)
+    ids = np.stack([rng.permutation(cfg.E)[:cfg.top_k] for _ in range(M)]).astype(np.int32)
+    if name == "qwen3":    # heavy-tailed load: route with the skewed logits
+        li = synth.make_layer(cfg, "cpu", experts=[])
+        _, logits = synth.make_tokens(cfg, M, "cpu", li)
+        ids, _ = O.route_softmax_topk(logits.numpy(), cfg.top_k)
+    emap, E_l = (None, cfg.E)
+    if masked:
+        em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+        emap = em.numpy()
+    K = min(cfg.K, 1024)
+    x, offs, pmap, inv, xp = _permute(moe, ids, cfg.E, K, emap, E_l)
+    r_offs, r_map, r_inv, _ = O.permute(ids, cfg.E, emap)
+    assert np.array_equal(offs, r_offs)
+    assert np.array_equal(pmap, r_map)
+    R = int(r_offs[-1])
+    assert np.array_equal(inv[:R], r_inv)
+    tok = torch.from_numpy(r_inv.astype(np.int64) // cfg.top_k).to(DEV)
+    assert torch.equal(xp[:R], x[tok])                         # gathered rows, bitwise
+    check_no_device_error(moe)
+
+
+def test_permute_empty_and_all_masked(moe):
+    offs = torch.full((9,), 5, dtype=torch.int32, device=DEV)
+    moe.moe_permute(None, 0, 2, 8, None, 8, None, 128, offs, None, None, None, None, 0)
+    assert offs.cpu().tolist() == [0] * 9
+    ids = np.array([[0, 1], [1, 0]], np.int32)
+    x, offs, pmap, inv, xp = _permute(moe, ids, 4, 128, emap=np.array([-1, -1, 0, 1], np.int32), E_l=2)
+    assert offs.tolist() == [0, 0, 0] and (pmap == -1).all()
+
+
+def test_permute_bad_ids_set_device_error(moe):
+    ids = np.array([[0, 1], [9, 2], [3, -1]], np.int32)        # 9 and -1 are out of range for E = 8
+    _, offs, pmap, inv, _ = _permute(moe, ids, 8, 128)
+    assert moe.moe_get_error() == moe.MOE_ERR_DEVICE_INDEX
+    assert moe.moe_get_error() == 0                            # cleared by the read
+    assert pmap[1, 0] == -1 and pmap[2, 1] == -1               # skipped like non-local routes
+    assert offs[-1] == 4
+
+
+# ------------------------------------------------------------------ whole layer
+
+def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0):
+    cfg = synth.CONFIGS[name]
+    li = layer_inputs(name)
+    x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
+    kw = {}
+    emap_np = None
+    if masked:
+        em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+        emap_np = em.numpy()
+        keep = torch.from_numpy(np.nonzero(emap_np >= 0)[0]).to(DEV)
+        kw = dict(expert_map=em.to(DEV), E_local=E_l, w1=li.w1[keep].contiguous(), w2=li.w2[keep].contiguous())
+        if li.w1_scale is not None:
+            kw.update(w1_scale=li.w1_scale[keep].contiguous(), w2_scale=li.w2_scale[keep].contiguous())
+    if bf16_storage:
+        kw.update(weights_dtype=moe.MOE_DTYPE_BF16, gemm2_dtype=moe.MOE_DTYPE_BF16, out_dtype=moe.MOE_DTYPE_BF16)
+    layer = make_layer(moe, name, li, **kw)
+    b = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    check_no_device_error(moe)
+
+    # routing and permute: bit-exact over all M tokens
+    lg = logits.cpu().numpy()
+    if cfg.route == "softmax":
+        rid, rw = O.route_softmax_topk(lg, cfg.top_k)
+    else:
+        rid, rw = O.route_sigmoid_grouped(lg, li.score_bias.cpu().numpy(), cfg.top_k, cfg.n_group,
+                                          cfg.topk_group, cfg.routed_scaling_factor)
+    assert np.array_equal(b.topk_ids.cpu().numpy(), rid)
+    r_offs, r_map, r_inv, _ = O.permute(rid, cfg.E, emap_np)
+    assert np.array_equal(b.offsets.cpu().numpy(), r_offs)
+    assert np.array_equal(b.pmap.cpu().numpy(), r_map)
+
+    # values on a token sample (all tokens when M <= sample size)
+    toks = sample_tokens(M, sample or 256)
+    xs = x.to(torch.float64).cpu().numpy()
+    w1 = ExpertsF64(kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale))
+    w2 = ExpertsF64(kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale))
+    shared = None
+    if li.ws1 is not None:
+        shared = np.zeros((M, cfg.K))
+        shared[toks] = O.shared_expert(xs[toks], li.ws1.double().cpu().numpy(), li.ws2.double().cpu().numpy())
+    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared)
+    got = b.out.double().cpu().numpy()[toks]
+    g2 = b.gemm2.double().cpu().numpy()
+    rel = 3e-2 if cfg.weight_format == "mxfp4" else 1e-2
+    abs_ = 0.0 if cfg.weight_format == "mxfp4" else 1e-3
+    if bf16_storage:
+        refb = O.bf16_round(ref).astype(np.float64)
+        # one bf16 ulp of the reference value (8 significant bits)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(refb), 1e-30))) - 7)
+        bound = tol(ref, rel, abs_) + ulp
+        assert np.all(np.abs(got - refb) <= bound), float(np.max(np.abs(got - refb) - bound))
+    else:
+        t = tol(ref, rel, abs_)
+        err = max_err(got, ref)
+        assert err <= t, f"max|gpu-oracle| = {err:.4g} > {t:.4g}"
+        # each gathered expert output row (gemm2_permuted), same bar
+        ty = tol(np.stack(list(ys.values())), rel, abs_)
+        pm = b.pmap.cpu().numpy()
+        worst = max(max_err(g2[pm[t_, j]], y) for (t_, j), y in ys.items())
+        assert worst <= ty, f"gemm2_permuted row error {worst:.4g} > {ty:.4g}"
+    return layer, b, x, logits
+
+
+@pytest.mark.parametrize("M", [16, 1, 5, 300])
+def test_layer_tiny(moe, M):
+    _check_layer(moe, "tiny", M)
+
+
+def test_layer_tiny_bf16_storage(moe):
+    _check_layer(moe, "tiny", 16, bf16_storage=True)
+
+
+@pytest.mark.parametrize("M", [1, 32, 256, 2048, 8192])
+def test_layer_qwen3(moe, M):
+    _check_layer(moe, "qwen3", M, sample=256)
+
+
+@pytest.mark.parametrize("M", [1, 8, 64, 512, 4096, 8192])
+def test_layer_mixtral(moe, M):
+    _check_layer(moe, "mixtral", M, sample=128 if M > 64 else None)
+
+
+def test_masked_stress_deferred_finalize(moe):
+    """Qwen3-shaped layer at M = 4096, half the experts non-local: the deferred
+    output (gemm2_permuted + weights + map) finalized by a separate call equals
+    the fused finalize bit for bit, and both match the oracle."""
+    layer, b, x, logits = _check_layer(moe, "qwen3", 4096, sample=128, masked=True)
+    fused = b.out.clone()
+    g2_before = b.gemm2.clone()
+    b2 = layer.forward(x, logits, do_finalize=False)
+    b2.out.fill_(float("nan"))
+    layer.finalize(b2)
+    torch.cuda.synchronize()
+    R = int(b2.offsets[-1])
+    assert torch.equal(b2.gemm2[:R], g2_before[:R])                 # deterministic experts
+    assert torch.equal(b2.out, fused)                               # deferred == fused, bitwise
+    check_no_device_error(moe)
+
+
+def test_complement_mask_additivity(moe):
+    """out(map A) + out(map not A) = out(no map), with the routing fixed."""
+    cfg = synth.CONFIGS["qwen3"]
+    li = layer_inputs("qwen3")
+    M = 512
+    x, logits = synth.make_tokens(cfg, M, DEV, li)
+    full = make_layer(moe, "qwen3", li)
+    out_full = full.forward(x, logits).out.clone()
+    ids, w = full.buffers(M).topk_ids.clone(), full.buffers(M).topk_weights.clone()
+    em, E_l = synth.masked_expert_map(cfg.E, seed=5)
+    sel = em.numpy() >= 0
+    outs = []
+    for keep in (sel, ~sel):
+        emap = np.full(cfg.E, -1, np.int32)
+        emap[keep] = np.arange(keep.sum())
+        kidx = torch.from_numpy(np.nonzero(keep)[0]).to(DEV)
+        lay = make_layer(moe, "qwen3", li, expert_map=torch.from_numpy(emap).to(DEV), E_local=int(keep.sum()),
+                         w1=li.w1[kidx].contiguous(), w2=li.w2[kidx].contiguous())
+        outs.append(lay.forward(x, logits, topk_ids=ids, topk_weights=w).out.double().clone())
+    torch.cuda.synchronize()
+    s = (outs[0] + outs[1]).cpu().numpy()
+    ref = out_full.double().cpu().numpy()
+    assert max_err(s, ref) <= 1e-5 * float(np.sqrt((ref ** 2).mean())) + 1e-6
+    check_no_device_error(moe)
+
+
+def test_masked_routes_and_padding_do_not_leak(moe):
+    """NaN in the weights of -1 routes and in never-referenced gemm2 rows
+    must not reach the output."""
+    cfg = synth.CONFIGS["qwen3"]
+    li = layer_inputs("qwen3")
+    M = 64
+    x, logits = synth.make_tokens(cfg, M, DEV, li)
+    em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+    keep = torch.from_numpy(np.nonzero(em.numpy() >= 0)[0]).to(DEV)
+    lay = make_layer(moe, "qwen3", li, expert_map=em.to(DEV), E_local=E_l,
+                     w1=li.w1[keep].contiguous(), w2=li.w2[keep].contiguous())
+    b = lay.forward(x, logits, do_finalize=False)
+    lay.finalize(b)
+    torch.cuda.synchronize()
+    clean = b.out.clone()
+    R = int(b.offsets[-1])
+    b.gemm2[R:] = float("nan")
+    b.topk_weights[b.pmap < 0] = float("nan")
+    lay.finalize(b)
+    torch.cuda.synchronize()
+    assert torch.isfinite(b.out).all()
+    assert torch.equal(b.out, clean)
+
+
+def test_shared_expert(moe):
+    cfg = synth.CONFIGS["deepseek"]
+    g = torch.Generator(device=DEV).manual_seed(3)
+    M, K, Ns = 64, cfg.K, cfg.shared_N
+    ws1 = (torch.randn(2 * Ns, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    ws2 = (torch.randn(K, Ns, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=g, device=DEV).to(torch.bfloat16)
+    out = torch.empty(M, K, dtype=torch.float32, device=DEV)
+    wsb = moe.moe_shared_expert_workspace_size(M, K, Ns)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    moe.moe_shared_expert(ws1, ws2, K, Ns, x, M, out, moe.MOE_DTYPE_F32, ws, wsb)
+    torch.cuda.synchronize()
+    ref = O.shared_expert(x.double().cpu().numpy(), ws1.double().cpu().numpy(), ws2.double().cpu().numpy())
+    assert max_err(out.cpu().numpy(), ref) <= tol(ref)
+    check_no_device_error(moe)
