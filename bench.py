@@ -1,0 +1,453 @@
+"""Benchmark of the fused MoE layer forward on GB300.
+
+One step = one forward of the Mixtral-8x7B-shaped MoE layer (K=4096,
+N=14336, E=8, top_k=2, bf16 weights and activations) at each batch size of
+the sweep M in {1, 8, 64, 512, 4096, 8192}: route -> permute -> grouped
+GEMM1+silu_and_mul -> grouped GEMM2 -> finalize, all in the CUDA library.
+``value`` = tokens of all ranks / (max over ranks of the timed seconds).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixtral|qwen3|deepseek|tiny]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Multi-GPU: replicas only (each rank runs the same workload on its own GPU, no
+collective on the data path; a barrier and a max-reduce of the timing only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at M=1..8192 tokens; % of HBM / tensor-core roofline"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank, seconds_per_rank):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return sum(units_per_rank) / max(seconds_per_rank)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev=0):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{dev}.csv")
+        sel = []
+        try:
+            u = str(torch.cuda.get_device_properties(dev).uuid)
+            sel = ["-i", u if u.startswith("GPU-") else "GPU-" + u]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = [l.strip().split(",") for l in open(self.path) if l.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r[5:9]):
+                if "Active" in v and "Not" not in v:
+                    reasons.add(n)
+        pw = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ workload
+
+def make_workload(cfg_name, device):
+    import mixture_experts_layer_15_gb300 as moe
+    cfg = synth.CONFIGS[cfg_name]
+    li = synth.make_layer(cfg, device)
+    fmt = moe.MOE_WEIGHTS_MXFP4 if cfg.weight_format == "mxfp4" else moe.MOE_WEIGHTS_BF16
+    layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
+                         w1_scale=li.w1_scale, w2_scale=li.w2_scale, fmt=fmt,
+                         route="softmax" if cfg.route == "softmax" else "sigmoid",
+                         score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                         routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2)
+    batches = {M: synth.make_tokens(cfg, M, device, li) for M in cfg.m_sweep}
+    return cfg, li, layer, batches
+
+
+def launches_per_forward(cfg, M):
+    """Kernels one forward launches (mirrors the library's launch plan)."""
+    n = 1                                                     # router
+    w = max(1, min(32, 8192 // cfg.E))
+    n += 1 if M * cfg.top_k <= 32 * w else 4                  # permute: fused, or count/scan/scatter/gather
+    n += 2                                                    # grouped GEMM1, GEMM2
+    n += 1                                                    # finalize
+    if cfg.shared_N:
+        n += 2                                                # shared expert GEMM1, GEMM2
+    return n
+
+
+def roofline_layer(cfg, M, touched, pk, sustained=True):
+    """Slower of touched-expert weight bytes at HBM bandwidth and FLOPs at
+    the bf16 tensor peak; returns (seconds, bytes, flops)."""
+    bpw = 2.0 if cfg.weight_format == "bf16" else (0.5 + 1.0 / 32.0)
+    wbytes = touched * 3.0 * cfg.K * cfg.N * bpw
+    flops = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+    if cfg.shared_N:
+        wbytes += 3.0 * cfg.K * cfg.shared_N * 2.0
+        flops += 6.0 * cfg.K * cfg.shared_N * M
+    tc = (pk["bf16_sus"] if sustained else pk["bf16"]) * 1e12
+    return max(wbytes / (pk["hbm"] * 1e9), flops / tc), wbytes, flops
+
+
+def run_gpu(args):
+    import mixture_experts_layer_15_gb300 as moe
+    rank, world = dist_init(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    cfg, li, layer, batches = make_workload(args.config, dev)
+    sweep = list(cfg.m_sweep)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def forward(M, ev=None):
+        x, logits = batches[M]
+        b = layer.buffers(M)
+        layer.route(logits, b)
+        moe.moe_permute(b.topk_ids, M, cfg.top_k, cfg.E, None, cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse,
+                        b.x_perm, b.perm_ws, b.perm_ws.numel())
+        if layer.ws1 is not None:
+            moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.shared, layer.gemm2_dtype,
+                                  b.shared_ws, b.shared_ws.numel())
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_experts(layer.cw, b.x_perm, b.offsets, M, cfg.top_k, b.gemm2, layer.gemm2_dtype, 0, None,
+                        layer.weights_dtype, None, None, layer.gemm2_dtype, 1.0, None, layer.out_dtype,
+                        b.exp_ws, b.exp_ws.numel())
+        if ev is not None:
+            ev[1].record(stream)
+        rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
+        moe.moe_finalize(b.gemm2, layer.gemm2_dtype, b.gemm2.shape[0], b.topk_weights, layer.weights_dtype,
+                         b.pmap, M, cfg.top_k, cfg.K, b.shared, layer.gemm2_dtype, rsf, b.out, layer.out_dtype)
+
+    for M in sweep:                                # allocate buffers outside any timing
+        layer.buffers(M)
+    for _ in range(args.warmup):
+        for M in sweep:
+            forward(M)
+    torch.cuda.synchronize()
+    st = moe.moe_get_error()
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {moe.status_string(st)}")
+
+    # touched experts per M (from the device's own routing)
+    touched = {M: int((layer.buffers(M).offsets.diff() > 0).sum().item()) for M in sweep}
+
+    ev_m = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] for M in sweep}
+    ev_g = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] for M in sweep}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0.record(stream)
+    for s in range(args.steps):
+        for M in sweep:
+            ev_m[M][s][0].record(stream)
+            forward(M, ev_g[M][s])
+            ev_m[M][s][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    st = moe.moe_get_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {moe.status_string(st)}")
+    secs = t0.elapsed_time(t1) / 1e3
+    secs_max = max_over_ranks(secs, world)
+    tokens_step = sum(sweep)
+    value = tokens_step * args.steps * world / secs_max
+
+    # per-M breakdown and the grouped-GEMM roofline
+    per_m = []
+    gemm_flops = gemm_secs = 0.0
+    for M in sweep:
+        tm = sum(a.elapsed_time(b) for a, b in ev_m[M]) / 1e3 / args.steps
+        tg = sum(a.elapsed_time(b) for a, b in ev_g[M]) / 1e3 / args.steps
+        troof, wbytes, flops = roofline_layer(cfg, M, touched[M], pk)
+        gf = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+        gemm_flops += gf
+        gemm_secs += tg
+        per_m.append({"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tg * 1e3,
+                      "touched_experts": touched[M], "roofline_ms": troof * 1e3,
+                      "roofline_frac": troof / tm,
+                      "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= flops / (pk["bf16_sus"] * 1e12) else "tensor",
+                      "gemm_tflops": gf / tg / 1e12, "gemm_weight_gbs": wbytes / tg / 1e9})
+    achieved = gemm_flops / gemm_secs / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(args.config)
+        except Exception:
+            traffic = None
+    roof = {"kernel": "grouped_gemm_kernel (GEMM1+silu_and_mul and GEMM2, 2 launches per forward)",
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+            "frac": achieved / pk["bf16_sus"], "peak_kind": f"{pk['src']} bf16 sustained",
+            "frac_of_burst": achieved / pk["bf16"], "traffic": traffic,
+            "algorithmic": "6*K*N*routes FLOPs per forward over the sweep"}
+
+    e2e = run_e2e(args, cfg, layer, batches, forward_fn=forward)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}-shaped MoE layer (K={cfg.K}, N={cfg.N}, E={cfg.E}, "
+                               f"top_k={cfg.top_k}, {cfg.weight_format} weights), one forward at each M",
+                   "M_sweep": sweep, "tokens_per_step": tokens_step,
+                   "storage": "f32 routing weights, gemm2_permuted and output; bf16 act",
+                   "l2": "inputs larger than L2 (expert weights streamed every forward)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "sweep": per_m, "e2e": e2e,
+        "gpu_launches": args.steps * sum(launches_per_forward(cfg, M) for M in sweep),
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(cfg, li, batches, args)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, cfg, layer, batches, forward_fn):
+    """Same metric through the public API with host buffers: each step copies
+    x and the router logits from pinned host memory to the device and reads
+    the output back, for every M of the sweep."""
+    stream = torch.cuda.current_stream()
+    host = {M: (x.cpu().pin_memory(), lg.cpu().pin_memory()) for M, (x, lg) in batches.items()}
+    outs = {M: torch.empty(layer.buffers(M).out.shape, dtype=layer.buffers(M).out.dtype).pin_memory()
+            for M in batches}
+    dev_in = {M: (torch.empty_like(x), torch.empty_like(lg)) for M, (x, lg) in batches.items()}
+    orig = dict(batches)
+    steps = max(3, args.steps // 4)
+    h2d = sum(x.numel() * x.element_size() + lg.numel() * lg.element_size() for x, lg in host.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs.values())
+    try:
+        for M in batches:
+            batches[M] = dev_in[M]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for it in range(2 + steps):
+            if it == 2:
+                torch.cuda.synchronize()
+                t0.record(stream)
+            for M in batches:
+                dev_in[M][0].copy_(host[M][0], non_blocking=True)
+                dev_in[M][1].copy_(host[M][1], non_blocking=True)
+                forward_fn(M)
+                outs[M].copy_(layer.buffers(M).out, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        batches.update(orig)
+    secs = t0.elapsed_time(t1) / 1e3
+    return {"value": sum(batches) * steps / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+class _F64Experts:
+    """Per-expert float64 copies of the weights, made once outside timing."""
+
+    def __init__(self, w, scale=None):
+        import oracle as O
+        self.cache = {}
+        self.w, self.scale, self.O = w, scale, O
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            if self.scale is None:
+                self.cache[e] = self.w[e].to(torch.float64).cpu().numpy()
+            else:
+                self.cache[e] = self.O.dequant_mxfp4(self.w[e].cpu().numpy(), self.scale[e].cpu().numpy())
+        return self.cache[e]
+
+    @property
+    def shape(self):
+        s = tuple(self.w.shape)
+        return s if self.scale is None else s[:-1] + (s[-1] * 2,)
+
+
+def _oracle_forward(O, cfg, li, w1, w2, x, logits):
+    return O.moe_forward(x, logits, w1, w2, cfg.top_k,
+                         route="softmax" if cfg.route == "softmax" else "sigmoid",
+                         score_bias=None if li.score_bias is None else li.score_bias.cpu().numpy(),
+                         n_group=cfg.n_group, topk_group=cfg.topk_group,
+                         routed_scaling_factor=cfg.routed_scaling_factor,
+                         ws1=None if li.ws1 is None else li.ws1.double().cpu().numpy(),
+                         ws2=None if li.ws2 is None else li.ws2.double().cpu().numpy())["out"]
+
+
+def _oracle_setup(cfg, li, batches):
+    import oracle as O
+    w1, w2 = _F64Experts(li.w1, li.w1_scale), _F64Experts(li.w2, li.w2_scale)
+    Mbig = max(batches)
+    x, logits = batches[Mbig]
+    xs = x.to(torch.float64).cpu().numpy()
+    ls = logits.cpu().numpy()
+    ids, _ = (O.route_softmax_topk(ls[:64], cfg.top_k) if cfg.route == "softmax" else
+              O.route_sigmoid_grouped(ls[:64], li.score_bias.cpu().numpy(), cfg.top_k, cfg.n_group,
+                                      cfg.topk_group, cfg.routed_scaling_factor))
+    for e in sorted(set(ids.reshape(-1).tolist())):   # convert the weights the sample uses, untimed
+        w1[e], w2[e]
+    return O, w1, w2, xs, ls
+
+
+def cpu_baseline(cfg, li, batches, args, budget_s=16.0):
+    """The oracle, as it stands, on a bounded sample of the largest batch:
+    its first S tokens through the whole layer (route, permute, experts,
+    finalize), S grown until the run takes about ``budget_s`` seconds."""
+    O, w1, w2, xs, ls = _oracle_setup(cfg, li, batches)
+    S, secs = 4, 0.0
+    while True:
+        t = time.perf_counter()
+        _oracle_forward(O, cfg, li, w1, w2, xs[:S], ls[:S])
+        secs = time.perf_counter() - t
+        if secs * 4 > budget_s or S >= 4096:
+            break
+        S *= 4
+    return {"value": S / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {S} tokens of the M={max(batches)} batch through the whole layer "
+                      f"(numpy float64, all BLAS threads), {secs:.2f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed on the host cores, each step a
+    bounded sample of the same workload; rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    cfg = synth.CONFIGS[args.config]
+    li = synth.make_layer(cfg, dev)
+    batches = {M: synth.make_tokens(cfg, M, dev, li) for M in cfg.m_sweep}
+    O, w1, w2, xs, ls = _oracle_setup(cfg, li, batches)
+    # size the per-step sample so the whole run stays within ~2 minutes
+    t = time.perf_counter()
+    _oracle_forward(O, cfg, li, w1, w2, xs[:2], ls[:2])
+    per_tok = max((time.perf_counter() - t) / 2, 1e-4)
+    S = int(max(1, min(64, 120.0 / (args.steps + args.warmup) / per_tok)))
+    for _ in range(args.warmup):
+        _oracle_forward(O, cfg, li, w1, w2, xs[:S], ls[:S])
+    t = time.perf_counter()
+    for s in range(args.steps):
+        o = (s * S) % max(1, xs.shape[0] - S)
+        _oracle_forward(O, cfg, li, w1, w2, xs[o:o + S], ls[o:o + S])
+    secs = time.perf_counter() - t
+    value = S * args.steps / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{cfg.name}-shaped MoE layer (K={cfg.K}, N={cfg.N}, E={cfg.E}, "
+                                   f"top_k={cfg.top_k}, {cfg.weight_format} weights), one forward at each M",
+                       "M_sweep": list(cfg.m_sweep)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{S} tokens of the M={max(cfg.m_sweep)} batch per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="mixtral", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
