@@ -177,6 +177,33 @@ moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_noalloc -- moe_permute for callers that cannot allocate device
+ * memory (no counterpart on the pages: it exists for this library's users).
+ * Some callers may not call cudaMalloc or hand the library a workspace: code
+ * capturing into a fixed graph memory pool, runtimes whose allocator is
+ * reserved, or real-time paths that must never allocate. This entry point
+ * takes the same arguments as moe_permute minus the workspace and gives the
+ * same results bit for bit; its scratch (the per-chunk expert histograms) is
+ * a fixed 1 MiB array inside the library that every GPU loading the library
+ * holds until the process exits.
+ *  - Limit: moe_permute_workspace_size(M, top_k, E_local) must be at most
+ *    1 MiB (for example M*top_k up to 2^21 routes at E_local = 128); larger
+ *    problems return MOE_ERR_WORKSPACE and enqueue nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - It calls no cudaMalloc, cudaFree or allocating routine.
+ *  - All calls on one device share the array; nothing in it needs clearing
+ *    between calls (every entry read is written first by the same call), but
+ *    calls whose kernels overlap on the GPU race on it and give wrong maps.
+ * ---------------------------------------------------------------------- */
+moe_status moe_permute_noalloc(const int32_t* topk_ids, int M, int top_k, int E,
+                               const int32_t* expert_map, int E_local,
+                               const void* x, int K,
+                               int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
+                               int32_t* permuted_to_expanded, void* x_perm, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_experts -- the experts: GEMM1, silu_and_mul, GEMM2, per local expert on
  * its rows of x_perm (modular_kernel.py, FusedMoEPermuteExpertsUnpermute.apply
  * and .activation). The result is unweighted and unreduced.

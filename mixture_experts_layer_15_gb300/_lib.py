@@ -32,7 +32,8 @@ MOE_WEIGHTS_MXFP4 = 1
 
 #: every function the header declares (checked against include/moe.h by the tests)
 EXPORTS = (
-    "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_experts_workspace_size",
+    "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
+    "moe_experts_workspace_size",
     "moe_experts", "moe_finalize", "moe_shared_expert_workspace_size", "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_debug_sigmoid",
 )
@@ -71,6 +72,7 @@ _SIGS = {
     "moe_route": ([_P, _I, _I, _I, _I, _P, _I, _I, _F, _P, _P, _I, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
     "moe_permute": ([_P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_experts_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I], _Z),
     "moe_experts": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _I, _F,
                      _P, _I, _P, _Z, _P], _I),
@@ -142,6 +144,16 @@ def moe_permute(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets
                                           _ptr(expanded_idx_to_permuted_idx), _ptr(permuted_to_expanded),
                                           _ptr(x_perm), _ptr(workspace), int(workspace_bytes),
                                           _stream(stream)))
+
+
+def moe_permute_noalloc(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                        expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm, stream=None):
+    """moe_permute without a workspace: its scratch is a fixed array in the library."""
+    _check("moe_permute_noalloc", lib.moe_permute_noalloc(_ptr(topk_ids), M, top_k, E, _ptr(expert_map),
+                                                          E_local, _ptr(x), K, _ptr(expert_offsets),
+                                                          _ptr(expanded_idx_to_permuted_idx),
+                                                          _ptr(permuted_to_expanded), _ptr(x_perm),
+                                                          _stream(stream)))
 
 
 def moe_experts_workspace_size(weights: moe_weights, M, top_k) -> int:
