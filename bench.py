@@ -133,7 +133,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg_name, device):
+def make_workload(cfg_name, device, only_m=None):
     import mixture_experts_layer_15_gb300 as moe
     cfg = synth.CONFIGS[cfg_name]
     li = synth.make_layer(cfg, device)
@@ -143,7 +143,8 @@ def make_workload(cfg_name, device):
                          route="softmax" if cfg.route == "softmax" else "sigmoid",
                          score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
                          routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2)
-    batches = {M: synth.make_tokens(cfg, M, device, li) for M in cfg.m_sweep}
+    sweep = cfg.m_sweep if not only_m else tuple(only_m)
+    batches = {M: synth.make_tokens(cfg, M, device, li) for M in sweep}
     return cfg, li, layer, batches
 
 
@@ -177,8 +178,8 @@ def run_gpu(args):
     rank, world = dist_init(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
-    cfg, li, layer, batches = make_workload(args.config, dev)
-    sweep = list(cfg.m_sweep)
+    cfg, li, layer, batches = make_workload(args.config, dev, args.m)
+    sweep = sorted(batches)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
@@ -287,7 +288,7 @@ def run_gpu(args):
         "clocks": clk,
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(cfg, li, batches, args)
+        line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(cfg, li, batches, args)
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -440,6 +441,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="mixtral", choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--m", type=int, nargs="*", default=None,
+                    help="run only these batch sizes of the sweep (profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
