@@ -133,9 +133,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg_name, device, only_m=None):
+def make_workload(cfg_name, device, only_m=None, experts=0):
+    import dataclasses
     import mixture_experts_layer_15_gb300 as moe
     cfg = synth.CONFIGS[cfg_name]
+    if experts:
+        kw = dict(E=experts)
+        if cfg.n_group > 1:
+            kw.update(n_group=min(cfg.n_group, experts // 2), topk_group=min(cfg.topk_group, experts // 2))
+        cfg = dataclasses.replace(cfg, **kw)
     li = synth.make_layer(cfg, device)
     fmt = moe.MOE_WEIGHTS_MXFP4 if cfg.weight_format == "mxfp4" else moe.MOE_WEIGHTS_BF16
     layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
@@ -178,7 +184,7 @@ def run_gpu(args):
     rank, world = dist_init(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
-    cfg, li, layer, batches = make_workload(args.config, dev, args.m)
+    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts)
     sweep = sorted(batches)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
@@ -444,6 +450,8 @@ def main():
     ap.add_argument("--m", type=int, nargs="*", default=None,
                     help="run only these batch sizes of the sweep (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: keep the first N experts of the config (not the benchmark workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -91,7 +91,8 @@ typedef enum moe_weight_format {
  *          Scale bytes must lie in 1..254 and every decoded value must be a
  *          normal bf16 or zero (the kernels decode to bf16 before the MMA).
  *
- * K and N must be multiples of 128. All pointers 16-byte aligned.
+ * K and N must be multiples of 128 (of 512 for MXFP4). All pointers 16-byte
+ * aligned.
  */
 typedef struct moe_weights {
     moe_weight_format format;
@@ -303,6 +304,15 @@ moe_status moe_get_error(cudaStream_t stream);
 
 /* MOE_OK if the current device has compute capability 10.3. */
 moe_status moe_device_check(void);
+
+/* Launch-plan override for moe_experts and moe_shared_expert (tuning and
+ * tests): token tile width (16, 32, 64, 128 or 256), the split-K factor of
+ * GEMM1 and GEMM2 (clamped so every split keeps at least one K-block), and
+ * the number of 128-row weight tiles per GEMM2 work unit (1 or 2; 2 needs
+ * K % 256 == 0). 0 restores the automatic choice. It applies to every later
+ * call in the process, including the *_workspace_size() queries, so query the
+ * workspace size after setting it. Not synchronised with concurrent calls. */
+moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles);
 
 /* The float32 sigmoid spec the sigmoid router selects with, applied to
  * x f32 [n] -> y f32 [n] (a test hook: the CPU oracle implements the same

@@ -35,7 +35,8 @@ EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
     "moe_experts", "moe_finalize", "moe_shared_expert_workspace_size", "moe_shared_expert",
-    "moe_status_string", "moe_get_error", "moe_device_check", "moe_debug_sigmoid",
+    "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
+    "moe_debug_sigmoid",
 )
 
 
@@ -82,6 +83,7 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_get_error": ([_P], _I),
     "moe_device_check": ([], _I),
+    "moe_set_plan_override": ([_I, _I, _I, _I], _I),
     "moe_debug_sigmoid": ([_P, _P, _I, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -200,6 +202,11 @@ def moe_get_error(stream=None) -> int:
 
 def moe_device_check() -> int:
     return int(lib.moe_device_check())
+
+
+def moe_set_plan_override(token_tile=0, splits_gemm1=0, splits_gemm2=0, gemm2_tiles=0):
+    _check("moe_set_plan_override", lib.moe_set_plan_override(token_tile, splits_gemm1, splits_gemm2,
+                                                              gemm2_tiles))
 
 
 def moe_debug_sigmoid(x, y, n, stream=None):

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -14,6 +16,35 @@ namespace moe {
 // writer wins) and the kernel skips the offending item.
 __device__ __forceinline__ void set_error(int* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// ---- programmatic dependent launch --------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation, so it may start while the previous kernel of the stream is
+// still finishing. It may only do local set-up (shared memory, TMEM, barrier
+// initialisation) before pdl_wait(), which returns once every earlier kernel
+// of the stream has completed and its writes are visible; all global-memory
+// reads and writes come after it. pdl_trigger() lets the next kernel start
+// its own set-up; it is issued right after pdl_wait() by every CTA, so a
+// dependent grid can only start once every CTA of this grid is resident (no
+// CTA of this grid can then be starved of an SM by the waiting dependents).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- dtype helpers -------------------------------------------------------------

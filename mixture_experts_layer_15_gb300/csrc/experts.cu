@@ -1,0 +1,230 @@
+// Host side of the experts step: TMA descriptors, the launch plan (token-tile
+// width, split-K), the workspace layout, and the GEMM1 -> GEMM2 launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+
+namespace moe {
+namespace {
+
+using gemm::GemmArgs;
+using gemm::kBK;
+using gemm::kBM;
+using gemm::kMaxSplitTiles;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D row-major tensor [outer, inner] of 1- or 2-byte elements, box {box_inner, box_outer}.
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * esize};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 operand tile: 64 elements (128 bytes) x box_outer rows, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    return encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, kBK, box_outer,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// ---- plan: token-tile width, split-K and workspace layout --------------------------
+struct PlanOverride {
+    int token_tile = 0;          // 0 = automatic
+    int splits[2] = {0, 0};      // GEMM1, GEMM2; 0 = automatic
+    int gemm2_na = 0;            // 128-row A tiles per GEMM2 unit (1 or 2); 0 = automatic
+};
+PlanOverride g_override;
+
+// Token tile: about twice the average rows per group (a group never holds
+// more than M rows: a token routes to an expert once), at least 32. 256-row
+// tiles fill all 512 TMEM columns, which leaves the epilogue unoverlapped; they
+// pay off only when work units are long (both reductions >= 4096) or when each
+// decoded MXFP4 weight tile should serve as many tokens as possible.
+int pick_bt(int M, int rows_alloc, int groups, int K, int N, bool mx) {
+    const int avg = (rows_alloc + groups - 1) / (groups > 0 ? groups : 1);
+    const int want = avg * 2 < M ? avg * 2 : M;
+    const int cap = (mx || (K >= 4096 && N >= 4096)) ? 256 : 128;
+    int bt = 32;
+    while (bt < want && bt < cap) bt <<= 1;
+    return bt;
+}
+
+struct GemmPlan {
+    int na, n_wtiles, splits, max_tiles;
+    size_t partial_bytes;
+};
+
+GemmPlan plan_gemm(int gemm_index, int bt, int na, int n_wtiles, int kr, int rows_alloc, int groups,
+                   int sm_count) {
+    GemmPlan p;
+    p.na = na;
+    p.n_wtiles = n_wtiles;
+    const int nonempty = groups < rows_alloc ? groups : rows_alloc;
+    p.max_tiles = n_wtiles * (rows_alloc / bt + nonempty + 1);
+    const int tt = (rows_alloc + bt - 1) / bt > nonempty ? (rows_alloc + bt - 1) / bt : nonempty;
+    const long long est = static_cast<long long>(n_wtiles) * (tt > 0 ? tt : 1);   // expected tiles
+    const int nkb = kr / kBK;
+    int s = 1;
+    if (est < 2LL * sm_count && p.max_tiles <= kMaxSplitTiles) {
+        // time ~ waves x (k-blocks per unit + the split epilogue's extra
+        // traffic: writing and reading back the fp32 partial tile, counted in
+        // k-blocks of operand traffic)
+        const double part = 2.0 * na * kBM * bt * 4.0;
+        const double kblock = na * kBM * kBK * 2.0 + bt * kBK * 2.0;
+        const double ovh = part / kblock;
+        const int cap = nkb / 4 > 1 ? (nkb / 4 < 16 ? nkb / 4 : 16) : 1;
+        double best = 1e30;
+        for (int c = 1; c <= cap; ++c) {
+            const long long units = est * c;
+            const long long waves = (units + sm_count - 1) / sm_count;
+            const double t = static_cast<double>(waves) * (static_cast<double>(nkb) / c + (c > 1 ? ovh : 0.0));
+            if (t < best - 1e-9) { best = t; s = c; }
+        }
+    }
+    if (g_override.splits[gemm_index] > 0 && p.max_tiles <= kMaxSplitTiles) s = g_override.splits[gemm_index];
+    if (s > nkb) s = nkb;
+    p.splits = s;
+    p.partial_bytes = s > 1 ? static_cast<size_t>(p.max_tiles) * s * na * kBM * bt * sizeof(float) : 0;
+    return p;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+    int bt;
+    GemmPlan g1, g2;
+    size_t off_act, off_p1, off_p2, total;
+};
+
+Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count) {
+    Layout L;
+    const int K = w->K, N = w->N;
+    L.bt = g_override.token_tile > 0 ? g_override.token_tile
+                                     : pick_bt(M, rows_alloc, groups, K, N, w->format == MOE_WEIGHTS_MXFP4);
+    L.g1 = plan_gemm(0, L.bt, 2, N / kBM, K, rows_alloc, groups, sm_count);
+    int na2 = (K % 256 == 0) ? 2 : 1;
+    if (g_override.gemm2_na == 1 || (g_override.gemm2_na == 2 && K % 256 == 0)) na2 = g_override.gemm2_na;
+    L.g2 = plan_gemm(1, L.bt, na2, K / (na2 * kBM), N, rows_alloc, groups, sm_count);
+    size_t off = 2 * kMaxSplitTiles * sizeof(int);           // two counter regions, kept zero
+    L.off_act = off;
+    off = align256(off + static_cast<size_t>(rows_alloc) * N * 2);
+    L.off_p1 = off;
+    off = align256(off + L.g1.partial_bytes);
+    L.off_p2 = off;
+    off = align256(off + L.g2.partial_bytes);
+    L.total = off;
+    return L;
+}
+
+// A-operand descriptors of one weight matrix [E*rows, kr] (bf16) or its packed
+// codes [E*rows, kr/2] + scales [E*rows, kr/32] (MXFP4).
+bool encode_weights(CUtensorMap* tmA, CUtensorMap* tmS, bool mx, const void* w, const uint8_t* sc,
+                    uint64_t kr, uint64_t rows) {
+    if (!mx) {
+        if (!encode_bf16(tmA, w, kr, rows, kBM)) return false;
+        *tmS = *tmA;                                        // unused
+        return true;
+    }
+    return encode_2d(tmA, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kr / 2, rows, kBK / 2, kBM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_2d(tmS, sc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kr / 32, rows, 16, kBM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+cudaError_t launch_one(bool mx, int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
+                       const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                       cudaStream_t s) {
+    return mx ? gemm::launch_gemm_mxfp4(mode, bt, na, out_dtype, tmA, tmS, tmB, a, grid, s)
+              : gemm::launch_gemm_bf16(mode, bt, na, out_dtype, tmA, tmS, tmB, a, grid, s);
+}
+
+}  // namespace
+
+void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na) {
+    g_override.token_tile = token_tile;
+    g_override.splits[0] = splits1;
+    g_override.splits[1] = splits2;
+    g_override.gemm2_na = gemm2_na;
+}
+
+size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev) {
+    return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count).total;
+}
+
+cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*workspace_bytes*/, int* err,
+                           const DeviceInfo& dev, cudaStream_t s) {
+    const moe_weights* w = p.w;
+    const int K = w->K, N = w->N;
+    const bool mx = w->format == MOE_WEIGHTS_MXFP4;
+    const int groups = p.offsets != nullptr ? w->E_local : 1;
+    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* counters1 = reinterpret_cast<int*>(ws);
+    int* counters2 = counters1 + kMaxSplitTiles;
+    void* act = ws + L.off_act;
+
+    CUtensorMap tmW1, tmS1, tmX, tmW2, tmS2, tmAct;
+    const uint64_t E = static_cast<uint64_t>(w->E_local);
+    if (!encode_weights(&tmW1, &tmS1, mx, w->w1, w->w1_scale, K, E * 2 * N) ||
+        !encode_weights(&tmW2, &tmS2, mx, w->w2, w->w2_scale, N, E * K) ||
+        !encode_bf16(&tmX, p.x, K, p.rows_alloc, L.bt) || !encode_bf16(&tmAct, act, N, p.rows_alloc, L.bt))
+        return cudaErrorInvalidValue;
+
+    const int grid = dev.sm_count;
+    GemmArgs a1{};
+    a1.offsets = p.offsets;
+    a1.single_rows = p.single_rows;
+    a1.groups = groups;
+    a1.rows_alloc = p.rows_alloc;
+    a1.kr = K;
+    a1.rows_per_group = 2 * N;
+    a1.n_wtiles = L.g1.n_wtiles;
+    a1.wtile_rows = kBM;
+    a1.a1_offset = N;
+    a1.splits = L.g1.splits;
+    a1.out_ld = N;
+    a1.out = act;
+    a1.partials = reinterpret_cast<float*>(ws + L.off_p1);
+    a1.counters = counters1;
+    a1.max_tiles = L.g1.max_tiles;
+    a1.err = err;
+    cudaError_t e = launch_one(mx, gemm::MODE_SWIGLU, L.bt, 2, MOE_DTYPE_BF16, tmW1, tmS1, tmX, a1, grid, s);
+    if (e != cudaSuccess) return e;
+
+    GemmArgs a2 = a1;
+    a2.kr = N;
+    a2.rows_per_group = K;
+    a2.n_wtiles = L.g2.n_wtiles;
+    a2.wtile_rows = L.g2.na * kBM;
+    a2.a1_offset = kBM;
+    a2.splits = L.g2.splits;
+    a2.out_ld = K;
+    a2.out = p.y;
+    a2.partials = reinterpret_cast<float*>(ws + L.off_p2);
+    a2.counters = counters2;
+    a2.max_tiles = L.g2.max_tiles;
+    return launch_one(mx, gemm::MODE_PLAIN, L.bt, L.g2.na, p.y_dtype, tmW2, tmS2, tmAct, a2, grid, s);
+}
+
+}  // namespace moe

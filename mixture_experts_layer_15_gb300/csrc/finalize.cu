@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const GT* __restrict__ g2, int num_rows, const void* __restrict__ w, int wdtype,
                 const int32_t* __restrict__ map, int top_k, int K, const ST* __restrict__ shared,
                 float rsf, OT* __restrict__ out, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const int c = blockIdx.y * kCols + threadIdx.x * 8;
     if (c >= K) return;
@@ -57,10 +59,9 @@ cudaError_t launch_typed(const void* g2, int num_rows, const void* w, int wdtype
                          int M, int top_k, int K, const void* shared, float rsf, void* out,
                          int* err, cudaStream_t s) {
     const dim3 grid(M, ceil_div(K, kCols));
-    finalize_kernel<GT, ST, OT><<<grid, kThreads, 0, s>>>(
-        static_cast<const GT*>(g2), num_rows, w, wdtype, map, top_k, K,
-        static_cast<const ST*>(shared), rsf, static_cast<OT*>(out), err);
-    return cudaGetLastError();
+    return launch_pdl(finalize_kernel<GT, ST, OT>, grid, dim3(kThreads), 0, s, static_cast<const GT*>(g2),
+                      num_rows, w, wdtype, map, top_k, K, static_cast<const ST*>(shared), rsf,
+                      static_cast<OT*>(out), err);
 }
 
 template <typename GT, typename ST>

@@ -9,25 +9,40 @@
 // with fp32 accumulation and run on tcgen05 MMAs with TMEM accumulators.
 //
 // Tile shape ("weights as the MMA's M side"): the MMA M dimension (128) runs
-// over weight rows and its N dimension (BT = 16..256) over token rows. Decode
-// batches (a few tokens per expert) then stream the weights at full MMA width
-// instead of padding tokens up to 128. A work unit is
+// over weight rows and its N dimension (up to BT = 16..256) over token rows.
+// Decode batches (a few tokens per expert) then stream the weights at full MMA
+// width instead of padding tokens up to 128; the MMA N of each tile is cut to
+// the tile's row count rounded up to 16, so a partial token tile does not pay
+// for the rows it does not have. A work unit is
 //     (group g, weight tile wt, token tile tt, k-split s)
 // and covers two 128-row A tiles (GEMM1: the gate rows n0..n0+127 and the
-// matching up rows N+n0..; GEMM2: output rows k0..k0+255) against one
-// BT-row token tile, i.e. two accumulators of 128 x BT fp32 in TMEM; the
-// GEMM1 epilogue therefore sees gate and up of the same output column in the
-// same thread and applies silu(gate)*up with no second pass.
+// matching up rows N+n0..; GEMM2: output rows k0..k0+255) against one token
+// tile, i.e. two accumulators of 128 x BT fp32 in TMEM; the GEMM1 epilogue
+// therefore sees gate and up of the same output column in the same thread and
+// applies silu(gate)*up with no second pass.
 //
-// CTA = 6 warps, persistent (one CTA per SM):
-//   warp 0     TMA producer: A0, A1, B tiles of 64 reduction elements into a
-//              STAGES-deep shared-memory ring (full/empty mbarriers);
+// CTA warps, persistent (one CTA per SM):
+//   warp 0     TMA producer: A, B tiles of 64 reduction elements into a
+//              shared-memory ring (full/empty mbarriers);
 //   warp 1     TMEM allocator and MMA issuer (one thread), commits free ring
 //              slots and signals finished accumulators;
-//   warps 2-5  epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
-//              lanes 32*(w%4)..), activation, masked stores by row.
+//   warps 2-9  epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
+//              lanes 32*(w%4).., the two warps of a lane quarter take
+//              alternate 16-column chunks), activation, masked stores by row;
+//   warps 10-13 (MXFP4 weights only) converters: decode the packed e2m1 codes
+//              and their E8M0 scales (flashinfer_moe_ep.py, _E2M1_LUT and
+//              _dequant_fp4_ue8m0_gran32) to bf16 in the 128-byte-swizzled
+//              layout the MMA reads, one weight row per thread.
 // Accumulators are double-buffered in TMEM when 2 x (2 x BT) <= 512 columns,
 // so the epilogue of one unit overlaps the mainloop of the next.
+//
+// MXFP4: the TMA ring carries the packed A tiles (128 rows x 32 bytes per 64
+// elements), the matching scale tiles (128 rows x 16 bytes = 8 k-blocks of
+// scales, re-read per k-block from L2) and the B tile; a second, shallower
+// ring holds the decoded bf16 A tiles. Decoding: two byte-permute lookups turn
+// four 3-bit magnitudes into the bf16 bit patterns of {0, .5, 1, 1.5, 2, 3, 4,
+// 6}, the sign bits are moved into place, and one bf16x2 multiply by the
+// power-of-two scale applies 2^(s-127) (exact for normal results).
 //
 // The unit list is built on the device from the group offsets: every CTA
 // scans ceil(count_g / BT) * weight tiles * splits over the groups in shared
@@ -43,24 +58,26 @@
 // kernel records MOE_ERR_DEVICE_TIMEOUT, raises a shared abort flag that
 // releases the other roles, lets its in-flight TMA loads and MMAs land,
 // frees its TMEM and returns.
+#pragma once
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
-namespace {
+namespace gemm {
 
 using namespace ptx;
 
 constexpr int kBM = 128;                  // weight rows per A tile (MMA M)
 constexpr int kBK = 64;                   // reduction elements per ring stage (128 B of bf16)
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kConvThreads = 128;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxSplitTiles = 16384;     // capacity of one counter region
@@ -87,12 +104,19 @@ struct GemmArgs {
     int* err;
 };
 
-template <int BT, int NA>
+template <int BT, int NA, bool MX>
 struct Cfg {
-    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int THREADS = 64 + kEpiThreads + (MX ? kConvThreads : 0);
+    static constexpr int A_BYTES = kBM * kBK * 2;                 // bf16 A tile (TMA'd or decoded)
+    static constexpr int RAW_BYTES = kBM * kBK / 2;               // packed e2m1 A tile
+    static constexpr int SC_BYTES = kBM * 16;                     // scale tile: 8 k-blocks of scales
     static constexpr int B_BYTES = BT * kBK * 2;
-    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
-    static constexpr int STAGES_FIT = (kSmemBudget - 12 * 1024) / STAGE_BYTES;
+    // ring stage: [A x NA | B] (bf16) or [raw x NA | scales x NA | B] (MXFP4)
+    static constexpr int B_OFF = MX ? NA * (RAW_BYTES + SC_BYTES) : NA * A_BYTES;
+    static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
+    static constexpr int DSTAGES = MX ? (BT >= 128 ? 2 : 3) : 0;  // decoded-A ring (MXFP4)
+    static constexpr int DSTAGE_BYTES = NA * A_BYTES;
+    static constexpr int STAGES_FIT = (kSmemBudget - 12 * 1024 - DSTAGES * DSTAGE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int ACC_COLS = NA * BT;
     static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
@@ -100,8 +124,10 @@ struct Cfg {
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     // shared memory layout (offsets from the 1024-aligned base)
-    static constexpr int OFF_BAR = STAGES * STAGE_BYTES;          // full[S], empty[S], tfull[2], tempty[2], drain
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_DEC = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_DEC + DSTAGES * DSTAGE_BYTES;
+    // full[S], empty[S], dfull[DS], dempty[DS], tfull[2], tempty[2], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * DSTAGES + 5;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort, last flag
     static constexpr int OFF_PREFIX = OFF_MISC + 16;              // [kMaxGroups+1]
     static constexpr int OFF_OFFS = OFF_PREFIX + (kMaxGroups + 1) * 4;   // [kMaxGroups+1]
@@ -110,10 +136,11 @@ struct Cfg {
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N");
+    static_assert(B_OFF % 1024 == 0 && STAGE_BYTES % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
 };
 
 struct Unit {
-    int g, wt, s, row0, row_end, kb0, kb1, tile;
+    int g, wt, s, row0, row_end, kb0, kb1, tile, ncols;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* offs, int BT,
@@ -134,6 +161,9 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
     un.wt = local / ntt;
     un.row0 = beg + tt * BT;
     un.row_end = min(end, a.rows_alloc);
+    const int rows = min(BT, un.row_end - un.row0);
+    un.ncols = (rows + 15) & ~15;              // MMA N of this tile: its rows rounded up to 16
+    if (un.ncols < 16) un.ncols = 16;
     const int nkb = a.kr / kBK;
     un.kb0 = un.s * nkb / a.splits;
     un.kb1 = (un.s + 1) * nkb / a.splits;
@@ -161,7 +191,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 template <typename OutT>
@@ -194,11 +224,61 @@ __device__ __forceinline__ void emit16(const Unit& un, const GemmArgs& a, int ro
     }
 }
 
-template <int BT, int NA, int MODE, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs a) {
-    using C = Cfg<BT, NA>;
+// ---- MXFP4 decode -------------------------------------------------------------------
+// Eight e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j)
+// -> eight bf16 values times 2^(scale-127), as four bf16x2 words.
+// Byte tables indexed by the 3-bit magnitude code: high and low bytes of the
+// bf16 encodings of 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+constexpr uint32_t kE2m1HiLo = 0x3F3F3F00u, kE2m1HiHi = 0x40404040u;
+constexpr uint32_t kE2m1LoLo = 0xC0800000u, kE2m1LoHi = 0xC0804000u;
+
+__device__ __forceinline__ void decode8(uint32_t w, uint32_t scale2, uint32_t (&o)[4]) {
+    const uint32_t sel_a = w & 0x7777u;                 // magnitudes of elements 0..3
+    const uint32_t sel_b = (w >> 16) & 0x7777u;         // magnitudes of elements 4..7
+    const uint32_t hi_a = __byte_perm(kE2m1HiLo, kE2m1HiHi, sel_a);
+    const uint32_t lo_a = __byte_perm(kE2m1LoLo, kE2m1LoHi, sel_a);
+    const uint32_t hi_b = __byte_perm(kE2m1HiLo, kE2m1HiHi, sel_b);
+    const uint32_t lo_b = __byte_perm(kE2m1LoLo, kE2m1LoHi, sel_b);
+    // interleave (lo, hi) byte pairs into bf16 halves; OR in the sign bits
+    // (bit 3 of each code -> bit 15 of its bf16)
+    o[0] = __byte_perm(lo_a, hi_a, 0x5140) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
+    o[1] = __byte_perm(lo_a, hi_a, 0x7362) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+    o[2] = __byte_perm(lo_b, hi_b, 0x5140) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
+    o[3] = __byte_perm(lo_b, hi_b, 0x7362) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
+    const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&o[i]);
+        v = __hmul2(v, s);
+        o[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+}
+
+// One weight row of one k-block: 32 packed bytes + 2 scale bytes -> 64 bf16
+// written into the 128-byte-swizzled K-major tile (row r, 16-byte chunk c at
+// chunk position c ^ (r & 7); the tile base is 1024-byte aligned).
+__device__ __forceinline__ void decode_row(const uint8_t* raw_row, uint32_t sc0, uint32_t sc1,
+                                           uint8_t* dec_tile, int r) {
+    const uint4 p0 = *reinterpret_cast<const uint4*>(raw_row);
+    const uint4 p1 = *reinterpret_cast<const uint4*>(raw_row + 16);
+    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    // bf16 2^(s-127) has exponent field s and a zero mantissa: bits s << 7
+    const uint32_t s2a = (sc0 << 7) | (sc0 << 23);
+    const uint32_t s2b = (sc1 << 7) | (sc1 << 23);
+    uint8_t* row = dec_tile + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t o[4];
+        decode8(words[c], c < 4 ? s2a : s2b, o);
+        *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <int BT, int NA, int MODE, typename OutT, bool MX>
+__global__ void __launch_bounds__(Cfg<BT, NA, MX>::THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    using C = Cfg<BT, NA, MX>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -207,9 +287,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (C::STAGES + s); };
-    auto tfull_bar = [&](int b) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + b); };
-    auto tempty_bar = [&](int b) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + 2 + b); };
-    const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * C::STAGES + 4);
+    auto dfull_bar = [&](int d) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + d); };
+    auto dempty_bar = [&](int d) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + C::DSTAGES + d); };
+    auto tfull_bar = [&](int b) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + 2 * C::DSTAGES + b); };
+    auto tempty_bar = [&](int b) { return sbase + C::OFF_BAR + 8u * (2 * C::STAGES + 2 * C::DSTAGES + 2 + b); };
+    const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * C::STAGES + 2 * C::DSTAGES + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -221,7 +303,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            // MXFP4: the converters release the packed tile, the MMA the B tile
+            mbar_init(empty_bar(s), MX ? 1 + kConvThreads : 1);
+        }
+        for (int d = 0; d < C::DSTAGES; ++d) {
+            mbar_init(dfull_bar(d), kConvThreads);
+            mbar_init(dempty_bar(d), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -231,20 +318,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
+        if (MX) prefetch_tensormap(&tmS);
         prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above is CTA-local; from here on the kernel reads what the
+    // previous kernels of the stream wrote
+    pdl_wait();
+    pdl_trigger();
     // group offsets (validated: non-decreasing, within the allocation)
-    for (int g = tid; g <= a.groups; g += kThreads) {
+    for (int g = tid; g <= a.groups; g += C::THREADS) {
         int v = a.offsets != nullptr ? __ldg(a.offsets + g) : (g == 0 ? 0 : a.single_rows);
         if (v < 0 || v > a.rows_alloc) { set_error(a.err, MOE_ERR_DEVICE_INDEX); v = v < 0 ? 0 : a.rows_alloc; }
         offs[g] = v;
     }
     __syncthreads();
-    for (int g = tid; g < a.groups; g += kThreads) {
+    for (int g = tid; g < a.groups; g += C::THREADS) {
         int cnt = offs[g + 1] - offs[g];
         if (cnt < 0) { set_error(a.err, MOE_ERR_DEVICE_INDEX); cnt = 0; }
         prefix[g] = ((cnt + BT - 1) / BT) * a.n_wtiles * a.splits;
@@ -270,11 +362,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int a0 = un.g * a.rows_per_group + un.wt * a.wtile_rows;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                    const uint32_t sA = sbase + stage * C::STAGE_BYTES;
+                    const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
-                    tma_load_2d(sA, &tmA, kb * kBK, a0, full_bar(stage));
-                    if (NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA, kb * kBK, a0 + a.a1_offset, full_bar(stage));
-                    tma_load_2d(sA + NA * C::A_BYTES, &tmB, kb * kBK, un.row0, full_bar(stage));
+                    if (MX) {
+                        // packed codes: 32 bytes per row per k-block; scales: the
+                        // 16-byte group of 8 k-blocks that holds this one
+                        tma_load_2d(st, &tmA, kb * (kBK / 2), a0, full_bar(stage));
+                        tma_load_2d(st + NA * C::RAW_BYTES, &tmS, (kb >> 3) * 16, a0, full_bar(stage));
+                        if (NA == 2) {
+                            tma_load_2d(st + C::RAW_BYTES, &tmA, kb * (kBK / 2), a0 + a.a1_offset, full_bar(stage));
+                            tma_load_2d(st + NA * C::RAW_BYTES + C::SC_BYTES, &tmS, (kb >> 3) * 16,
+                                        a0 + a.a1_offset, full_bar(stage));
+                        }
+                    } else {
+                        tma_load_2d(st, &tmA, kb * kBK, a0, full_bar(stage));
+                        if (NA == 2) tma_load_2d(st + C::A_BYTES, &tmA, kb * kBK, a0 + a.a1_offset, full_bar(stage));
+                    }
+                    tma_load_2d(st + C::B_OFF, &tmB, kb * kBK, un.row0, full_bar(stage));
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -294,13 +398,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, BT);
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, dstage = 0;
+            uint32_t phase = 0, dphase = 0;
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
                 const Unit un = decode_unit(u, prefix, offs, BT, a);
+                const uint32_t idesc = idesc_bf16_f32(kBM, un.ncols);
                 const int buf = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a.err)) break;
@@ -308,9 +412,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t d = tmem_base + buf * C::ACC_COLS;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+                    if (MX && !wait_bar(dfull_bar(dstage), dphase, abort_flag, a.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sA0 = sbase + stage * C::STAGE_BYTES;
-                    const uint32_t sB = sA0 + NA * C::A_BYTES;
+                    const uint32_t st = sbase + stage * C::STAGE_BYTES;
+                    const uint32_t sA0 = MX ? sbase + C::OFF_DEC + dstage * C::DSTAGE_BYTES : st;
+                    const uint32_t sB = st + C::B_OFF;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bdesc = sw128_kmajor_desc(sB + kk * 32);
@@ -321,6 +427,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     mma_commit(empty_bar(stage));            // ring slot free once these MMAs finish
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                    if (MX) {
+                        mma_commit(dempty_bar(dstage));      // decoded tile free likewise
+                        if (++dstage == C::DSTAGES) { dstage = 0; dphase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 mma_commit(tfull_bar(buf));                  // accumulator ready for the epilogue
@@ -331,11 +441,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {}
         }
         __syncwarp();
-    } else {
-        // ================= epilogue (warps 2..5) =================
+    } else if (warp < 2 + kEpiWarps) {
+        // ================= epilogue (warps 2..9) =================
         const int q = warp & 3;                              // TMEM lanes 32q..32q+31
         const int row_in_tile = q * 32 + lane;
         const int etid = tid - 64;
+        const int c_first = 16 * ((warp - 2) >> 2);          // this warp's first 16-column chunk
+        constexpr int c_step = 16 * (kEpiWarps / 4);
         int it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
             const Unit un = decode_unit(u, prefix, offs, BT, a);
@@ -348,7 +460,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
             if (a.splits == 1) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < BT; c0 += 16) {
+                for (int c0 = c_first; c0 < un.ncols; c0 += c_step) {
                     float v0[16], v1[16];
                     if (NA == 2) tmem_ld16x2(tb + c0, tb + BT + c0, v0, v1);
                     else tmem_ld16(tb + c0, v0);
@@ -361,7 +473,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const bool tile_ok = un.tile < a.max_tiles;
                 float* part = a.partials + (static_cast<size_t>(un.tile) * a.splits + un.s) * slot;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BT; c0 += 16) {
+                for (int c0 = c_first; c0 < un.ncols; c0 += c_step) {
                     float v0[16], v1[16];
                     if (NA == 2) tmem_ld16x2(tb + c0, tb + BT + c0, v0, v1);
                     else tmem_ld16(tb + c0, v0);
@@ -394,7 +506,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     __threadfence();
                     const float* p0 = a.partials + static_cast<size_t>(un.tile) * a.splits * slot;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < BT; c0 += 16) {
+                    for (int c0 = c_first; c0 < un.ncols; c0 += c_step) {
                         float v0[16], v1[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) { v0[i] = 0.0f; v1[i] = 0.0f; }
@@ -412,6 +524,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 named_bar_sync(1, kEpiThreads);              // last_flag is reused by the next unit
             }
         }
+    } else if (MX) {
+        // ================= converters (warps 10..13, MXFP4 only) =================
+        const int r = tid - 64 - kEpiThreads;                // weight row of each A tile
+        int stage = 0, dstage = 0;
+        uint32_t phase = 0, dphase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const Unit un = decode_unit(u, prefix, offs, BT, a);
+            for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+                if (!wait_bar(dempty_bar(dstage), dphase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+                const uint8_t* st = smem + stage * C::STAGE_BYTES;
+                uint8_t* dec = smem + C::OFF_DEC + dstage * C::DSTAGE_BYTES;
+                const int sb = 2 * (kb & 7);                 // this k-block's 2 scale bytes
+#pragma unroll
+                for (int t = 0; t < NA; ++t) {
+                    const uint8_t* sc = st + NA * C::RAW_BYTES + t * C::SC_BYTES + r * 16 + sb;
+                    decode_row(st + t * C::RAW_BYTES + r * 32, sc[0], sc[1], dec + t * C::A_BYTES, r);
+                }
+                // generic-proxy shared-memory writes -> visible to the MMA (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(empty_bar(stage));
+                mbar_arrive(dfull_bar(dstage));
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                if (++dstage == C::DSTAGES) { dstage = 0; dphase ^= 1u; }
+            }
+        }
     }
 
     // ---- teardown ----
@@ -421,42 +560,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-// ---------------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// bf16 2D tensor [outer, inner] (row-major) with a (box_outer x 64) box, 128B swizzle.
-bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    auto fn = get_encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int BT, int NA, int MODE, typename OutT>
-cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                          cudaStream_t s) {
-    using C = Cfg<BT, NA>;
-    auto kern = grouped_gemm_kernel<BT, NA, MODE, OutT>;
+// ---- launching one instantiation ------------------------------------------------------
+template <int BT, int NA, int MODE, typename OutT, bool MX>
+cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmS, const CUtensorMap& tmB,
+                          const GemmArgs& a, int grid, cudaStream_t s) {
+    using C = Cfg<BT, NA, MX>;
+    auto kern = grouped_gemm_kernel<BT, NA, MODE, OutT, MX>;
     static std::atomic<uint64_t> configured{0};      // bit per device ordinal
     int dev = 0;
     cudaGetDevice(&dev);
@@ -466,151 +575,41 @@ cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, tmA, tmS, tmB, a);
 }
 
-template <int NA, int MODE, typename OutT>
-cudaError_t launch_bt(int bt, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                      cudaStream_t s) {
+template <int NA, int MODE, typename OutT, bool MX>
+cudaError_t launch_bt(int bt, const CUtensorMap& tmA, const CUtensorMap& tmS, const CUtensorMap& tmB,
+                      const GemmArgs& a, int grid, cudaStream_t s) {
     switch (bt) {
-        case 16: return launch_kernel<16, NA, MODE, OutT>(tmA, tmB, a, grid, s);
-        case 32: return launch_kernel<32, NA, MODE, OutT>(tmA, tmB, a, grid, s);
-        case 64: return launch_kernel<64, NA, MODE, OutT>(tmA, tmB, a, grid, s);
-        case 128: return launch_kernel<128, NA, MODE, OutT>(tmA, tmB, a, grid, s);
-        default: return launch_kernel<256, NA, MODE, OutT>(tmA, tmB, a, grid, s);
+        case 16: return launch_kernel<16, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
+        case 32: return launch_kernel<32, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
+        case 64: return launch_kernel<64, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
+        case 128: return launch_kernel<128, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
+        default: return launch_kernel<256, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
     }
 }
 
-// ---- plan: token-tile width, split-K and workspace layout --------------------------
-int pick_bt(int M, int rows_alloc, int groups) {
-    // a group never holds more than M rows (a token routes to an expert once)
-    const int avg = (rows_alloc + groups - 1) / (groups > 0 ? groups : 1);
-    int want = avg * 2 < M ? avg * 2 : M;
-    int bt = 16;
-    while (bt < want && bt < 256) bt <<= 1;
-    return bt;
-}
-
-struct GemmPlan {
-    int na, n_wtiles, splits, max_tiles;
-    size_t partial_bytes;
-};
-
-GemmPlan plan_gemm(int bt, int na, int n_wtiles, int kr, int rows_alloc, int groups, int sm_count) {
-    GemmPlan p;
-    p.na = na;
-    p.n_wtiles = n_wtiles;
-    const int nonempty = groups < rows_alloc ? groups : rows_alloc;
-    p.max_tiles = n_wtiles * (rows_alloc / bt + nonempty + 1);
-    const int est_tt = (rows_alloc + bt - 1) / bt > nonempty ? (rows_alloc + bt - 1) / bt : nonempty;
-    const long long est = static_cast<long long>(n_wtiles) * (est_tt > 0 ? est_tt : 1);
-    const int nkb = kr / kBK;
-    int s = 1;
-    if (est < 2LL * sm_count && p.max_tiles <= kMaxSplitTiles) {
-        s = static_cast<int>((2LL * sm_count + est - 1) / est);
-        int cap = nkb / 4 > 1 ? nkb / 4 : 1;
-        if (s > cap) s = cap;
-        if (s > 16) s = 16;
-        if (s < 1) s = 1;
+// GEMM1 (mode 0) or GEMM2 (mode 1) of one weight format.
+template <bool MX>
+cudaError_t launch_gemm(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmS,
+                        const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
+    if (mode == MODE_SWIGLU) return launch_bt<2, MODE_SWIGLU, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
+    if (na == 2) {
+        if (out_dtype == MOE_DTYPE_F32) return launch_bt<2, MODE_PLAIN, float, MX>(bt, tmA, tmS, tmB, a, grid, s);
+        return launch_bt<2, MODE_PLAIN, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
     }
-    p.splits = s;
-    p.partial_bytes = s > 1 ? static_cast<size_t>(p.max_tiles) * s * na * kBM * bt * sizeof(float) : 0;
-    return p;
+    if (out_dtype == MOE_DTYPE_F32) return launch_bt<1, MODE_PLAIN, float, MX>(bt, tmA, tmS, tmB, a, grid, s);
+    return launch_bt<1, MODE_PLAIN, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
 }
 
-size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+// Defined in gemm_bf16.cu and gemm_mxfp4.cu (one translation unit per weight format).
+cudaError_t launch_gemm_bf16(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
+                             const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                             cudaStream_t s);
+cudaError_t launch_gemm_mxfp4(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
+                              const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                              cudaStream_t s);
 
-struct Layout {
-    int bt;
-    GemmPlan g1, g2;
-    size_t off_act, off_p1, off_p2, total;
-};
-
-Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count) {
-    Layout L;
-    const int K = w->K, N = w->N;
-    L.bt = pick_bt(M, rows_alloc, groups);
-    L.g1 = plan_gemm(L.bt, 2, N / kBM, K, rows_alloc, groups, sm_count);
-    const int na2 = (K % 256 == 0) ? 2 : 1;
-    L.g2 = plan_gemm(L.bt, na2, K / (na2 * kBM), N, rows_alloc, groups, sm_count);
-    size_t off = 2 * kMaxSplitTiles * sizeof(int);           // two counter regions, kept zero
-    L.off_act = off;
-    off = align256(off + static_cast<size_t>(rows_alloc) * N * 2);
-    L.off_p1 = off;
-    off = align256(off + L.g1.partial_bytes);
-    L.off_p2 = off;
-    off = align256(off + L.g2.partial_bytes);
-    L.total = off;
-    return L;
-}
-
-}  // namespace
-
-size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev) {
-    return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count).total;
-}
-
-cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*workspace_bytes*/, int* err,
-                           const DeviceInfo& dev, cudaStream_t s) {
-    const moe_weights* w = p.w;
-    const int K = w->K, N = w->N;
-    const int groups = p.offsets != nullptr ? w->E_local : 1;
-    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* counters1 = reinterpret_cast<int*>(ws);
-    int* counters2 = counters1 + kMaxSplitTiles;
-    void* act = ws + L.off_act;
-
-    if (w->format != MOE_WEIGHTS_BF16) return cudaErrorNotSupported;
-
-    CUtensorMap tmW1, tmX, tmW2, tmAct;
-    const uint64_t E = static_cast<uint64_t>(w->E_local);
-    if (!encode_bf16_2d(&tmW1, w->w1, K, E * 2 * N, kBM) ||
-        !encode_bf16_2d(&tmX, p.x, K, p.rows_alloc, L.bt) ||
-        !encode_bf16_2d(&tmW2, w->w2, N, E * K, kBM) ||
-        !encode_bf16_2d(&tmAct, act, N, p.rows_alloc, L.bt))
-        return cudaErrorInvalidValue;
-
-    const int grid = dev.sm_count;
-    GemmArgs a1{};
-    a1.offsets = p.offsets;
-    a1.single_rows = p.single_rows;
-    a1.groups = groups;
-    a1.rows_alloc = p.rows_alloc;
-    a1.kr = K;
-    a1.rows_per_group = 2 * N;
-    a1.n_wtiles = L.g1.n_wtiles;
-    a1.wtile_rows = kBM;
-    a1.a1_offset = N;
-    a1.splits = L.g1.splits;
-    a1.out_ld = N;
-    a1.out = act;
-    a1.partials = reinterpret_cast<float*>(ws + L.off_p1);
-    a1.counters = counters1;
-    a1.max_tiles = L.g1.max_tiles;
-    a1.err = err;
-    cudaError_t e = launch_bt<2, MODE_SWIGLU, __nv_bfloat16>(L.bt, tmW1, tmX, a1, grid, s);
-    if (e != cudaSuccess) return e;
-
-    GemmArgs a2 = a1;
-    a2.kr = N;
-    a2.rows_per_group = K;
-    a2.n_wtiles = L.g2.n_wtiles;
-    a2.wtile_rows = L.g2.na * kBM;
-    a2.a1_offset = kBM;
-    a2.splits = L.g2.splits;
-    a2.out_ld = K;
-    a2.out = p.y;
-    a2.partials = reinterpret_cast<float*>(ws + L.off_p2);
-    a2.counters = counters2;
-    a2.max_tiles = L.g2.max_tiles;
-    if (L.g2.na == 2) {
-        if (p.y_dtype == MOE_DTYPE_F32) return launch_bt<2, MODE_PLAIN, float>(L.bt, tmW2, tmAct, a2, grid, s);
-        return launch_bt<2, MODE_PLAIN, __nv_bfloat16>(L.bt, tmW2, tmAct, a2, grid, s);
-    }
-    if (p.y_dtype == MOE_DTYPE_F32) return launch_bt<1, MODE_PLAIN, float>(L.bt, tmW2, tmAct, a2, grid, s);
-    return launch_bt<1, MODE_PLAIN, __nv_bfloat16>(L.bt, tmW2, tmAct, a2, grid, s);
-}
-
+}  // namespace gemm
 }  // namespace moe

@@ -89,6 +89,8 @@ moe_status check_weights(const moe_weights* w) {
     if (w->format == MOE_WEIGHTS_MXFP4) {
         if (w->w1_scale == nullptr || w->w2_scale == nullptr) return MOE_ERR_INVALID_ARG;
         if (!aligned16(w->w1_scale) || !aligned16(w->w2_scale)) return MOE_ERR_ALIGNMENT;
+        // scale rows of K/32 and N/32 bytes must be 16-byte multiples for the TMA
+        if (w->K % 512 != 0 || w->N % 512 != 0) return MOE_ERR_ALIGNMENT;
     } else if (w->w1_scale != nullptr || w->w2_scale != nullptr) {
         return MOE_ERR_INVALID_ARG;
     }
@@ -148,6 +150,16 @@ moe_status moe_get_error(cudaStream_t stream) {
         if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
     }
     return static_cast<moe_status>(v);
+}
+
+moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles) {
+    if (token_tile != 0 && token_tile != 16 && token_tile != 32 && token_tile != 64 && token_tile != 128 &&
+        token_tile != 256)
+        return MOE_ERR_INVALID_ARG;
+    if (splits_gemm1 < 0 || splits_gemm1 > 64 || splits_gemm2 < 0 || splits_gemm2 > 64) return MOE_ERR_INVALID_ARG;
+    if (gemm2_tiles < 0 || gemm2_tiles > 2) return MOE_ERR_INVALID_ARG;
+    moe::set_plan_override(token_tile, splits_gemm1, splits_gemm2, gemm2_tiles);
+    return MOE_OK;
 }
 
 moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream) {
@@ -279,7 +291,6 @@ moe_status moe_experts(const moe_weights* w, const void* x_perm, const int32_t* 
     if (M == 0) return MOE_OK;                                          // nothing arrives: empty output
     if (x_perm == nullptr || expert_offsets == nullptr || gemm2_permuted == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x_perm) || !aligned16(gemm2_permuted)) return MOE_ERR_ALIGNMENT;
-    if (w->format != MOE_WEIGHTS_BF16) return MOE_ERR_UNSUPPORTED;
     DeviceInfo info;
     int* err = nullptr;
     const moe_status st = device_gate(&info, &err);

@@ -48,6 +48,8 @@ __device__ __forceinline__ int local_expert(const int32_t* __restrict__ ids,
 __device__ void chunk_ranks(const int32_t* ids, const int32_t* emap, int chunk_base, int n,
                             int E, int E_l, int* hist, int* chunk_total, int* err,
                             int& le, int& rank) {
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, W = blockDim.x >> 5;
     for (int i = tid; i < W * E_l; i += blockDim.x) hist[i] = 0;
     __syncthreads();
@@ -139,6 +141,8 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchu
     extern __shared__ int sm[];
     int* total = sm;                         // [E_l]
     int* tmp = total + E_l;                  // [33]
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < E_l; e += blockDim.x) {
         int run = 0;
         for (int c = 0; c < nchunks; ++c) {
@@ -184,6 +188,8 @@ __global__ void permute_gather_kernel(const int32_t* __restrict__ offsets, int E
                                       const int32_t* __restrict__ inverse, int top_k,
                                       const __nv_bfloat16* __restrict__ x, int K,
                                       __nv_bfloat16* __restrict__ x_perm) {
+    pdl_wait();
+    pdl_trigger();
     const int R = __ldg(offsets + E_l);
     const int warps = blockDim.x >> 5;
     const int n16 = K / 8;
@@ -222,22 +228,26 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
             grid = ceil_div(n, W);
             grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
         }
-        permute_fused_kernel<<<grid, threads, smem, s>>>(ids, n, top_k, E, emap, E_l, xb, K,
-                                                        offsets, map, inverse, xp, err);
-        return cudaGetLastError();
+        return launch_pdl(permute_fused_kernel, dim3(grid), dim3(threads), smem, s, ids, n, top_k, E, emap, E_l,
+                          xb, K, offsets, map, inverse, xp, err);
     }
     int32_t* chunk = static_cast<int32_t*>(ws);
     const size_t smem_h = sizeof(int) * (W * E_l + E_l);
-    permute_count_kernel<<<nchunks, threads, smem_h, s>>>(ids, n, E, emap, E_l, chunk, err);
-    permute_scan_kernel<<<1, 1024, sizeof(int) * (E_l + 33), s>>>(chunk, nchunks, E_l, offsets);
-    permute_scatter_kernel<<<nchunks, threads, smem_h, s>>>(ids, n, E, emap, E_l, chunk, map, inverse);
-    if (x_perm != nullptr) {
-        const int rows_per_block = 8;   // 256 threads, one warp per row
-        int grid = ceil_div(n, rows_per_block);
-        if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
-        permute_gather_kernel<<<grid, 32 * rows_per_block, 0, s>>>(offsets, E_l, inverse, top_k, xb, K, xp);
-    }
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nchunks), dim3(threads), smem_h, s, ids, n, E, emap,
+                               E_l, chunk, err);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), sizeof(int) * (E_l + 33), s, chunk, nchunks, E_l,
+                   offsets);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(permute_scatter_kernel, dim3(nchunks), dim3(threads), smem_h, s, ids, n, E, emap, E_l,
+                   static_cast<const int32_t*>(chunk), map, inverse);
+    if (e != cudaSuccess || x_perm == nullptr) return e;
+    const int rows_per_block = 8;   // 256 threads, one warp per row
+    int grid = ceil_div(n, rows_per_block);
+    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    return launch_pdl(permute_gather_kernel, dim3(grid), dim3(32 * rows_per_block), 0, s,
+                      static_cast<const int32_t*>(offsets), E_l, static_cast<const int32_t*>(inverse), top_k, xb,
+                      K, xp);
 }
 
 }  // namespace moe

@@ -121,6 +121,8 @@ template <int SLOTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_softmax_kernel(const float* __restrict__ logits, int M, int E, int top_k, float rsf,
                      int32_t* __restrict__ ids, void* __restrict__ weights, int wdtype) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= M) return;
@@ -152,6 +154,8 @@ route_sigmoid_grouped_kernel(const float* __restrict__ logits, const float* __re
                              int M, int E, int top_k, int n_group, int topk_group, float rsf,
                              int32_t* __restrict__ ids, void* __restrict__ weights, int wdtype) {
     extern __shared__ float sh_b[];          // [kWarpsPerBlock][E] biased scores
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kWarpsPerBlock + warp;
@@ -220,14 +224,12 @@ cudaError_t launch_route_slots(const float* logits, int M, int E, int top_k, int
                                const float* bias, int n_group, int topk_group, float rsf,
                                int32_t* ids, void* w, int wdtype, cudaStream_t s) {
     const dim3 grid(ceil_div(M, kWarpsPerBlock)), block(kWarpsPerBlock * 32);
-    if (method == MOE_ROUTE_SOFTMAX_TOPK) {
-        route_softmax_kernel<SLOTS><<<grid, block, 0, s>>>(logits, M, E, top_k, rsf, ids, w, wdtype);
-    } else {
-        const size_t smem = sizeof(float) * kWarpsPerBlock * E;   // <= 32 KB for E <= 1024
-        route_sigmoid_grouped_kernel<SLOTS><<<grid, block, smem, s>>>(
-            logits, bias, M, E, top_k, n_group, topk_group, rsf, ids, w, wdtype);
-    }
-    return cudaGetLastError();
+    if (method == MOE_ROUTE_SOFTMAX_TOPK)
+        return launch_pdl(route_softmax_kernel<SLOTS>, grid, block, 0, s, logits, M, E, top_k, rsf, ids, w,
+                          wdtype);
+    const size_t smem = sizeof(float) * kWarpsPerBlock * E;   // <= 32 KB for E <= 1024
+    return launch_pdl(route_sigmoid_grouped_kernel<SLOTS>, grid, block, smem, s, logits, bias, M, E, top_k,
+                      n_group, topk_group, rsf, ids, w, wdtype);
 }
 
 }  // namespace

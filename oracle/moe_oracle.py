@@ -81,14 +81,21 @@ def ue8m0_scale(s) -> np.ndarray:
 
 
 def bf16_round(x) -> np.ndarray:
-    """float -> nearest bfloat16 (ties to even), returned as float32 values."""
+    """float -> nearest bfloat16 (ties to even), returned as float32 values.
+
+    Works on the float32 bit pattern: add 0x7FFF plus the lowest kept bit,
+    then clear the low 16 bits (for finite inputs and infinities this cannot
+    overflow 32 bits); NaN stays NaN."""
     f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    u = f.view(np.uint32).astype(np.uint64)
+    u = f.view(np.uint32)
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += u
+    r += np.uint32(0x7FFF)
+    r &= np.uint32(0xFFFF0000)
+    out = r.view(np.float32)
     nan = np.isnan(f)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    u = (u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
-    out = u.astype(np.uint32).view(np.float32).copy()
-    out[nan] = np.float32(np.nan)
+    if nan.any():
+        out[nan] = np.float32(np.nan)
     return out
 
 
@@ -110,9 +117,9 @@ def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
     vals = np.empty((rows, C), dtype=np.float32)
     vals[:, 0::2] = table[packed & 0x0F]
     vals[:, 1::2] = table[packed >> 4]
-    sf = np.repeat(ue8m0_scale(scales), 32, axis=1)
+    sf = ue8m0_scale(scales)                              # [rows, C/32], one scale per 32 values
     with np.errstate(over="ignore", invalid="ignore"):
-        prod = vals * sf
+        prod = (vals.reshape(rows, C // 32, 32) * sf[:, :, None]).reshape(rows, C)
     return bf16_round(prod).astype(np.float64)
 
 

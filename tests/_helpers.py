@@ -25,12 +25,16 @@ def max_err(got, ref):
     return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))))
 
 
+_DEQ_CACHE = {}
+
+
 class ExpertsF64:
     """``[e]`` -> float64 numpy weights of local expert e, converted lazily
-    (bf16 tensors, or MXFP4 bytes dequantised by the oracle)."""
+    (bf16 tensors, or MXFP4 bytes dequantised by the oracle; the latter kept
+    in a bounded cache, since dequantising one expert takes seconds)."""
 
-    def __init__(self, w, scale=None):
-        self.w, self.scale = w, scale
+    def __init__(self, w, scale=None, cache=64):
+        self.w, self.scale, self.cache = w, scale, cache
 
     def __len__(self):
         return self.w.shape[0]
@@ -38,7 +42,13 @@ class ExpertsF64:
     def __getitem__(self, e):
         if self.scale is None:
             return self.w[e].to(torch.float64).cpu().numpy()
-        return O.dequant_mxfp4(self.w[e].cpu().numpy(), self.scale[e].cpu().numpy())
+        key = (self.w.data_ptr(), tuple(self.w.shape), int(e))
+        if key not in _DEQ_CACHE:
+            if len(_DEQ_CACHE) >= self.cache:
+                _DEQ_CACHE.pop(next(iter(_DEQ_CACHE)))
+            _DEQ_CACHE[key] = O.dequant_mxfp4(self.w[e].cpu().numpy(),
+                                              self.scale[e].cpu().numpy()).astype(np.float32)
+        return _DEQ_CACHE[key].astype(np.float64)
 
     @property
     def shape(self):
@@ -82,6 +92,25 @@ def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None,
     sh = None if shared is None else shared[tokens]
     out = O.finalize(g2, weights[tokens], pmap, sh, rsf)
     return out, {(tokens[a], j): y for (a, j), y in ys.items()}
+
+
+def sample_tokens_few_experts(ids, n, budget, seed=0):
+    """Up to n tokens whose routes together touch at most ``budget`` experts
+    (the first and last token always considered), for oracles whose cost is
+    per expert."""
+    M = ids.shape[0]
+    order = [0, M - 1] + np.random.default_rng(seed).permutation(M).tolist()
+    seen, toks = set(), []
+    for t in order:
+        if t in toks:
+            continue
+        new = set(int(e) for e in ids[t]) - seen
+        if len(seen) + len(new) <= budget:
+            seen |= new
+            toks.append(int(t))
+        if len(toks) >= n:
+            break
+    return sorted(toks)
 
 
 def sample_tokens(M, n=256, seed=0):

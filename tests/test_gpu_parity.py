@@ -15,7 +15,7 @@ import torch
 
 import oracle as O
 import synth
-from _helpers import ExpertsF64, lib, max_err, oracle_tokens, sample_tokens, tol
+from _helpers import ExpertsF64, lib, max_err, oracle_tokens, sample_tokens, sample_tokens_few_experts, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -217,7 +217,10 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
     assert np.array_equal(b.pmap.cpu().numpy(), r_map)
 
     # values on a token sample (all tokens when M <= sample size)
-    toks = sample_tokens(M, sample or 256)
+    if cfg.weight_format == "mxfp4":
+        toks = sample_tokens_few_experts(rid, sample or 16, budget=48, seed=M)
+    else:
+        toks = sample_tokens(M, sample or 256)
     xs = x.to(torch.float64).cpu().numpy()
     w1 = ExpertsF64(kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale))
     w2 = ExpertsF64(kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale))
@@ -265,6 +268,41 @@ def test_layer_qwen3(moe, M):
 @pytest.mark.parametrize("M", [1, 8, 64, 512, 4096, 8192])
 def test_layer_mixtral(moe, M):
     _check_layer(moe, "mixtral", M, sample=128 if M > 64 else None)
+
+
+@pytest.mark.parametrize("M", [1, 64, 1024, 8192])
+def test_layer_deepseek_mxfp4(moe, M):
+    """DeepSeek-V3-shaped layer: sigmoid grouped router, MXFP4 routed experts,
+    bf16 shared expert; 3e-2 * RMS against the oracle on the same bytes."""
+    _check_layer(moe, "deepseek", M, sample=16)
+
+
+def test_mxfp4_decode_all_codes(moe):
+    """Random e2m1 codes (all 16 values, uniformly) under a spread of scale
+    bytes, compared over the whole output with the MXFP4 path's bar
+    (3e-2 * RMS) against the oracle on the same bytes. A decode error (nibble
+    order, sign, scale exponent) would be of the order of the values."""
+    g = torch.Generator(device="cpu").manual_seed(21)
+    E, K, N, M, k = 4, 512, 512, 48, 2
+    p1 = torch.randint(0, 256, (E, 2 * N, K // 2), generator=g, dtype=torch.uint8)
+    s1 = torch.randint(112, 127, (E, 2 * N, K // 32), generator=g, dtype=torch.uint8)
+    p2 = torch.randint(0, 256, (E, K, N // 2), generator=g, dtype=torch.uint8)
+    s2 = torch.randint(110, 125, (E, K, N // 32), generator=g, dtype=torch.uint8)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    logits = torch.randn(M, E, generator=g)
+    lay = moe.MoELayer(K=K, N=N, E=E, top_k=k, w1=p1.to(DEV), w2=p2.to(DEV), w1_scale=s1.to(DEV),
+                       w2_scale=s2.to(DEV), fmt=moe.MOE_WEIGHTS_MXFP4)
+    b = lay.forward(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    check_no_device_error(moe)
+    w1 = np.stack([O.dequant_mxfp4(p1[e].numpy(), s1[e].numpy()) for e in range(E)])
+    w2 = np.stack([O.dequant_mxfp4(p2[e].numpy(), s2[e].numpy()) for e in range(E)])
+    r = O.moe_forward(x.double().numpy(), logits.numpy(), w1, w2, k)
+    assert np.array_equal(b.pmap.cpu().numpy(), r["map"])
+    got = b.out.double().cpu().numpy()
+    assert max_err(got, r["out"]) <= tol(r["out"], 3e-2, 0.0)
+    R = int(r["offsets"][-1])
+    assert max_err(b.gemm2[:R].double().cpu().numpy(), r["gemm2_permuted"]) <= tol(r["gemm2_permuted"], 3e-2, 0.0)
 
 
 def test_masked_stress_deferred_finalize(moe):
