@@ -64,12 +64,22 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The slowest rank's time (replicas: the job ends when the last one does)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v, world, device="cuda"):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -159,10 +169,12 @@ def launches_per_forward(cfg, M):
     n = 1                                                     # router
     w = max(1, min(32, 8192 // cfg.E))
     n += 1 if M * cfg.top_k <= 32 * w else 4                  # permute: fused, or count/scan/scatter/gather
-    n += 2                                                    # grouped GEMM1, GEMM2
+    # grouped GEMM1 + GEMM2: one fused launch when GEMM2 units take two
+    # 128-row weight tiles (K % 256 == 0), else two launches
+    n += 1 if cfg.K % 256 == 0 else 2
     n += 1                                                    # finalize
     if cfg.shared_N:
-        n += 2                                                # shared expert GEMM1, GEMM2
+        n += 1 if cfg.K % 256 == 0 else 2                     # shared expert (same kernel, one group)
     return n
 
 
@@ -179,16 +191,9 @@ def roofline_layer(cfg, M, touched, pk, sustained=True):
     return max(wbytes / (pk["hbm"] * 1e9), flops / tc), wbytes, flops
 
 
-def run_gpu(args):
-    import mixture_experts_layer_15_gb300 as moe
-    rank, world = dist_init(args.gpus)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    pk = peaks()
-    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts)
-    sweep = sorted(batches)
-    stream = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-
+def make_forward(moe, cfg, layer, batches, stream):
+    """One layer forward at batch size M through the C ABI: route, permute,
+    [shared expert], experts (GEMM1, GEMM2; ``ev`` brackets them), finalize."""
     def forward(M, ev=None):
         x, logits = batches[M]
         b = layer.buffers(M)
@@ -208,10 +213,13 @@ def run_gpu(args):
         rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
         moe.moe_finalize(b.gemm2, layer.gemm2_dtype, b.gemm2.shape[0], b.topk_weights, layer.weights_dtype,
                          b.pmap, M, cfg.top_k, cfg.K, b.shared, layer.gemm2_dtype, rsf, b.out, layer.out_dtype)
+    return forward
 
+
+def warm_up(moe, layer, sweep, forward, warmup):
     for M in sweep:                                # allocate buffers outside any timing
         layer.buffers(M)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         for M in sweep:
             forward(M)
     torch.cuda.synchronize()
@@ -219,63 +227,111 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device error during warm-up: {moe.status_string(st)}")
 
-    # touched experts per M (from the device's own routing)
-    touched = {M: int((layer.buffers(M).offsets.diff() > 0).sum().item()) for M in sweep}
 
-    ev_m = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)] for M in sweep}
-    ev_g = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)] for M in sweep}
+def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clocks=None, reps=5):
+    """K timed steps of the whole sweep, with CUDA events only around the timed
+    region (events between the kernels of a forward would break their
+    programmatic-dependent-launch chaining). Then a per-M breakdown: for each
+    M, ``reps`` single forwards (and single experts calls), each after an L2
+    flush, each bracketed by events. Returns (seconds over all steps, per-M
+    breakdown, GEMM FLOPs, GEMM seconds, clocks)."""
+    touched = {M: int((layer.buffers(M).offsets.diff() > 0).sum().item()) for M in sweep}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
+    if clocks is not None:
+        clocks.start()
     t0.record(stream)
-    for s in range(args.steps):
+    for _ in range(steps):
         for M in sweep:
-            ev_m[M][s][0].record(stream)
-            forward(M, ev_g[M][s])
-            ev_m[M][s][1].record(stream)
+            forward(M)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     st = moe.moe_get_error()
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {moe.status_string(st)}")
     secs = t0.elapsed_time(t1) / 1e3
-    secs_max = max_over_ranks(secs, world)
-    tokens_step = sum(sweep)
-    value = tokens_step * args.steps * world / secs_max
 
-    # per-M breakdown and the grouped-GEMM roofline
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device)   # 256 MB > L2
     per_m = []
     gemm_flops = gemm_secs = 0.0
     for M in sweep:
-        tm = sum(a.elapsed_time(b) for a, b in ev_m[M]) / 1e3 / args.steps
-        tg = sum(a.elapsed_time(b) for a, b in ev_g[M]) / 1e3 / args.steps
+        tf, tg = [], []
+        for r in range(reps):
+            for which, acc in ((0, tf), (1, tg)):
+                flush.fill_(r & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                if which == 0:
+                    e0.record(stream)
+                    forward(M)
+                    e1.record(stream)
+                else:
+                    forward(M, (e0, e1))
+                torch.cuda.synchronize()
+                acc.append(e0.elapsed_time(e1) / 1e3)
+        tm, tgm = statistics.median(tf), statistics.median(tg)
         troof, wbytes, flops = roofline_layer(cfg, M, touched[M], pk)
         gf = 6.0 * cfg.K * cfg.N * M * cfg.top_k
         gemm_flops += gf
-        gemm_secs += tg
-        per_m.append({"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tg * 1e3,
+        gemm_secs += tgm
+        per_m.append({"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tgm * 1e3,
                       "touched_experts": touched[M], "roofline_ms": troof * 1e3,
                       "roofline_frac": troof / tm,
                       "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= flops / (pk["bf16_sus"] * 1e12) else "tensor",
-                      "gemm_tflops": gf / tg / 1e12, "gemm_weight_gbs": wbytes / tg / 1e9})
+                      "gemm_tflops": gf / tgm / 1e12})
+    del flush
+    return secs, per_m, gemm_flops, gemm_secs, clk
+
+
+def other_config(moe, name, args, pk, dev, stream):
+    """The same measurement on another config (reported beside the headline)."""
+    cfg, li, layer, batches = make_workload(name, dev)
+    sweep = sorted(batches)
+    forward = make_forward(moe, cfg, layer, batches, stream)
+    warm_up(moe, layer, sweep, forward, 3)
+    steps = max(5, args.steps // 5)
+    secs, per_m, gf, gs, _ = timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk)
+    out = {"workload": f"{cfg.name}-shaped MoE layer (K={cfg.K}, N={cfg.N}, E={cfg.E}, top_k={cfg.top_k}, "
+                       f"{cfg.weight_format} weights{', shared expert' if cfg.shared_N else ''})",
+           "tokens_per_s": sum(sweep) * steps / secs, "steps": steps, "gemm_tflops": gf / gs / 1e12,
+           "sweep": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()} for r in per_m]}
+    del layer, li, batches
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args):
+    import mixture_experts_layer_15_gb300 as moe
+    rank, world = dist_init(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts)
+    sweep = sorted(batches)
+    forward = make_forward(moe, cfg, layer, batches, stream)
+    warm_up(moe, layer, sweep, forward, args.warmup)
+    clocks = ClockSampler(torch.cuda.current_device())
+    secs, per_m, gemm_flops, gemm_secs, clk = timed_sweep(moe, cfg, layer, sweep, forward, args.steps, stream,
+                                                          pk, world, clocks)
+    secs_max = max_over_ranks(secs, world)
+    tokens_step = sum(sweep)
+    value = tokens_step * args.steps * world / secs_max
     achieved = gemm_flops / gemm_secs / 1e12
-    traffic = None
+    traffic = tcase = talg = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
+    if os.path.exists(tpath) and not (args.m or args.experts):
         try:
-            traffic = json.load(open(tpath)).get(args.config)
+            t = json.load(open(tpath)).get(args.config) or {}
+            traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
         except Exception:
             traffic = None
-    roof = {"kernel": "grouped_gemm_kernel (GEMM1+silu_and_mul and GEMM2, 2 launches per forward)",
+    roof = {"kernel": "grouped_gemm_kernel (GEMM1+silu_and_mul and GEMM2 in one launch per forward)",
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
             "frac": achieved / pk["bf16_sus"], "peak_kind": f"{pk['src']} bf16 sustained",
-            "frac_of_burst": achieved / pk["bf16"], "traffic": traffic,
+            "frac_of_burst": achieved / pk["bf16"], "traffic": traffic, "traffic_case": tcase,
+            "traffic_algorithmic": talg,
             "algorithmic": "6*K*N*routes FLOPs per forward over the sweep"}
 
     e2e = run_e2e(args, cfg, layer, batches, forward_fn=forward)
@@ -295,6 +351,11 @@ def run_gpu(args):
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(cfg, li, batches, args)
+        if args.others and not args.m and not args.experts:
+            del layer, batches
+            torch.cuda.empty_cache()
+            line["other_configs"] = {name: other_config(moe, name, args, pk, dev, stream)
+                                     for name in args.others.split(",") if name and name != args.config}
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -450,6 +511,8 @@ def main():
     ap.add_argument("--m", type=int, nargs="*", default=None,
                     help="run only these batch sizes of the sweep (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling)")
+    ap.add_argument("--others", default="qwen3,deepseek",
+                    help="other configs measured after the headline one and reported beside it ('' = none)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: keep the first N experts of the config (not the benchmark workload)")
     args = ap.parse_args()

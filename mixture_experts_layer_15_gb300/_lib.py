@@ -83,7 +83,7 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_get_error": ([_P], _I),
     "moe_device_check": ([], _I),
-    "moe_set_plan_override": ([_I, _I, _I, _I], _I),
+    "moe_set_plan_override": ([_I, _I, _I, _I, _I], _I),
     "moe_debug_sigmoid": ([_P, _P, _I, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -204,9 +204,9 @@ def moe_device_check() -> int:
     return int(lib.moe_device_check())
 
 
-def moe_set_plan_override(token_tile=0, splits_gemm1=0, splits_gemm2=0, gemm2_tiles=0):
+def moe_set_plan_override(token_tile=0, splits_gemm1=0, splits_gemm2=0, gemm2_tiles=0, fuse=0):
     _check("moe_set_plan_override", lib.moe_set_plan_override(token_tile, splits_gemm1, splits_gemm2,
-                                                              gemm2_tiles))
+                                                              gemm2_tiles, fuse))
 
 
 def moe_debug_sigmoid(x, y, n, stream=None):

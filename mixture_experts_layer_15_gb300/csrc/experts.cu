@@ -53,6 +53,7 @@ struct PlanOverride {
     int token_tile = 0;          // 0 = automatic
     int splits[2] = {0, 0};      // GEMM1, GEMM2; 0 = automatic
     int gemm2_na = 0;            // 128-row A tiles per GEMM2 unit (1 or 2); 0 = automatic
+    int fuse = 0;                // 0 = automatic, 1 = one fused launch, 2 = two launches
 };
 PlanOverride g_override;
 
@@ -113,6 +114,8 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
     int bt;
+    bool fused;
+    int max_token_tiles;
     GemmPlan g1, g2;
     size_t off_act, off_p1, off_p2, total;
 };
@@ -126,7 +129,13 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     int na2 = (K % 256 == 0) ? 2 : 1;
     if (g_override.gemm2_na == 1 || (g_override.gemm2_na == 2 && K % 256 == 0)) na2 = g_override.gemm2_na;
     L.g2 = plan_gemm(1, L.bt, na2, K / (na2 * kBM), N, rows_alloc, groups, sm_count);
-    size_t off = 2 * kMaxSplitTiles * sizeof(int);           // two counter regions, kept zero
+    // GEMM1 and GEMM2 in one launch when GEMM2 units take two A tiles and the
+    // token-tile counters fit their region
+    L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
+    L.fused = L.g2.na == 2 && L.max_token_tiles <= kMaxSplitTiles && g_override.fuse != 2;
+    // four counter regions, kept zero between calls: split-K arrivals of
+    // GEMM1 and GEMM2, token-tile ready and consumed counts
+    size_t off = 4 * kMaxSplitTiles * sizeof(int);
     L.off_act = off;
     off = align256(off + static_cast<size_t>(rows_alloc) * N * 2);
     L.off_p1 = off;
@@ -152,20 +161,20 @@ bool encode_weights(CUtensorMap* tmA, CUtensorMap* tmS, bool mx, const void* w, 
                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-cudaError_t launch_one(bool mx, int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
-                       const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                       cudaStream_t s) {
-    return mx ? gemm::launch_gemm_mxfp4(mode, bt, na, out_dtype, tmA, tmS, tmB, a, grid, s)
-              : gemm::launch_gemm_bf16(mode, bt, na, out_dtype, tmA, tmS, tmB, a, grid, s);
+cudaError_t launch_one(bool mx, int fused, int mode, int bt, int na, int out_dtype, const gemm::Maps& m,
+                       const gemm::KernelArgs& ka, int grid, cudaStream_t s) {
+    return mx ? gemm::launch_gemm_mxfp4(fused, mode, bt, na, out_dtype, m, ka, grid, s)
+              : gemm::launch_gemm_bf16(fused, mode, bt, na, out_dtype, m, ka, grid, s);
 }
 
 }  // namespace
 
-void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na) {
+void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na, int fuse) {
     g_override.token_tile = token_tile;
     g_override.splits[0] = splits1;
     g_override.splits[1] = splits2;
     g_override.gemm2_na = gemm2_na;
+    g_override.fuse = fuse;
 }
 
 size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev) {
@@ -180,19 +189,18 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     const int groups = p.offsets != nullptr ? w->E_local : 1;
     const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* counters1 = reinterpret_cast<int*>(ws);
-    int* counters2 = counters1 + kMaxSplitTiles;
+    int* counters = reinterpret_cast<int*>(ws);
     void* act = ws + L.off_act;
 
-    CUtensorMap tmW1, tmS1, tmX, tmW2, tmS2, tmAct;
+    gemm::Maps m;
     const uint64_t E = static_cast<uint64_t>(w->E_local);
-    if (!encode_weights(&tmW1, &tmS1, mx, w->w1, w->w1_scale, K, E * 2 * N) ||
-        !encode_weights(&tmW2, &tmS2, mx, w->w2, w->w2_scale, N, E * K) ||
-        !encode_bf16(&tmX, p.x, K, p.rows_alloc, L.bt) || !encode_bf16(&tmAct, act, N, p.rows_alloc, L.bt))
+    if (!encode_weights(&m.A[0], &m.S[0], mx, w->w1, w->w1_scale, K, E * 2 * N) ||
+        !encode_weights(&m.A[1], &m.S[1], mx, w->w2, w->w2_scale, N, E * K) ||
+        !encode_bf16(&m.B[0], p.x, K, p.rows_alloc, L.bt) || !encode_bf16(&m.B[1], act, N, p.rows_alloc, L.bt))
         return cudaErrorInvalidValue;
 
-    const int grid = dev.sm_count;
-    GemmArgs a1{};
+    gemm::KernelArgs ka{};
+    GemmArgs& a1 = ka.g[0];
     a1.offsets = p.offsets;
     a1.single_rows = p.single_rows;
     a1.groups = groups;
@@ -206,13 +214,11 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a1.out_ld = N;
     a1.out = act;
     a1.partials = reinterpret_cast<float*>(ws + L.off_p1);
-    a1.counters = counters1;
+    a1.counters = counters;
     a1.max_tiles = L.g1.max_tiles;
     a1.err = err;
-    cudaError_t e = launch_one(mx, gemm::MODE_SWIGLU, L.bt, 2, MOE_DTYPE_BF16, tmW1, tmS1, tmX, a1, grid, s);
-    if (e != cudaSuccess) return e;
-
-    GemmArgs a2 = a1;
+    GemmArgs& a2 = ka.g[1];
+    a2 = a1;
     a2.kr = N;
     a2.rows_per_group = K;
     a2.n_wtiles = L.g2.n_wtiles;
@@ -222,9 +228,28 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a2.out_ld = K;
     a2.out = p.y;
     a2.partials = reinterpret_cast<float*>(ws + L.off_p2);
-    a2.counters = counters2;
+    a2.counters = counters + kMaxSplitTiles;
     a2.max_tiles = L.g2.max_tiles;
-    return launch_one(mx, gemm::MODE_PLAIN, L.bt, L.g2.na, p.y_dtype, tmW2, tmS2, tmAct, a2, grid, s);
+    ka.ready = counters + 2 * kMaxSplitTiles;
+    ka.consumed = counters + 3 * kMaxSplitTiles;
+    ka.max_token_tiles = L.max_token_tiles;
+
+    const int grid = dev.sm_count;
+    if (L.fused) {
+        ka.nphase = 2;
+        return launch_one(mx, 1, gemm::MODE_PLAIN, L.bt, 2, p.y_dtype, m, ka, grid, s);
+    }
+    ka.nphase = 1;
+    gemm::Maps m1 = m;                                   // phase-0 maps of each launch
+    cudaError_t e = launch_one(mx, 0, gemm::MODE_SWIGLU, L.bt, 2, MOE_DTYPE_BF16, m1, ka, grid, s);
+    if (e != cudaSuccess) return e;
+    gemm::KernelArgs k2 = ka;
+    k2.g[0] = a2;
+    gemm::Maps m2 = m;
+    m2.A[0] = m.A[1];
+    m2.S[0] = m.S[1];
+    m2.B[0] = m.B[1];
+    return launch_one(mx, 0, gemm::MODE_PLAIN, L.bt, L.g2.na, p.y_dtype, m2, k2, grid, s);
 }
 
 }  // namespace moe

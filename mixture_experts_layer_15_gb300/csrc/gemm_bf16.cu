@@ -4,10 +4,9 @@
 namespace moe {
 namespace gemm {
 
-cudaError_t launch_gemm_bf16(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
-                                  const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                                  cudaStream_t s) {
-    return launch_gemm<false>(mode, bt, na, out_dtype, tmA, tmS, tmB, a, grid, s);
+cudaError_t launch_gemm_bf16(int fused, int mode, int bt, int na, int out_dtype, const Maps& m,
+                                  const KernelArgs& ka, int grid, cudaStream_t s) {
+    return launch_gemm<false>(fused, mode, bt, na, out_dtype, m, ka, grid, s);
 }
 
 }  // namespace gemm

@@ -26,13 +26,14 @@
 //              shared-memory ring (full/empty mbarriers);
 //   warp 1     TMEM allocator and MMA issuer (one thread), commits free ring
 //              slots and signals finished accumulators;
-//   warps 2-9  epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
-//              lanes 32*(w%4).., the two warps of a lane quarter take
-//              alternate 16-column chunks), activation, masked stores by row;
-//   warps 10-13 (MXFP4 weights only) converters: decode the packed e2m1 codes
+//   epilogue   8 warps (bf16 weights) or 4 (MXFP4): tcgen05.ld of the
+//              accumulators (warp w reads TMEM lanes 32*(w%4)..; with 8 warps
+//              the two warps of a lane quarter take alternate 16-column
+//              chunks), activation, masked stores by row;
+//   converters 8 warps (MXFP4 weights only): decode the packed e2m1 codes
 //              and their E8M0 scales (flashinfer_moe_ep.py, _E2M1_LUT and
 //              _dequant_fp4_ue8m0_gran32) to bf16 in the 128-byte-swizzled
-//              layout the MMA reads, one weight row per thread.
+//              layout the MMA reads, two threads per weight row.
 // Accumulators are double-buffered in TMEM when 2 x (2 x BT) <= 512 columns,
 // so the epilogue of one unit overlaps the mainloop of the next.
 //
@@ -75,9 +76,13 @@ using namespace ptx;
 
 constexpr int kBM = 128;                  // weight rows per A tile (MMA M)
 constexpr int kBK = 64;                   // reduction elements per ring stage (128 B of bf16)
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kConvThreads = 128;
+// Warp budget per CTA: bf16 weights use 8 epilogue warps; MXFP4 weights use
+// 4 epilogue warps and 8 converter warps (the decode is the heavier job).
+template <bool MX> struct Warps {
+    static constexpr int EPI = MX ? 4 : 8;
+    static constexpr int EPI_THREADS = 32 * EPI;
+    static constexpr int CONV_THREADS = MX ? 256 : 0;
+};
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxSplitTiles = 16384;     // capacity of one counter region
@@ -104,9 +109,23 @@ struct GemmArgs {
     int* err;
 };
 
+// Arguments of one launch: a single GEMM (nphase = 1), or GEMM1 followed by
+// GEMM2 in the same persistent grid (nphase = 2). In the fused form a GEMM2
+// unit may only read the act rows of its token tile once every GEMM1 weight
+// tile of that token tile has been written: ready[t] counts those tiles,
+// consumed[t] counts the GEMM2 units that have loaded the tile; the last one
+// returns both to zero, so the counters are zero between calls.
+struct KernelArgs {
+    GemmArgs g[2];
+    int nphase;
+    int* ready;                  // [token tiles]
+    int* consumed;               // [token tiles]
+    int max_token_tiles;
+};
+
 template <int BT, int NA, bool MX>
 struct Cfg {
-    static constexpr int THREADS = 64 + kEpiThreads + (MX ? kConvThreads : 0);
+    static constexpr int THREADS = 64 + Warps<MX>::EPI_THREADS + Warps<MX>::CONV_THREADS;
     static constexpr int A_BYTES = kBM * kBK * 2;                 // bf16 A tile (TMA'd or decoded)
     static constexpr int RAW_BYTES = kBM * kBK / 2;               // packed e2m1 A tile
     static constexpr int SC_BYTES = kBM * 16;                     // scale tile: 8 k-blocks of scales
@@ -116,7 +135,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
     static constexpr int DSTAGES = MX ? (BT >= 128 ? 2 : 3) : 0;  // decoded-A ring (MXFP4)
     static constexpr int DSTAGE_BYTES = NA * A_BYTES;
-    static constexpr int STAGES_FIT = (kSmemBudget - 12 * 1024 - DSTAGES * DSTAGE_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (kSmemBudget - 20 * 1024 - DSTAGES * DSTAGE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int ACC_COLS = NA * BT;
     static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
@@ -129,8 +148,9 @@ struct Cfg {
     // full[S], empty[S], dfull[DS], dempty[DS], tfull[2], tempty[2], drain
     static constexpr int NUM_BARS = 2 * STAGES + 2 * DSTAGES + 5;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort, last flag
-    static constexpr int OFF_PREFIX = OFF_MISC + 16;              // [kMaxGroups+1]
-    static constexpr int OFF_OFFS = OFF_PREFIX + (kMaxGroups + 1) * 4;   // [kMaxGroups+1]
+    static constexpr int OFF_PREFIX = OFF_MISC + 16;              // [2][kMaxGroups+1] units per phase
+    static constexpr int OFF_TTP = OFF_PREFIX + 2 * (kMaxGroups + 1) * 4;  // [kMaxGroups+1] token tiles
+    static constexpr int OFF_OFFS = OFF_TTP + (kMaxGroups + 1) * 4;      // [kMaxGroups+1]
     static constexpr int OFF_TMP = OFF_OFFS + (kMaxGroups + 1) * 4;      // [33]
     static constexpr int SMEM_BYTES = OFF_TMP + 33 * 4 + 1024;   // + alignment slack
     static_assert(STAGES >= 2, "ring too shallow");
@@ -188,6 +208,30 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
+}
+
+// Bounded wait until *p >= target (acquire, gpu scope). Same give-up rules as
+// wait_bar.
+__device__ __forceinline__ bool wait_counter(const int* p, int target, volatile int* abort_flag, int* err) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                set_error(err, MOE_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -254,31 +298,39 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t scale2, uint32_t (&
     }
 }
 
-// One weight row of one k-block: 32 packed bytes + 2 scale bytes -> 64 bf16
-// written into the 128-byte-swizzled K-major tile (row r, 16-byte chunk c at
-// chunk position c ^ (r & 7); the tile base is 1024-byte aligned).
-__device__ __forceinline__ void decode_row(const uint8_t* raw_row, uint32_t sc0, uint32_t sc1,
-                                           uint8_t* dec_tile, int r) {
-    const uint4 p0 = *reinterpret_cast<const uint4*>(raw_row);
-    const uint4 p1 = *reinterpret_cast<const uint4*>(raw_row + 16);
-    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+// Half a weight row of one k-block: 16 packed bytes (32 codes) + their scale
+// byte -> 32 bf16, written into the 128-byte-swizzled K-major tile (row r,
+// 16-byte chunk c at chunk position c ^ (r & 7); the tile base is 1024-byte
+// aligned). Half h covers chunks 4h .. 4h+3.
+__device__ __forceinline__ void decode_half(const uint8_t* raw, uint32_t sc, uint8_t* dec_tile, int r, int h) {
+    const uint4 p = *reinterpret_cast<const uint4*>(raw);
+    const uint32_t words[4] = {p.x, p.y, p.z, p.w};
     // bf16 2^(s-127) has exponent field s and a zero mantissa: bits s << 7
-    const uint32_t s2a = (sc0 << 7) | (sc0 << 23);
-    const uint32_t s2b = (sc1 << 7) | (sc1 << 23);
+    const uint32_t s2 = (sc << 7) | (sc << 23);
     uint8_t* row = dec_tile + r * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int j = 0; j < 4; ++j) {
+        const int c = 4 * h + j;
         uint32_t o[4];
-        decode8(words[c], c < 4 ? s2a : s2b, o);
+        decode8(words[j], s2, o);
         *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
-template <int BT, int NA, int MODE, typename OutT, bool MX>
+// MODE/OutT describe phase 0 of a single-GEMM launch. A fused launch
+// (FUSED = true, NA = 2) runs GEMM1 (silu_and_mul, bf16 act) as phase 0 and
+// GEMM2 (plain, OutT) as phase 1.
+template <int BT, int NA, int MODE, typename OutT, bool MX, bool FUSED>
 __global__ void __launch_bounds__(Cfg<BT, NA, MX>::THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
-                    const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmS0,
+                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmB1,
+                    const KernelArgs ka) {
     using C = Cfg<BT, NA, MX>;
+    static_assert(!FUSED || NA == 2, "fused launches use two A tiles per unit");
+    constexpr int kEpiWarps = Warps<MX>::EPI;
+    constexpr int kEpiThreads = Warps<MX>::EPI_THREADS;
+    constexpr int kConvThreads = Warps<MX>::CONV_THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -295,9 +347,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-    int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+    int* prefix0 = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+    int* prefix1 = prefix0 + (kMaxGroups + 1);
+    int* ttp = reinterpret_cast<int*>(smem + C::OFF_TTP);
     int* offs = reinterpret_cast<int*>(smem + C::OFF_OFFS);
     int* tmp = reinterpret_cast<int*>(smem + C::OFF_TMP);
+    const GemmArgs& a0 = ka.g[0];
+    const int groups = a0.groups;
 
     // ---- prologue: barriers, TMEM, unit schedule ----
     if (tid == 0) {
@@ -317,9 +373,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tmA);
-        if (MX) prefetch_tensormap(&tmS);
-        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmA0);
+        if (MX) prefetch_tensormap(&tmS0);
+        prefetch_tensormap(&tmB0);
+        if (FUSED) {
+            prefetch_tensormap(&tmA1);
+            if (MX) prefetch_tensormap(&tmS1);
+            prefetch_tensormap(&tmB1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -330,25 +391,48 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     pdl_wait();
     pdl_trigger();
     // group offsets (validated: non-decreasing, within the allocation)
-    for (int g = tid; g <= a.groups; g += C::THREADS) {
-        int v = a.offsets != nullptr ? __ldg(a.offsets + g) : (g == 0 ? 0 : a.single_rows);
-        if (v < 0 || v > a.rows_alloc) { set_error(a.err, MOE_ERR_DEVICE_INDEX); v = v < 0 ? 0 : a.rows_alloc; }
+    for (int g = tid; g <= groups; g += C::THREADS) {
+        int v = a0.offsets != nullptr ? __ldg(a0.offsets + g) : (g == 0 ? 0 : a0.single_rows);
+        if (v < 0 || v > a0.rows_alloc) { set_error(a0.err, MOE_ERR_DEVICE_INDEX); v = v < 0 ? 0 : a0.rows_alloc; }
         offs[g] = v;
     }
     __syncthreads();
-    for (int g = tid; g < a.groups; g += C::THREADS) {
+    for (int g = tid; g < groups; g += C::THREADS) {
         int cnt = offs[g + 1] - offs[g];
-        if (cnt < 0) { set_error(a.err, MOE_ERR_DEVICE_INDEX); cnt = 0; }
-        prefix[g] = ((cnt + BT - 1) / BT) * a.n_wtiles * a.splits;
+        if (cnt < 0) { set_error(a0.err, MOE_ERR_DEVICE_INDEX); cnt = 0; }
+        const int ntt = (cnt + BT - 1) / BT;
+        prefix0[g] = ntt * a0.n_wtiles * a0.splits;
+        if (FUSED) {
+            prefix1[g] = ntt * ka.g[1].n_wtiles * ka.g[1].splits;
+            ttp[g] = ntt;
+        }
     }
     __syncthreads();
-    const int total_units = block_exclusive_scan(prefix, a.groups, tmp);
-    if (tid == 0) prefix[a.groups] = total_units;
+    const int units0 = block_exclusive_scan(prefix0, groups, tmp);
+    int units1 = 0;
+    if (FUSED) {
+        units1 = block_exclusive_scan(prefix1, groups, tmp);
+        const int ntiles = block_exclusive_scan(ttp, groups, tmp);
+        if (ntiles > ka.max_token_tiles) {               // cannot happen with the host's sizing
+            if (tid == 0) set_error(a0.err, MOE_ERR_DEVICE_INDEX);
+            units1 = 0;
+        }
+    }
+    if (tid == 0) { prefix0[groups] = units0; if (FUSED) prefix1[groups] = units1; }
+    const int total_units = units0 + units1;
     // make the TMEM address written by tcgen05.alloc visible to all threads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
+    // unit u -> (phase, decoded unit)
+    auto unit_at = [&](int u, int& ph) -> Unit {
+        ph = (FUSED && u >= units0) ? 1 : 0;
+        return ph ? decode_unit(u - units0, prefix1, offs, BT, ka.g[1]) : decode_unit(u, prefix0, offs, BT, a0);
+    };
+    // global index of a unit's token tile (fused launches)
+    auto tile_index = [&](const Unit& un) { return ttp[un.g] + (un.row0 - offs[un.g]) / BT; };
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -358,30 +442,52 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t issued = 0, issued_phase = 0;       // per-stage: load in flight / its phase
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit(u, prefix, offs, BT, a);
-                const int a0 = un.g * a.rows_per_group + un.wt * a.wtile_rows;
+                int ph;
+                const Unit un = unit_at(u, ph);
+                const GemmArgs& a = ka.g[ph];
+                const CUtensorMap* tA = ph ? &tmA1 : &tmA0;
+                const CUtensorMap* tS = ph ? &tmS1 : &tmS0;
+                const CUtensorMap* tB = ph ? &tmB1 : &tmB0;
+                if (FUSED && ph == 1) {
+                    // the act rows of this token tile must be complete
+                    if (!wait_counter(ka.ready + tile_index(un), ka.g[0].n_wtiles, abort_flag, a0.err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
+                const int a_row = un.g * a.rows_per_group + un.wt * a.wtile_rows;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a0.err)) { ok = false; break; }
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
                     if (MX) {
                         // packed codes: 32 bytes per row per k-block; scales: the
                         // 16-byte group of 8 k-blocks that holds this one
-                        tma_load_2d(st, &tmA, kb * (kBK / 2), a0, full_bar(stage));
-                        tma_load_2d(st + NA * C::RAW_BYTES, &tmS, (kb >> 3) * 16, a0, full_bar(stage));
+                        tma_load_2d(st, tA, kb * (kBK / 2), a_row, full_bar(stage));
+                        tma_load_2d(st + NA * C::RAW_BYTES, tS, (kb >> 3) * 16, a_row, full_bar(stage));
                         if (NA == 2) {
-                            tma_load_2d(st + C::RAW_BYTES, &tmA, kb * (kBK / 2), a0 + a.a1_offset, full_bar(stage));
-                            tma_load_2d(st + NA * C::RAW_BYTES + C::SC_BYTES, &tmS, (kb >> 3) * 16,
-                                        a0 + a.a1_offset, full_bar(stage));
+                            tma_load_2d(st + C::RAW_BYTES, tA, kb * (kBK / 2), a_row + a.a1_offset, full_bar(stage));
+                            tma_load_2d(st + NA * C::RAW_BYTES + C::SC_BYTES, tS, (kb >> 3) * 16,
+                                        a_row + a.a1_offset, full_bar(stage));
                         }
                     } else {
-                        tma_load_2d(st, &tmA, kb * kBK, a0, full_bar(stage));
-                        if (NA == 2) tma_load_2d(st + C::A_BYTES, &tmA, kb * kBK, a0 + a.a1_offset, full_bar(stage));
+                        tma_load_2d(st, tA, kb * kBK, a_row, full_bar(stage));
+                        if (NA == 2) tma_load_2d(st + C::A_BYTES, tA, kb * kBK, a_row + a.a1_offset, full_bar(stage));
                     }
-                    tma_load_2d(st + C::B_OFF, &tmB, kb * kBK, un.row0, full_bar(stage));
+                    tma_load_2d(st + C::B_OFF, tB, kb * kBK, un.row0, full_bar(stage));
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (FUSED && ph == 1 && ok) {
+                    // the last unit to have read this token tile clears its counters
+                    const int t = tile_index(un);
+                    const int done = atomicAdd(ka.consumed + t, 1) + 1;
+                    if (done == ka.g[1].n_wtiles * ka.g[1].splits) {
+                        ka.ready[t] = 0;
+                        ka.consumed[t] = 0;
+                    }
                 }
             }
             if (!ok) {
@@ -403,16 +509,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
-                const Unit un = decode_unit(u, prefix, offs, BT, a);
+                int ph;
+                const Unit un = unit_at(u, ph);
                 const uint32_t idesc = idesc_bf16_f32(kBM, un.ncols);
                 const int buf = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
-                if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a.err)) break;
+                if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a0.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + buf * C::ACC_COLS;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
-                    if (MX && !wait_bar(dfull_bar(dstage), dphase, abort_flag, a.err)) { ok = false; break; }
+                    if (!wait_bar(full_bar(stage), phase, abort_flag, a0.err)) { ok = false; break; }
+                    if (MX && !wait_bar(dfull_bar(dstage), dphase, abort_flag, a0.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     const uint32_t sA0 = MX ? sbase + C::OFF_DEC + dstage * C::DSTAGE_BYTES : st;
@@ -448,12 +555,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int etid = tid - 64;
         const int c_first = 16 * ((warp - 2) >> 2);          // this warp's first 16-column chunk
         constexpr int c_step = 16 * (kEpiWarps / 4);
+        // one unit's outputs from the accumulator values v0/v1 of columns [c0, c0+16)
+        auto emit = [&](int ph, const Unit& un, const GemmArgs& a, int c0, const float (&v0)[16],
+                        const float (&v1)[16]) {
+            if (FUSED) {
+                if (ph == 0) emit16<2, MODE_SWIGLU, __nv_bfloat16>(un, a, row_in_tile, c0, v0, v1);
+                else emit16<2, MODE_PLAIN, OutT>(un, a, row_in_tile, c0, v0, v1);
+            } else {
+                emit16<NA, MODE, OutT>(un, a, row_in_tile, c0, v0, v1);
+            }
+        };
+        // fused launches: after the stores of a finished GEMM1 tile, count it
+        auto signal_ready = [&](int ph, const Unit& un) {
+            if (!FUSED || ph != 0) return;
+            fence_proxy_async_global();                      // act stores -> later TMA reads
+            __threadfence();
+            named_bar_sync(1, kEpiThreads);
+            if (etid == 0) atomicAdd(ka.ready + tile_index(un), 1);
+        };
         int it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
-            const Unit un = decode_unit(u, prefix, offs, BT, a);
+            int ph;
+            const Unit un = unit_at(u, ph);
+            const GemmArgs& a = ka.g[ph];
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
-            wait_bar(tfull_bar(buf), use, abort_flag, a.err);
+            wait_bar(tfull_bar(buf), use, abort_flag, a0.err);
             named_bar_sync(1, kEpiThreads);                  // all threads decide together
             if (*abort_flag) break;
             tc_fence_after();
@@ -464,10 +591,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     float v0[16], v1[16];
                     if (NA == 2) tmem_ld16x2(tb + c0, tb + BT + c0, v0, v1);
                     else tmem_ld16(tb + c0, v0);
-                    emit16<NA, MODE, OutT>(un, a, row_in_tile, c0, v0, v1);
+                    emit(ph, un, a, c0, v0, v1);
                 }
                 tc_fence_before();
                 mbar_arrive(tempty_bar(buf));
+                signal_ready(ph, un);
             } else {
                 const size_t slot = static_cast<size_t>(NA) * kBM * BT;
                 const bool tile_ok = un.tile < a.max_tiles;
@@ -496,7 +624,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         last = (old == a.splits - 1);
                         if (last) a.counters[un.tile] = 0;   // left at zero for the next call
                     } else {
-                        set_error(a.err, MOE_ERR_DEVICE_INDEX);
+                        set_error(a0.err, MOE_ERR_DEVICE_INDEX);
                     }
                     *last_flag = last;
                 }
@@ -518,30 +646,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                 if (NA == 2) v1[i] += __ldcg(ps + static_cast<size_t>(BT + c0 + i) * kBM + row_in_tile);
                             }
                         }
-                        emit16<NA, MODE, OutT>(un, a, row_in_tile, c0, v0, v1);
+                        emit(ph, un, a, c0, v0, v1);
                     }
+                    signal_ready(ph, un);
                 }
                 named_bar_sync(1, kEpiThreads);              // last_flag is reused by the next unit
             }
         }
     } else if (MX) {
-        // ================= converters (warps 10..13, MXFP4 only) =================
-        const int r = tid - 64 - kEpiThreads;                // weight row of each A tile
+        // ================= converters (MXFP4 only: the warps after the epilogue) =================
+        // two threads per weight row: h = 0 decodes elements 0..31 of the
+        // k-block, h = 1 elements 32..63, each with its own scale byte
+        const int ct = tid - 64 - kEpiThreads;
+        const int r = ct >> 1, h = ct & 1;
         int stage = 0, dstage = 0;
         uint32_t phase = 0, dphase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const Unit un = decode_unit(u, prefix, offs, BT, a);
+            int ph;
+            const Unit un = unit_at(u, ph);
             for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
-                if (!wait_bar(dempty_bar(dstage), dphase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+                if (!wait_bar(full_bar(stage), phase, abort_flag, a0.err)) { ok = false; break; }
+                if (!wait_bar(dempty_bar(dstage), dphase ^ 1u, abort_flag, a0.err)) { ok = false; break; }
                 const uint8_t* st = smem + stage * C::STAGE_BYTES;
                 uint8_t* dec = smem + C::OFF_DEC + dstage * C::DSTAGE_BYTES;
-                const int sb = 2 * (kb & 7);                 // this k-block's 2 scale bytes
+                const int sb = 2 * (kb & 7) + h;             // this half's scale byte
 #pragma unroll
                 for (int t = 0; t < NA; ++t) {
-                    const uint8_t* sc = st + NA * C::RAW_BYTES + t * C::SC_BYTES + r * 16 + sb;
-                    decode_row(st + t * C::RAW_BYTES + r * 32, sc[0], sc[1], dec + t * C::A_BYTES, r);
+                    const uint8_t sc = st[NA * C::RAW_BYTES + t * C::SC_BYTES + r * 16 + sb];
+                    decode_half(st + t * C::RAW_BYTES + r * 32 + h * 16, sc, dec + t * C::A_BYTES, r, h);
                 }
                 // generic-proxy shared-memory writes -> visible to the MMA (async proxy)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -561,11 +694,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 // ---- launching one instantiation ------------------------------------------------------
-template <int BT, int NA, int MODE, typename OutT, bool MX>
-cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmS, const CUtensorMap& tmB,
-                          const GemmArgs& a, int grid, cudaStream_t s) {
+struct Maps {
+    CUtensorMap A[2], S[2], B[2];
+};
+
+template <int BT, int NA, int MODE, typename OutT, bool MX, bool FUSED>
+cudaError_t launch_kernel(const Maps& m, const KernelArgs& ka, int grid, cudaStream_t s) {
     using C = Cfg<BT, NA, MX>;
-    auto kern = grouped_gemm_kernel<BT, NA, MODE, OutT, MX>;
+    auto kern = grouped_gemm_kernel<BT, NA, MODE, OutT, MX, FUSED>;
     static std::atomic<uint64_t> configured{0};      // bit per device ordinal
     int dev = 0;
     cudaGetDevice(&dev);
@@ -575,41 +711,66 @@ cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmS, const 
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, tmA, tmS, tmB, a);
+    if (!FUSED)
+        return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, m.A[0], m.S[0], m.B[0], m.A[0],
+                          m.S[0], m.B[0], ka);
+    // the CTAs of a fused launch wait on one another: all of them must be
+    // resident at once, which a cooperative launch guarantees
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, m.A[0], m.S[0], m.B[0], m.A[1], m.S[1], m.B[1], ka);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cfg.numAttrs = 1;                            // cooperative only
+        e = cudaLaunchKernelEx(&cfg, kern, m.A[0], m.S[0], m.B[0], m.A[1], m.S[1], m.B[1], ka);
+    }
+    return e;
 }
 
-template <int NA, int MODE, typename OutT, bool MX>
-cudaError_t launch_bt(int bt, const CUtensorMap& tmA, const CUtensorMap& tmS, const CUtensorMap& tmB,
-                      const GemmArgs& a, int grid, cudaStream_t s) {
+template <int NA, int MODE, typename OutT, bool MX, bool FUSED>
+cudaError_t launch_bt(int bt, const Maps& m, const KernelArgs& ka, int grid, cudaStream_t s) {
     switch (bt) {
-        case 16: return launch_kernel<16, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
-        case 32: return launch_kernel<32, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
-        case 64: return launch_kernel<64, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
-        case 128: return launch_kernel<128, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
-        default: return launch_kernel<256, NA, MODE, OutT, MX>(tmA, tmS, tmB, a, grid, s);
+        case 16: return launch_kernel<16, NA, MODE, OutT, MX, FUSED>(m, ka, grid, s);
+        case 32: return launch_kernel<32, NA, MODE, OutT, MX, FUSED>(m, ka, grid, s);
+        case 64: return launch_kernel<64, NA, MODE, OutT, MX, FUSED>(m, ka, grid, s);
+        case 128: return launch_kernel<128, NA, MODE, OutT, MX, FUSED>(m, ka, grid, s);
+        default: return launch_kernel<256, NA, MODE, OutT, MX, FUSED>(m, ka, grid, s);
     }
 }
 
-// GEMM1 (mode 0) or GEMM2 (mode 1) of one weight format.
+// A single GEMM (fused = 0; mode 0 = GEMM1, 1 = GEMM2 with na tiles per unit)
+// or GEMM1 -> GEMM2 fused (fused = 1), of one weight format.
 template <bool MX>
-cudaError_t launch_gemm(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmS,
-                        const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
-    if (mode == MODE_SWIGLU) return launch_bt<2, MODE_SWIGLU, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
-    if (na == 2) {
-        if (out_dtype == MOE_DTYPE_F32) return launch_bt<2, MODE_PLAIN, float, MX>(bt, tmA, tmS, tmB, a, grid, s);
-        return launch_bt<2, MODE_PLAIN, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
+cudaError_t launch_gemm(int fused, int mode, int bt, int na, int out_dtype, const Maps& m, const KernelArgs& ka,
+                        int grid, cudaStream_t s) {
+    if (fused) {
+        if (out_dtype == MOE_DTYPE_F32) return launch_bt<2, MODE_PLAIN, float, MX, true>(bt, m, ka, grid, s);
+        return launch_bt<2, MODE_PLAIN, __nv_bfloat16, MX, true>(bt, m, ka, grid, s);
     }
-    if (out_dtype == MOE_DTYPE_F32) return launch_bt<1, MODE_PLAIN, float, MX>(bt, tmA, tmS, tmB, a, grid, s);
-    return launch_bt<1, MODE_PLAIN, __nv_bfloat16, MX>(bt, tmA, tmS, tmB, a, grid, s);
+    if (mode == MODE_SWIGLU) return launch_bt<2, MODE_SWIGLU, __nv_bfloat16, MX, false>(bt, m, ka, grid, s);
+    if (na == 2) {
+        if (out_dtype == MOE_DTYPE_F32) return launch_bt<2, MODE_PLAIN, float, MX, false>(bt, m, ka, grid, s);
+        return launch_bt<2, MODE_PLAIN, __nv_bfloat16, MX, false>(bt, m, ka, grid, s);
+    }
+    if (out_dtype == MOE_DTYPE_F32) return launch_bt<1, MODE_PLAIN, float, MX, false>(bt, m, ka, grid, s);
+    return launch_bt<1, MODE_PLAIN, __nv_bfloat16, MX, false>(bt, m, ka, grid, s);
 }
 
 // Defined in gemm_bf16.cu and gemm_mxfp4.cu (one translation unit per weight format).
-cudaError_t launch_gemm_bf16(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
-                             const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                             cudaStream_t s);
-cudaError_t launch_gemm_mxfp4(int mode, int bt, int na, int out_dtype, const CUtensorMap& tmA,
-                              const CUtensorMap& tmS, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                              cudaStream_t s);
+cudaError_t launch_gemm_bf16(int fused, int mode, int bt, int na, int out_dtype, const Maps& m,
+                             const KernelArgs& ka, int grid, cudaStream_t s);
+cudaError_t launch_gemm_mxfp4(int fused, int mode, int bt, int na, int out_dtype, const Maps& m,
+                              const KernelArgs& ka, int grid, cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace moe

@@ -152,13 +152,13 @@ moe_status moe_get_error(cudaStream_t stream) {
     return static_cast<moe_status>(v);
 }
 
-moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles) {
+moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse) {
     if (token_tile != 0 && token_tile != 16 && token_tile != 32 && token_tile != 64 && token_tile != 128 &&
         token_tile != 256)
         return MOE_ERR_INVALID_ARG;
     if (splits_gemm1 < 0 || splits_gemm1 > 64 || splits_gemm2 < 0 || splits_gemm2 > 64) return MOE_ERR_INVALID_ARG;
-    if (gemm2_tiles < 0 || gemm2_tiles > 2) return MOE_ERR_INVALID_ARG;
-    moe::set_plan_override(token_tile, splits_gemm1, splits_gemm2, gemm2_tiles);
+    if (gemm2_tiles < 0 || gemm2_tiles > 2 || fuse < 0 || fuse > 2) return MOE_ERR_INVALID_ARG;
+    moe::set_plan_override(token_tile, splits_gemm1, splits_gemm2, gemm2_tiles, fuse);
     return MOE_OK;
 }
 

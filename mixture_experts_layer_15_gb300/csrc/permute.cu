@@ -218,17 +218,20 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
     const int W = warps_per_chunk(E_l);
     const int threads = 32 * W;
     const int nchunks = ceil_div(n, threads);
+    // a single chunk uses only as many warps as it has routes
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
     if (nchunks <= 1) {
-        const size_t smem = sizeof(int) * (W * E_l + E_l + 1 + threads + 33);
+        const int w1 = ceil_div(n, 32) < 1 ? 1 : ceil_div(n, 32);
+        const int t1 = 32 * w1;
+        const size_t smem = sizeof(int) * (w1 * E_l + E_l + 1 + t1 + 33);
         int grid = 1;
         if (x_perm != nullptr) {
-            // enough warps to copy every row in about one pass, at most 2 per SM
-            grid = ceil_div(n, W);
+            // one warp per gathered row (at most 2 CTAs per SM)
+            grid = ceil_div(n, w1);
             grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
         }
-        return launch_pdl(permute_fused_kernel, dim3(grid), dim3(threads), smem, s, ids, n, top_k, E, emap, E_l,
+        return launch_pdl(permute_fused_kernel, dim3(grid), dim3(t1), smem, s, ids, n, top_k, E, emap, E_l,
                           xb, K, offsets, map, inverse, xp, err);
     }
     int32_t* chunk = static_cast<int32_t*>(ws);
