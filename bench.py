@@ -166,9 +166,11 @@ def make_workload(cfg_name, device, only_m=None, experts=0):
 
 def launches_per_forward(cfg, M):
     """Kernels one forward launches (mirrors the library's launch plan)."""
-    n = 1                                                     # router
     w = max(1, min(32, 8192 // cfg.E))
-    n += 1 if M * cfg.top_k <= 32 * w else 4                  # permute: fused, or count/scan/scatter/gather
+    if M <= 64 and M * cfg.top_k <= 32 * w:
+        n = 1                                                 # router + permute in one kernel
+    else:
+        n = 1 + (1 if M * cfg.top_k <= 32 * w else 4)         # router; permute fused or count/scan/scatter/gather
     # grouped GEMM1 + GEMM2: one fused launch when GEMM2 units take two
     # 128-row weight tiles (K % 256 == 0), else two launches
     n += 1 if cfg.K % 256 == 0 else 2
@@ -197,9 +199,11 @@ def make_forward(moe, cfg, layer, batches, stream):
     def forward(M, ev=None):
         x, logits = batches[M]
         b = layer.buffers(M)
-        layer.route(logits, b)
-        moe.moe_permute(b.topk_ids, M, cfg.top_k, cfg.E, None, cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse,
-                        b.x_perm, b.perm_ws, b.perm_ws.numel())
+        rsf_r = layer.rsf if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0
+        moe.moe_route_permute(logits, M, cfg.E, cfg.top_k, layer.method, layer.score_bias, layer.n_group,
+                              layer.topk_group, rsf_r, b.topk_ids, b.topk_weights, layer.weights_dtype, None,
+                              cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse, b.x_perm, b.perm_ws,
+                              b.perm_ws.numel())
         if layer.ws1 is not None:
             moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.shared, layer.gemm2_dtype,
                                   b.shared_ws, b.shared_ws.numel())
@@ -363,38 +367,66 @@ def run_gpu(args):
 
 
 def run_e2e(args, cfg, layer, batches, forward_fn):
-    """Same metric through the public API with host buffers: each step copies
-    x and the router logits from pinned host memory to the device and reads
-    the output back, for every M of the sweep."""
-    stream = torch.cuda.current_stream()
+    """Same metric through the public API with host buffers: every step copies
+    each batch's x and router logits from pinned host memory to the device
+    and reads each output back. Three streams pipeline the step: the H2D copy
+    of a batch, its forward, and the D2H copy of its output; events keep each
+    buffer from being reused before its previous user is done."""
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    Ms = sorted(batches)
     host = {M: (x.cpu().pin_memory(), lg.cpu().pin_memory()) for M, (x, lg) in batches.items()}
     outs = {M: torch.empty(layer.buffers(M).out.shape, dtype=layer.buffers(M).out.dtype).pin_memory()
-            for M in batches}
+            for M in Ms}
     dev_in = {M: (torch.empty_like(x), torch.empty_like(lg)) for M, (x, lg) in batches.items()}
+    ev = lambda: torch.cuda.Event()
+    in_free = {M: ev() for M in Ms}      # forward of M has consumed its inputs
+    in_ready = {M: ev() for M in Ms}     # inputs of M are on the device
+    out_ready = {M: ev() for M in Ms}    # output of M computed
+    out_free = {M: ev() for M in Ms}     # output of M copied back
+    for M in Ms:
+        in_free[M].record(comp)
+        out_free[M].record(comp)
     orig = dict(batches)
     steps = max(3, args.steps // 4)
     h2d = sum(x.numel() * x.element_size() + lg.numel() * lg.element_size() for x, lg in host.values())
     d2h = sum(o.numel() * o.element_size() for o in outs.values())
     try:
-        for M in batches:
+        for M in Ms:
             batches[M] = dev_in[M]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for it in range(2 + steps):
             if it == 2:
                 torch.cuda.synchronize()
-                t0.record(stream)
-            for M in batches:
-                dev_in[M][0].copy_(host[M][0], non_blocking=True)
-                dev_in[M][1].copy_(host[M][1], non_blocking=True)
+                t0.record(comp)
+                h2d_s.wait_event(t0)                    # no timed copy starts before t0
+                d2h_s.wait_event(t0)
+            for M in Ms:
+                h2d_s.wait_event(in_free[M])
+                with torch.cuda.stream(h2d_s):
+                    dev_in[M][0].copy_(host[M][0], non_blocking=True)
+                    dev_in[M][1].copy_(host[M][1], non_blocking=True)
+                in_ready[M].record(h2d_s)
+                comp.wait_event(in_ready[M])
+                comp.wait_event(out_free[M])
                 forward_fn(M)
-                outs[M].copy_(layer.buffers(M).out, non_blocking=True)
-        t1.record(stream)
+                in_free[M].record(comp)
+                out_ready[M].record(comp)
+                d2h_s.wait_event(out_ready[M])
+                with torch.cuda.stream(d2h_s):
+                    outs[M].copy_(layer.buffers(M).out, non_blocking=True)
+                out_free[M].record(d2h_s)
+            if it == 1 + steps:
+                for M in Ms:
+                    comp.wait_event(out_free[M])         # the step ends when its outputs are on the host
+        t1.record(comp)
         torch.cuda.synchronize()
     finally:
         batches.update(orig)
     secs = t0.elapsed_time(t1) / 1e3
-    return {"value": sum(batches) * steps / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+    return {"value": sum(Ms) * steps / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipelining": "H2D, compute and D2H on three streams; every step copies all its inputs and outputs"}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -178,6 +178,23 @@ moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route_permute -- moe_route followed by moe_permute, with the arguments
+ * of both, giving the same results bit for bit. For small batches (M <= 64
+ * and M*top_k routes within one permute chunk) one kernel routes every token
+ * and permutes the routes, one launch fewer on the latency-bound path; the
+ * workspace is then not used (it may be NULL). Otherwise it runs the two
+ * steps and needs moe_permute_workspace_size() bytes of workspace.
+ * ---------------------------------------------------------------------- */
+moe_status moe_route_permute(const float* logits, int M, int E, int top_k,
+                             moe_route_method method, const float* score_bias,
+                             int n_group, int topk_group, float routed_scaling_factor,
+                             int32_t* topk_ids, void* topk_weights, moe_dtype weights_dtype,
+                             const int32_t* expert_map, int E_local, const void* x, int K,
+                             int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
+                             int32_t* permuted_to_expanded, void* x_perm,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute_noalloc -- moe_permute for callers that cannot allocate device
  * memory (no counterpart on the pages: it exists for this library's users).
  * Some callers may not call cudaMalloc or hand the library a workspace: code

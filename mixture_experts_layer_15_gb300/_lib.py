@@ -32,7 +32,7 @@ MOE_WEIGHTS_MXFP4 = 1
 
 #: every function the header declares (checked against include/moe.h by the tests)
 EXPORTS = (
-    "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
+    "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
     "moe_experts", "moe_finalize", "moe_shared_expert_workspace_size", "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
@@ -73,6 +73,8 @@ _SIGS = {
     "moe_route": ([_P, _I, _I, _I, _I, _P, _I, _I, _F, _P, _P, _I, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
     "moe_permute": ([_P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_route_permute": ([_P, _I, _I, _I, _I, _P, _I, _I, _F, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _Z,
+                           _P], _I),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_experts_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I], _Z),
     "moe_experts": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _I, _F,
@@ -146,6 +148,17 @@ def moe_permute(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets
                                           _ptr(expanded_idx_to_permuted_idx), _ptr(permuted_to_expanded),
                                           _ptr(x_perm), _ptr(workspace), int(workspace_bytes),
                                           _stream(stream)))
+
+
+def moe_route_permute(logits, M, E, top_k, method, score_bias, n_group, topk_group, routed_scaling_factor,
+                      topk_ids, topk_weights, weights_dtype, expert_map, E_local, x, K, expert_offsets,
+                      expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm, workspace, workspace_bytes,
+                      stream=None):
+    _check("moe_route_permute", lib.moe_route_permute(
+        _ptr(logits), M, E, top_k, method, _ptr(score_bias), n_group, topk_group, routed_scaling_factor,
+        _ptr(topk_ids), _ptr(topk_weights), weights_dtype, _ptr(expert_map), E_local, _ptr(x), K,
+        _ptr(expert_offsets), _ptr(expanded_idx_to_permuted_idx), _ptr(permuted_to_expanded), _ptr(x_perm),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def moe_permute_noalloc(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,

@@ -235,6 +235,63 @@ moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E, const i
                                          workspace, err, info, stream));
 }
 
+moe_status moe_route_permute(const float* logits, int M, int E, int top_k, moe_route_method method,
+                             const float* score_bias, int n_group, int topk_group, float routed_scaling_factor,
+                             int32_t* topk_ids, void* topk_weights, moe_dtype weights_dtype,
+                             const int32_t* expert_map, int E_local, const void* x, int K,
+                             int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
+                             int32_t* permuted_to_expanded, void* x_perm, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    // the checks of moe_route ...
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || top_k > E || top_k > 32) return MOE_ERR_INVALID_ARG;
+    if (!valid_dtype(weights_dtype)) return MOE_ERR_INVALID_ARG;
+    if (method == MOE_ROUTE_SOFTMAX_TOPK) {
+        if (score_bias != nullptr) return MOE_ERR_INVALID_ARG;
+    } else if (method == MOE_ROUTE_SIGMOID_GROUPED_TOPK) {
+        if (score_bias == nullptr) return MOE_ERR_INVALID_ARG;
+        if (n_group < 1 || n_group > 32 || E % n_group != 0 || E / n_group < 2) return MOE_ERR_INVALID_ARG;
+        if (topk_group < 1 || topk_group > n_group) return MOE_ERR_INVALID_ARG;
+        if (top_k > topk_group * (E / n_group)) return MOE_ERR_INVALID_ARG;
+    } else {
+        return MOE_ERR_INVALID_ARG;
+    }
+    // ... and of moe_permute
+    if (E_local < 1 || E_local > 1024) return MOE_ERR_INVALID_ARG;
+    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (x_perm != nullptr) {
+        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
+        if (K % 8 != 0 || !aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+    }
+    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (M > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr ||
+                  expanded_idx_to_permuted_idx == nullptr || permuted_to_expanded == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    const bool fused = M > 0 && moe::route_permute_fusible(M, top_k, E, E_local, method);
+    const size_t need = moe::permute_workspace_bytes(M > 0 ? M : 1, top_k, E_local);
+    if (M > 0 && !fused && need > 0 && (workspace == nullptr || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    if (M == 0) return from_cuda(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E_local + 1), stream));
+    if (fused)
+        return from_cuda(moe::launch_route_permute(logits, M, E, top_k, method, score_bias, n_group, topk_group,
+                                                   routed_scaling_factor, topk_ids, topk_weights, weights_dtype,
+                                                   expert_map, E_local, x, K, expert_offsets,
+                                                   expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm,
+                                                   err, info, stream));
+    const cudaError_t e = moe::launch_route(logits, M, E, top_k, method, score_bias, n_group, topk_group,
+                                            routed_scaling_factor, topk_ids, topk_weights, weights_dtype, err,
+                                            stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_permute(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                                         expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm, workspace,
+                                         err, info, stream));
+}
+
 size_t moe_experts_workspace_size(const moe_weights* w, int M, int top_k) {
     if (check_weights(w) != MOE_OK || M < 0 || top_k <= 0) return 0;
     DeviceInfo info;

@@ -38,6 +38,16 @@ cudaError_t launch_permute(const int32_t* topk_ids, int M, int top_k, int E,
                            void* x_perm, void* workspace, int* err, const DeviceInfo& dev,
                            cudaStream_t stream);
 
+// Router + single-chunk permute in one kernel (small batches); same results as
+// launch_route followed by launch_permute.
+bool route_permute_fusible(int M, int top_k, int E, int E_local, int method);
+cudaError_t launch_route_permute(const float* logits, int M, int E, int top_k, int method,
+                                 const float* score_bias, int n_group, int topk_group, float rsf,
+                                 int32_t* topk_ids, void* topk_weights, int weights_dtype,
+                                 const int32_t* expert_map, int E_local, const void* x, int K,
+                                 int32_t* expert_offsets, int32_t* map, int32_t* inverse, void* x_perm,
+                                 int* err, const DeviceInfo& dev, cudaStream_t stream);
+
 // ---- finalize (finalize.cu) ----------------------------------------------------
 cudaError_t launch_finalize(const void* gemm2, int gemm2_dtype, int num_rows,
                             const void* weights, int weights_dtype, const int32_t* map,

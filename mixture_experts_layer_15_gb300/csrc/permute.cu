@@ -17,7 +17,7 @@
 // One chunk (M*top_k <= 32*W): a single kernel; every CTA recomputes the tiny
 // sort in shared memory and copies its share of the rows.
 // Several chunks: count -> scan -> scatter -> gather (4 launches).
-#include "common.cuh"
+#include "router_device.cuh"
 
 namespace moe {
 namespace {
@@ -33,7 +33,7 @@ __device__ __forceinline__ int local_expert(const int32_t* __restrict__ ids,
                                             const int32_t* __restrict__ emap,
                                             int i, int n, int E, int E_l, int* err) {
     if (i >= n) return -2;                 // padding lane: in no group
-    const int id = __ldg(ids + i);
+    const int id = ids[i];                 // global or shared memory
     if (id < 0 || id >= E) { set_error(err, MOE_ERR_DEVICE_INDEX); return -1; }
     if (emap == nullptr) return id;
     const int le = __ldg(emap + id);
@@ -82,13 +82,15 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* _
 }
 
 // ---- single chunk: one kernel ------------------------------------------------
-__global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int top_k, int E,
-                                     const int32_t* __restrict__ emap, int E_l,
-                                     const __nv_bfloat16* __restrict__ x, int K,
-                                     int32_t* __restrict__ offsets, int32_t* __restrict__ map,
-                                     int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
-                                     int* err) {
-    extern __shared__ int sm[];
+// The whole permute of at most blockDim.x routes (ids in global or shared
+// memory): every CTA sorts them in shared memory; CTA 0 writes the offsets and
+// maps; every CTA copies its share of the rows.
+__device__ __forceinline__ void permute_single_chunk(const int32_t* ids, int n, int top_k, int E,
+                                                     const int32_t* __restrict__ emap, int E_l,
+                                                     const __nv_bfloat16* __restrict__ x, int K,
+                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ map,
+                                                     int32_t* __restrict__ inverse,
+                                                     __nv_bfloat16* __restrict__ x_perm, int* err, int* sm) {
     const int W = blockDim.x >> 5;
     int* hist = sm;                          // [W][E_l]
     int* total = hist + W * E_l;             // [E_l + 1]
@@ -119,6 +121,67 @@ __global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int
         copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(i / top_k) * K),
                  reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(pi) * K), n16, tid & 31);
     }
+}
+
+__global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int top_k, int E,
+                                     const int32_t* __restrict__ emap, int E_l,
+                                     const __nv_bfloat16* __restrict__ x, int K,
+                                     int32_t* __restrict__ offsets, int32_t* __restrict__ map,
+                                     int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
+                                     int* err) {
+    extern __shared__ int sm[];
+    permute_single_chunk(ids, n, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, sm);
+}
+
+// Router and single-chunk permute in one kernel (small batches): every CTA
+// routes all M tokens (one warp per token, the router's own per-token code),
+// keeps the ids in shared memory, then permutes them. CTA 0 writes the ids
+// and weights.
+template <int SLOTS, bool SIGMOID>
+__global__ void route_permute_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int M,
+                                     int E, int top_k, int n_group, int topk_group, float rsf,
+                                     int32_t* __restrict__ ids_out, void* __restrict__ w_out, int wdtype,
+                                     const int32_t* __restrict__ emap, int E_l,
+                                     const __nv_bfloat16* __restrict__ x, int K,
+                                     int32_t* __restrict__ offsets, int32_t* __restrict__ map,
+                                     int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
+                                     int* err) {
+    extern __shared__ int sm[];
+    const int W = blockDim.x >> 5, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int* ids_s = sm;                                             // [blockDim] routed expert per route
+    float* bsc = reinterpret_cast<float*>(ids_s + blockDim.x);   // [W][E] sigmoid router scratch
+    int* rest = reinterpret_cast<int*>(bsc + (SIGMOID ? W * E : 0));
+    pdl_wait();
+    pdl_trigger();
+    for (int t = warp; t < M; t += W) {
+        int id;
+        float w;
+        if (SIGMOID)
+            route::route_token_sigmoid<SLOTS>(logits + static_cast<size_t>(t) * E, bias, E, top_k, n_group,
+                                              topk_group, rsf, lane, bsc + warp * E, id, w);
+        else
+            route::route_token_softmax<SLOTS>(logits + static_cast<size_t>(t) * E, E, top_k, rsf, lane, id, w);
+        if (lane < top_k) {
+            const int o = t * top_k + lane;
+            ids_s[o] = id;
+            if (blockIdx.x == 0) {
+                ids_out[o] = id;
+                store_from_f32(w_out, o, w, wdtype);
+            }
+        }
+    }
+    __syncthreads();
+    permute_single_chunk(ids_s, M * top_k, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, rest);
+}
+
+template <int SLOTS, bool SIGMOID>
+cudaError_t launch_route_permute_t(dim3 grid, dim3 block, size_t smem, cudaStream_t s, const float* logits,
+                                   const float* bias, int M, int E, int top_k, int n_group, int topk_group,
+                                   float rsf, int32_t* ids, void* w, int wdtype, const int32_t* emap, int E_l,
+                                   const __nv_bfloat16* x, int K, int32_t* offsets, int32_t* map, int32_t* inverse,
+                                   __nv_bfloat16* xp, int* err) {
+    return launch_pdl(route_permute_kernel<SLOTS, SIGMOID>, grid, block, smem, s, logits, bias, M, E, top_k,
+                      n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, x, K, offsets, map, inverse, xp, err);
 }
 
 // ---- several chunks ------------------------------------------------------------
@@ -201,6 +264,54 @@ __global__ void permute_gather_kernel(const int32_t* __restrict__ offsets, int E
 }
 
 }  // namespace
+
+bool route_permute_fusible(int M, int top_k, int E, int E_l, int method) {
+    const int n = M * top_k;
+    const int Wmax = warps_per_chunk(E_l);
+    if (M > 64 || n > 32 * Wmax) return false;
+    int W = (n + 31) / 32;
+    W = W < (M < 16 ? M : 16) ? (M < 16 ? M : 16) : W;
+    if (W > Wmax) W = Wmax;
+    const size_t smem = sizeof(int) * (2 * 32 * W + W * E_l + E_l + 1 + 33) +
+                        (method == MOE_ROUTE_SIGMOID_GROUPED_TOPK ? sizeof(float) * W * E : 0);
+    return smem <= 48 * 1024;
+}
+
+cudaError_t launch_route_permute(const float* logits, int M, int E, int top_k, int method, const float* bias,
+                                 int n_group, int topk_group, float rsf, int32_t* ids, void* w, int wdtype,
+                                 const int32_t* emap, int E_l, const void* x, int K, int32_t* offsets,
+                                 int32_t* map, int32_t* inverse, void* x_perm, int* err, const DeviceInfo& dev,
+                                 cudaStream_t s) {
+    const int n = M * top_k;
+    const int Wmax = warps_per_chunk(E_l);
+    int W = (n + 31) / 32;
+    W = W < (M < 16 ? M : 16) ? (M < 16 ? M : 16) : W;   // enough warps to route in few rounds
+    if (W > Wmax) W = Wmax;
+    const bool sig = method == MOE_ROUTE_SIGMOID_GROUPED_TOPK;
+    const size_t smem = sizeof(int) * (2 * 32 * W + W * E_l + E_l + 1 + 33) + (sig ? sizeof(float) * W * E : 0);
+    int grid = 1;
+    if (x_perm != nullptr) {
+        grid = ceil_div(n, W);
+        grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
+    }
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
+    const int slots = ceil_div(E, 32);
+#define MOE_RP(S)                                                                                            \
+    return sig ? launch_route_permute_t<S, true>(dim3(grid), dim3(32 * W), smem, s, logits, bias, M, E, top_k, \
+                                                 n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, xb, K,   \
+                                                 offsets, map, inverse, xp, err)                              \
+               : launch_route_permute_t<S, false>(dim3(grid), dim3(32 * W), smem, s, logits, bias, M, E,      \
+                                                  top_k, n_group, topk_group, rsf, ids, w, wdtype, emap, E_l,  \
+                                                  xb, K, offsets, map, inverse, xp, err)
+    if (slots <= 1) MOE_RP(1);
+    if (slots <= 2) MOE_RP(2);
+    if (slots <= 4) MOE_RP(4);
+    if (slots <= 8) MOE_RP(8);
+    if (slots <= 16) MOE_RP(16);
+    MOE_RP(32);
+#undef MOE_RP
+}
 
 size_t permute_workspace_bytes(int M, int top_k, int E_local) {
     const long long n = static_cast<long long>(M) * top_k;

@@ -112,12 +112,17 @@ class MoELayer:
         M = x.shape[0]
         b = self.buffers(M)
         if topk_ids is None:
-            self.route(logits, b, stream)
+            # route and permute (one kernel for small batches)
+            rsf = self.rsf if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0
+            L.moe_route_permute(logits, M, self.E, self.top_k, self.method, self.score_bias, self.n_group,
+                                self.topk_group, rsf, b.topk_ids, b.topk_weights, self.weights_dtype,
+                                self.expert_map, self.E_local, x, self.K, b.offsets, b.pmap, b.inverse, b.x_perm,
+                                b.perm_ws, b.perm_ws.numel(), stream)
             ids, wts = b.topk_ids, b.topk_weights
         else:
             ids, wts = topk_ids, topk_weights
-        L.moe_permute(ids, M, self.top_k, self.E, self.expert_map, self.E_local, x, self.K, b.offsets,
-                      b.pmap, b.inverse, b.x_perm, b.perm_ws, b.perm_ws.numel(), stream)
+            L.moe_permute(ids, M, self.top_k, self.E, self.expert_map, self.E_local, x, self.K, b.offsets,
+                          b.pmap, b.inverse, b.x_perm, b.perm_ws, b.perm_ws.numel(), stream)
         if self.ws1 is not None:
             L.moe_shared_expert(self.ws1, self.ws2, self.K, self.Ns, x, M, b.shared, self.gemm2_dtype,
                                 b.shared_ws, b.shared_ws.numel(), stream)

@@ -182,6 +182,68 @@ def test_permute_bad_ids_set_device_error(moe):
     assert offs[-1] == 4
 
 
+# ------------------------------------------------------------------ route + permute
+
+def _route_permute(moe, cfg, li, logits, x, M, emap, E_l, wdt, fused):
+    k, K = cfg.top_k, x.shape[1]
+    sig = cfg.route != "softmax"
+    method = moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK if sig else moe.MOE_ROUTE_SOFTMAX_TOPK
+    bias = li.score_bias.to(DEV) if sig else None
+    rsf = cfg.routed_scaling_factor if sig else 1.0
+    tdt = torch.float32 if wdt == moe.MOE_DTYPE_F32 else torch.bfloat16
+    fill = 3 if fused else 5
+    ids = torch.full((M, k), fill, dtype=torch.int32, device=DEV)
+    w = torch.full((M, k), float(fill), dtype=tdt, device=DEV)
+    offs = torch.full((E_l + 1,), fill, dtype=torch.int32, device=DEV)
+    pmap = torch.full((M, k), fill, dtype=torch.int32, device=DEV)
+    inv = torch.full((max(M * k, 1),), fill, dtype=torch.int32, device=DEV)
+    xp = torch.full((max(M * k, 1), K), float(fill), dtype=torch.bfloat16, device=DEV)
+    wsb = moe.moe_permute_workspace_size(M, k, E_l)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    em = None if emap is None else torch.from_numpy(np.asarray(emap, np.int32)).to(DEV)
+    if fused:
+        moe.moe_route_permute(logits, M, cfg.E, k, method, bias, cfg.n_group, cfg.topk_group, rsf, ids, w, wdt,
+                              em, E_l, x, K, offs, pmap, inv, xp, ws, ws.numel())
+    else:
+        moe.moe_route(logits, M, cfg.E, k, method, bias, cfg.n_group, cfg.topk_group, rsf, ids, w, wdt)
+        moe.moe_permute(ids, M, k, cfg.E, em, E_l, x, K, offs, pmap, inv, xp, ws, ws.numel())
+    R = int(offs[-1])
+    return ids, w, offs, pmap, inv[:R], xp[:R]
+
+
+@pytest.mark.parametrize("name,M,masked", [("tiny", 16, False), ("mixtral", 1, False), ("mixtral", 8, False),
+                                           ("mixtral", 64, False), ("qwen3", 1, False), ("qwen3", 32, True),
+                                           ("qwen3", 64, False), ("deepseek", 1, False), ("deepseek", 64, True),
+                                           ("mixtral", 65, False), ("qwen3", 4096, True), ("deepseek", 512, False)])
+def test_route_permute_matches_two_calls(moe, name, M, masked):
+    """moe_route_permute (one kernel for M <= 64, else the two launches) gives
+    the results of moe_route followed by moe_permute, bit for bit."""
+    cfg = synth.CONFIGS[name]
+    li = synth.make_layer(cfg, "cpu", experts=[])
+    x, logits = synth.make_tokens(cfg, M, DEV, li if cfg.logit_bias_std else None)
+    x = x[:, :1024].contiguous()
+    emap, E_l = None, cfg.E
+    if masked:
+        em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+        emap = em.numpy()
+    for wdt in (moe.MOE_DTYPE_F32, moe.MOE_DTYPE_BF16):
+        a = _route_permute(moe, cfg, li, logits, x, M, emap, E_l, wdt, fused=False)
+        b = _route_permute(moe, cfg, li, logits, x, M, emap, E_l, wdt, fused=True)
+        for u, v in zip(a, b):
+            assert u.shape == v.shape and torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u,
+                                                      v.view(torch.int16) if v.dtype == torch.bfloat16 else v)
+    # and the ids are the oracle's
+    if cfg.route == "softmax":
+        rid, _ = O.route_softmax_topk(logits.cpu().numpy(), cfg.top_k)
+    else:
+        rid, _ = O.route_sigmoid_grouped(logits.cpu().numpy(), li.score_bias.numpy(), cfg.top_k, cfg.n_group,
+                                         cfg.topk_group, cfg.routed_scaling_factor)
+    assert np.array_equal(b[0].cpu().numpy(), rid)
+    r_offs, r_map, _, _ = O.permute(rid, cfg.E, emap)
+    assert np.array_equal(b[2].cpu().numpy(), r_offs) and np.array_equal(b[3].cpu().numpy(), r_map)
+    check_no_device_error(moe)
+
+
 # ------------------------------------------------------------------ whole layer
 
 def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0):
