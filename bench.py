@@ -174,7 +174,7 @@ def launches_per_forward(cfg, M):
     # grouped GEMM1 + GEMM2: one fused launch when GEMM2 units take two
     # 128-row weight tiles (K % 256 == 0), else two launches
     n += 1 if cfg.K % 256 == 0 else 2
-    n += 1                                                    # finalize
+    n += 1                                                    # finalize, or the out-init of the fused finalize
     if cfg.shared_N:
         n += 1 if cfg.K % 256 == 0 else 2                     # shared expert (same kernel, one group)
     return n
@@ -193,9 +193,11 @@ def roofline_layer(cfg, M, touched, pk, sustained=True):
     return max(wbytes / (pk["hbm"] * 1e9), flops / tc), wbytes, flops
 
 
-def make_forward(moe, cfg, layer, batches, stream):
-    """One layer forward at batch size M through the C ABI: route, permute,
-    [shared expert], experts (GEMM1, GEMM2; ``ev`` brackets them), finalize."""
+def make_forward(moe, cfg, layer, batches, stream, finalize="fused"):
+    """One layer forward at batch size M through the C ABI: route + permute,
+    [shared expert], experts (GEMM1, GEMM2; ``ev`` brackets them) and the
+    finalize: folded into GEMM2 (finalize="fused", moe_experts_fused_finalize)
+    or as a pass of its own over gemm2_permuted (finalize="two-pass")."""
     def forward(M, ev=None):
         x, logits = batches[M]
         b = layer.buffers(M)
@@ -207,14 +209,21 @@ def make_forward(moe, cfg, layer, batches, stream):
         if layer.ws1 is not None:
             moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.shared, layer.gemm2_dtype,
                                   b.shared_ws, b.shared_ws.numel())
+        rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
         if ev is not None:
             ev[0].record(stream)
+        if finalize == "fused":
+            moe.moe_experts_fused_finalize(layer.cw, b.x_perm, b.offsets, M, cfg.top_k, b.topk_weights,
+                                           layer.weights_dtype, b.inverse, b.shared, layer.gemm2_dtype, rsf,
+                                           b.out, b.exp_ws, b.exp_ws.numel())
+            if ev is not None:
+                ev[1].record(stream)
+            return
         moe.moe_experts(layer.cw, b.x_perm, b.offsets, M, cfg.top_k, b.gemm2, layer.gemm2_dtype, 0, None,
                         layer.weights_dtype, None, None, layer.gemm2_dtype, 1.0, None, layer.out_dtype,
                         b.exp_ws, b.exp_ws.numel())
         if ev is not None:
             ev[1].record(stream)
-        rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
         moe.moe_finalize(b.gemm2, layer.gemm2_dtype, b.gemm2.shape[0], b.topk_weights, layer.weights_dtype,
                          b.pmap, M, cfg.top_k, cfg.K, b.shared, layer.gemm2_dtype, rsf, b.out, layer.out_dtype)
     return forward
@@ -232,13 +241,52 @@ def warm_up(moe, layer, sweep, forward, warmup):
         raise RuntimeError(f"device error during warm-up: {moe.status_string(st)}")
 
 
-def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clocks=None, reps=5):
+def l2_scrub(buf):
+    """Untimed L2 scrub between breakdown samples: a read of a 1 GB buffer.
+    It evicts everything (dirty lines are written back here, outside the
+    timed region) and leaves only clean lines behind, so the next sample
+    starts from a cold L2 without paying for another buffer's write-back."""
+    torch.sum(buf)
+
+
+def graph_time(forward, M, stream, scrub, reps):
+    """Median time of a CUDA-graph replay of one forward at M (launch costs
+    removed), each replay after an L2 scrub; None if capture fails."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            forward(M)
+        stream.wait_stream(side)
+        with torch.cuda.graph(g):
+            forward(M)
+        torch.cuda.synchronize()
+    except Exception as e:                      # capture unsupported: report, do not fail the bench
+        torch.cuda.synchronize()
+        return None, f"{type(e).__name__}: {e}"[:200]
+    ts = []
+    for _ in range(reps):
+        scrub()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    del g
+    return statistics.median(ts), None
+
+
+def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clocks=None, reps=20,
+                graph_max_m=64):
     """K timed steps of the whole sweep, with CUDA events only around the timed
     region (events between the kernels of a forward would break their
     programmatic-dependent-launch chaining). Then a per-M breakdown: for each
-    M, ``reps`` single forwards (and single experts calls), each after an L2
-    flush, each bracketed by events. Returns (seconds over all steps, per-M
-    breakdown, GEMM FLOPs, GEMM seconds, clocks)."""
+    M, the median of ``reps`` single forwards (and single experts calls),
+    each after an L2 scrub, each bracketed by events; for M <= graph_max_m
+    also the median of CUDA-graph replays of the forward. Returns (seconds
+    over all steps, per-M breakdown, GEMM FLOPs, GEMM seconds, clocks)."""
     touched = {M: int((layer.buffers(M).offsets.diff() > 0).sum().item()) for M in sweep}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -258,14 +306,15 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
         raise RuntimeError(f"device error in the timed region: {moe.status_string(st)}")
     secs = t0.elapsed_time(t1) / 1e3
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device)   # 256 MB > L2
+    buf = torch.zeros(256 << 20, dtype=torch.float32, device=stream.device)     # 1 GB > L2
+    scrub = lambda: l2_scrub(buf)
     per_m = []
     gemm_flops = gemm_secs = 0.0
     for M in sweep:
         tf, tg = [], []
         for r in range(reps):
             for which, acc in ((0, tf), (1, tg)):
-                flush.fill_(r & 0xFF)
+                scrub()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 if which == 0:
                     e0.record(stream)
@@ -280,12 +329,23 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
         gf = 6.0 * cfg.K * cfg.N * M * cfg.top_k
         gemm_flops += gf
         gemm_secs += tgm
-        per_m.append({"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tgm * 1e3,
-                      "touched_experts": touched[M], "roofline_ms": troof * 1e3,
-                      "roofline_frac": troof / tm,
-                      "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= flops / (pk["bf16_sus"] * 1e12) else "tensor",
-                      "gemm_tflops": gf / tgm / 1e12})
-    del flush
+        rec = {"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tgm * 1e3,
+               "touched_experts": touched[M], "roofline_ms": troof * 1e3,
+               "roofline_frac": troof / tm,
+               "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= flops / (pk["bf16_sus"] * 1e12) else "tensor",
+               "gemm_tflops": gf / tgm / 1e12}
+        if M <= graph_max_m:
+            tgr, err = graph_time(forward, M, stream, scrub, reps)
+            if tgr is not None:
+                rec["graph_ms"] = tgr * 1e3
+                rec["graph_roofline_frac"] = troof / tgr
+            else:
+                rec["graph_error"] = err
+        per_m.append(rec)
+    st = moe.moe_get_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the breakdown: {moe.status_string(st)}")
+    del buf
     return secs, per_m, gemm_flops, gemm_secs, clk
 
 
@@ -293,7 +353,7 @@ def other_config(moe, name, args, pk, dev, stream):
     """The same measurement on another config (reported beside the headline)."""
     cfg, li, layer, batches = make_workload(name, dev)
     sweep = sorted(batches)
-    forward = make_forward(moe, cfg, layer, batches, stream)
+    forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
     warm_up(moe, layer, sweep, forward, 3)
     steps = max(5, args.steps // 5)
     secs, per_m, gf, gs, _ = timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk)
@@ -314,7 +374,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts)
     sweep = sorted(batches)
-    forward = make_forward(moe, cfg, layer, batches, stream)
+    forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
     warm_up(moe, layer, sweep, forward, args.warmup)
     clocks = ClockSampler(torch.cuda.current_device())
     secs, per_m, gemm_flops, gemm_secs, clk = timed_sweep(moe, cfg, layer, sweep, forward, args.steps, stream,
@@ -347,7 +407,10 @@ def run_gpu(args):
                                f"top_k={cfg.top_k}, {cfg.weight_format} weights), one forward at each M",
                    "M_sweep": sweep, "tokens_per_step": tokens_step,
                    "storage": "f32 routing weights, gemm2_permuted and output; bf16 act",
-                   "l2": "inputs larger than L2 (expert weights streamed every forward)",
+                   "finalize": ("folded into the GEMM2 epilogue (f32 reductions into out; gemm2_permuted not "
+                                "materialised)" if args.finalize == "fused" else
+                                "separate pass over gemm2_permuted (deterministic order)"),
+                   "l2": "timed steps: inputs larger than L2 (expert weights streamed every forward); per-M breakdown: a 1 GB read scrub before each sample (median of 20)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "sweep": per_m, "e2e": e2e,
         "gpu_launches": args.steps * sum(launches_per_forward(cfg, M) for M in sweep),
@@ -542,6 +605,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--m", type=int, nargs="*", default=None,
                     help="run only these batch sizes of the sweep (profiling)")
+    ap.add_argument("--finalize", default="fused", choices=["fused", "two-pass"],
+                    help="finalize folded into GEMM2 (f32 reductions, order not fixed) or a separate pass")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling)")
     ap.add_argument("--others", default="qwen3,deepseek",
                     help="other configs measured after the headline one and reported beside it ('' = none)")

@@ -265,6 +265,44 @@ moe_status moe_experts(const moe_weights* w,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_experts_fused_finalize -- the experts with the finalize folded into
+ * GEMM2 (moe_output.py, UnfinalizedMoEOutput: when the routed output is left
+ * unfinalized, the top-k reduction can fold into the consumer that runs
+ * next; here the consumer is GEMM2's own epilogue). Computes
+ *
+ *   out[t] = shared_out[t] + rsf * sum_{routes (t, j) with a local expert} w[t,j] * y[t,j]
+ *
+ * with y the unweighted GEMM2 row of the route, as moe_experts followed by
+ * moe_finalize does, without writing gemm2_permuted: every GEMM2 accumulator
+ * value goes straight from the tensor memory into out with an f32 reduction.
+ * This removes the [R, K] f32 round trip through HBM and the finalize launch.
+ *
+ *   x_perm, expert_offsets, M, top_k, workspace: as in moe_experts (same
+ *                    workspace size query, same zero-once rule).
+ *   expert_weights   [M, top_k] in weights_dtype (expanded order t*top_k+j).
+ *   permuted_to_expanded  i32 [M*top_k] from moe_permute: entry p < R is the
+ *                    expanded index of permuted row p (the inverse of
+ *                    expanded_idx_to_permuted_idx). Entries outside
+ *                    [0, M*top_k) set MOE_ERR_DEVICE_INDEX and are skipped.
+ *   shared_out       [M, K] in shared_dtype, or NULL (then out starts at 0).
+ *   out              f32 [M, K] (f32 only: the reductions accumulate in it).
+ *
+ * Differences from moe_experts + moe_finalize: the order in which the top_k
+ * routes (and the split-K parts of one route) are added is not fixed, so the
+ * result can differ between runs by f32 rounding (a few ulp of out); it is
+ * within the same tolerance of the exact result. gemm2_permuted is neither
+ * read nor written. Returns MOE_ERR_INVALID_ARG if out aliases an input.
+ * ---------------------------------------------------------------------- */
+moe_status moe_experts_fused_finalize(const moe_weights* w,
+                                      const void* x_perm, const int32_t* expert_offsets,
+                                      int M, int top_k,
+                                      const void* expert_weights, moe_dtype weights_dtype,
+                                      const int32_t* permuted_to_expanded,
+                                      const void* shared_out, moe_dtype shared_dtype,
+                                      float routed_scaling_factor, float* out,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_finalize -- apply the routing weights and reduce over top_k
  * (modular_kernel.py, FusedMoEPrepareAndFinalize.finalize), then the routed
  * scale and the shared-expert add (moe_output.py, MoEOutput: the shared

@@ -34,7 +34,8 @@ MOE_WEIGHTS_MXFP4 = 1
 EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
-    "moe_experts", "moe_finalize", "moe_shared_expert_workspace_size", "moe_shared_expert",
+    "moe_experts", "moe_experts_fused_finalize", "moe_finalize", "moe_shared_expert_workspace_size",
+    "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid",
 )
@@ -79,6 +80,8 @@ _SIGS = {
     "moe_experts_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I], _Z),
     "moe_experts": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _I, _F,
                      _P, _I, _P, _Z, _P], _I),
+    "moe_experts_fused_finalize": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
+                                    _P, _Z, _P], _I),
     "moe_finalize": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P], _I),
     "moe_shared_expert_workspace_size": ([_I, _I, _I], _Z),
     "moe_shared_expert": ([_P, _P, _I, _I, _P, _I, _P, _I, _P, _Z, _P], _I),
@@ -185,6 +188,15 @@ def moe_experts(weights: moe_weights, x_perm, expert_offsets, M, top_k, gemm2_pe
                                           _ptr(expanded_idx_to_permuted_idx), _ptr(shared_out),
                                           shared_dtype, routed_scaling_factor, _ptr(out), out_dtype,
                                           _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def moe_experts_fused_finalize(weights: moe_weights, x_perm, expert_offsets, M, top_k, expert_weights,
+                               weights_dtype, permuted_to_expanded, shared_out, shared_dtype,
+                               routed_scaling_factor, out, workspace, workspace_bytes, stream=None):
+    _check("moe_experts_fused_finalize", lib.moe_experts_fused_finalize(
+        ctypes.byref(weights), _ptr(x_perm), _ptr(expert_offsets), M, top_k, _ptr(expert_weights), weights_dtype,
+        _ptr(permuted_to_expanded), _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def moe_finalize(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights, weights_dtype,

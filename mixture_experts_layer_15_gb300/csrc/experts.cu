@@ -76,8 +76,10 @@ struct GemmPlan {
     size_t partial_bytes;
 };
 
+// direct: the splits reduce into the output themselves (the finalizing GEMM2):
+// no partial tiles, and an extra split costs one more tile of reductions.
 GemmPlan plan_gemm(int gemm_index, int bt, int na, int n_wtiles, int kr, int rows_alloc, int groups,
-                   int sm_count) {
+                   int sm_count, bool direct = false) {
     GemmPlan p;
     p.na = na;
     p.n_wtiles = n_wtiles;
@@ -91,7 +93,7 @@ GemmPlan plan_gemm(int gemm_index, int bt, int na, int n_wtiles, int kr, int row
         // time ~ waves x (k-blocks per unit + the split epilogue's extra
         // traffic: writing and reading back the fp32 partial tile, counted in
         // k-blocks of operand traffic)
-        const double part = 2.0 * na * kBM * bt * 4.0;
+        const double part = (direct ? 1.0 : 2.0) * na * kBM * bt * 4.0;
         const double kblock = na * kBM * kBK * 2.0 + bt * kBK * 2.0;
         const double ovh = part / kblock;
         const int cap = nkb / 4 > 1 ? (nkb / 4 < 16 ? nkb / 4 : 16) : 1;
@@ -106,7 +108,7 @@ GemmPlan plan_gemm(int gemm_index, int bt, int na, int n_wtiles, int kr, int row
     if (g_override.splits[gemm_index] > 0 && p.max_tiles <= kMaxSplitTiles) s = g_override.splits[gemm_index];
     if (s > nkb) s = nkb;
     p.splits = s;
-    p.partial_bytes = s > 1 ? static_cast<size_t>(p.max_tiles) * s * na * kBM * bt * sizeof(float) : 0;
+    p.partial_bytes = (s > 1 && !direct) ? static_cast<size_t>(p.max_tiles) * s * na * kBM * bt * sizeof(float) : 0;
     return p;
 }
 
@@ -120,7 +122,8 @@ struct Layout {
     size_t off_act, off_p1, off_p2, total;
 };
 
-Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count) {
+// fin: GEMM2 finalizes in its epilogue (needs no more workspace than without)
+Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin = false) {
     Layout L;
     const int K = w->K, N = w->N;
     L.bt = g_override.token_tile > 0 ? g_override.token_tile
@@ -128,7 +131,7 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     L.g1 = plan_gemm(0, L.bt, 2, N / kBM, K, rows_alloc, groups, sm_count);
     int na2 = (K % 256 == 0) ? 2 : 1;
     if (g_override.gemm2_na == 1 || (g_override.gemm2_na == 2 && K % 256 == 0)) na2 = g_override.gemm2_na;
-    L.g2 = plan_gemm(1, L.bt, na2, K / (na2 * kBM), N, rows_alloc, groups, sm_count);
+    L.g2 = plan_gemm(1, L.bt, na2, K / (na2 * kBM), N, rows_alloc, groups, sm_count, fin);
     // GEMM1 and GEMM2 in one launch when GEMM2 units take two A tiles and the
     // token-tile counters fit their region
     L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
@@ -187,7 +190,8 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     const int K = w->K, N = w->N;
     const bool mx = w->format == MOE_WEIGHTS_MXFP4;
     const int groups = p.offsets != nullptr ? w->E_local : 1;
-    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count);
+    const bool fin = p.fin_out != nullptr;
+    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count, fin);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* counters = reinterpret_cast<int*>(ws);
     void* act = ws + L.off_act;
@@ -226,7 +230,12 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a2.a1_offset = kBM;
     a2.splits = L.g2.splits;
     a2.out_ld = K;
-    a2.out = p.y;
+    a2.out = fin ? static_cast<void*>(p.fin_out) : p.y;
+    a2.inverse = p.inverse;
+    a2.fw = p.fin_weights;
+    a2.fw_dtype = p.fin_weights_dtype;
+    a2.top_k = p.top_k;
+    a2.rsf = p.rsf;
     a2.partials = reinterpret_cast<float*>(ws + L.off_p2);
     a2.counters = counters + kMaxSplitTiles;
     a2.max_tiles = L.g2.max_tiles;
@@ -235,8 +244,15 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     ka.max_token_tiles = L.max_token_tiles;
 
     const int grid = dev.sm_count;
+    if (fin) {
+        // out = shared (or 0) first; the GEMM2 epilogue adds every route into it
+        const cudaError_t e0 = launch_out_init(p.fin_shared, p.fin_shared_dtype, p.M, K, p.fin_out, dev, s);
+        if (e0 != cudaSuccess) return e0;
+    }
     if (L.fused) {
         ka.nphase = 2;
+        if (fin) return mx ? gemm::launch_gemm_final_mxfp4(1, L.bt, 2, m, ka, grid, s)
+                           : gemm::launch_gemm_final_bf16(1, L.bt, 2, m, ka, grid, s);
         return launch_one(mx, 1, gemm::MODE_PLAIN, L.bt, 2, p.y_dtype, m, ka, grid, s);
     }
     ka.nphase = 1;
@@ -249,6 +265,8 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     m2.A[0] = m.A[1];
     m2.S[0] = m.S[1];
     m2.B[0] = m.B[1];
+    if (fin) return mx ? gemm::launch_gemm_final_mxfp4(0, L.bt, L.g2.na, m2, k2, grid, s)
+                       : gemm::launch_gemm_final_bf16(0, L.bt, L.g2.na, m2, k2, grid, s);
     return launch_one(mx, 0, gemm::MODE_PLAIN, L.bt, L.g2.na, p.y_dtype, m2, k2, grid, s);
 }
 

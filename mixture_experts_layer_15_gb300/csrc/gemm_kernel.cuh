@@ -88,7 +88,11 @@ constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxSplitTiles = 16384;     // capacity of one counter region
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-enum { MODE_SWIGLU = 0, MODE_PLAIN = 1 };
+// MODE_FINAL: GEMM2 with the finalize folded into its epilogue: every
+// accumulator value y of permuted row p is added as rsf * w[e] * y into
+// out[e / top_k] (e = permuted_to_expanded[p]) with f32 reductions; nothing
+// else is stored, and a split-K split reduces its own partial directly.
+enum { MODE_SWIGLU = 0, MODE_PLAIN = 1, MODE_FINAL = 2 };
 
 struct GemmArgs {
     const int32_t* offsets;   // [groups+1] or nullptr
@@ -107,6 +111,12 @@ struct GemmArgs {
     int* counters;
     int max_tiles;
     int* err;
+    // MODE_FINAL only
+    const int32_t* inverse;   // permuted_to_expanded [rows]
+    const void* fw;           // routing weights [rows] (expanded order)
+    int fw_dtype;
+    int top_k;
+    float rsf;
 };
 
 // Arguments of one launch: a single GEMM (nphase = 1), or GEMM1 followed by
@@ -152,7 +162,8 @@ struct Cfg {
     static constexpr int OFF_TTP = OFF_PREFIX + 2 * (kMaxGroups + 1) * 4;  // [kMaxGroups+1] token tiles
     static constexpr int OFF_OFFS = OFF_TTP + (kMaxGroups + 1) * 4;      // [kMaxGroups+1]
     static constexpr int OFF_TMP = OFF_OFFS + (kMaxGroups + 1) * 4;      // [33]
-    static constexpr int SMEM_BYTES = OFF_TMP + 33 * 4 + 1024;   // + alignment slack
+    static constexpr int OFF_ROUTE = OFF_TMP + 36 * 4;                   // MODE_FINAL: [BT] token, [BT] scale
+    static constexpr int SMEM_BYTES = OFF_ROUTE + 2 * BT * 4 + 1024;    // + alignment slack
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N");
@@ -268,6 +279,52 @@ __device__ __forceinline__ void emit16(const Unit& un, const GemmArgs& a, int ro
     }
 }
 
+// The routing of a unit's token columns, loaded into shared memory by the
+// epilogue threads before they wait for the accumulator (so the loads overlap
+// the unit's mainloop): tok[c] = token of column c (-1: none), scl[c] =
+// rsf * routing weight.
+__device__ __forceinline__ void load_route_table(const Unit& un, const GemmArgs& a, int etid, int nthreads,
+                                                 int* tok, float* scl) {
+    for (int c = etid; c < un.ncols; c += nthreads) {
+        const int r = un.row0 + c;
+        int t = -1;
+        float sc = 0.0f;
+        if (r < un.row_end) {
+            const int e = __ldg(a.inverse + r);
+            if (e < 0 || e >= a.rows_alloc) {
+                set_error(a.err, MOE_ERR_DEVICE_INDEX);
+            } else {
+                t = e / a.top_k;
+                sc = a.rsf * load_as_f32(a.fw, static_cast<size_t>(e), a.fw_dtype);
+            }
+        }
+        tok[c] = t;
+        scl[c] = sc;
+    }
+}
+
+// MODE_FINAL epilogue of 16 token columns [c0, c0+16): every lane adds its
+// weight row's values, times the column's scaled weight, into the tokens'
+// output rows. The 32 lanes of a warp hold 32 consecutive weight rows, so
+// each reduction instruction covers 128 contiguous bytes of one output row.
+template <int NA>
+__device__ __forceinline__ void emit16_final(const Unit& un, const GemmArgs& a, int row_in_tile, int c0,
+                                             const int* tok, const float* scl,
+                                             const float (&v0)[16], const float (&v1)[16]) {
+    float* out = static_cast<float*>(a.out);
+    const int col = un.wt * a.wtile_rows + row_in_tile;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int t = tok[c0 + i];                   // same address in every lane: a broadcast
+        if (t >= 0) {
+            const float si = scl[c0 + i];
+            float* o = out + static_cast<size_t>(t) * a.out_ld + col;
+            atomicAdd(o, si * v0[i]);
+            if (NA == 2) atomicAdd(o + kBM, si * v1[i]);
+        }
+    }
+}
+
 // ---- MXFP4 decode -------------------------------------------------------------------
 // Eight e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j)
 // -> eight bf16 values times 2^(scale-127), as four bf16x2 words.
@@ -352,6 +409,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     int* ttp = reinterpret_cast<int*>(smem + C::OFF_TTP);
     int* offs = reinterpret_cast<int*>(smem + C::OFF_OFFS);
     int* tmp = reinterpret_cast<int*>(smem + C::OFF_TMP);
+    int* route_tok = reinterpret_cast<int*>(smem + C::OFF_ROUTE);
+    float* route_scl = reinterpret_cast<float*>(smem + C::OFF_ROUTE + 4 * BT);
     const GemmArgs& a0 = ka.g[0];
     const int groups = a0.groups;
 
@@ -558,11 +617,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         // one unit's outputs from the accumulator values v0/v1 of columns [c0, c0+16)
         auto emit = [&](int ph, const Unit& un, const GemmArgs& a, int c0, const float (&v0)[16],
                         const float (&v1)[16]) {
-            if (FUSED) {
-                if (ph == 0) emit16<2, MODE_SWIGLU, __nv_bfloat16>(un, a, row_in_tile, c0, v0, v1);
-                else emit16<2, MODE_PLAIN, OutT>(un, a, row_in_tile, c0, v0, v1);
+            if (FUSED && ph == 0) {
+                emit16<2, MODE_SWIGLU, __nv_bfloat16>(un, a, row_in_tile, c0, v0, v1);
+            } else if (MODE == MODE_FINAL) {
+                emit16_final<NA>(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
             } else {
-                emit16<NA, MODE, OutT>(un, a, row_in_tile, c0, v0, v1);
+                emit16<NA, (FUSED ? MODE_PLAIN : MODE), OutT>(un, a, row_in_tile, c0, v0, v1);
             }
         };
         // fused launches: after the stores of a finished GEMM1 tile, count it
@@ -580,12 +640,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             const GemmArgs& a = ka.g[ph];
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
+            if (MODE == MODE_FINAL && (!FUSED || ph == 1)) {
+                named_bar_sync(1, kEpiThreads);              // the previous unit is done with the table
+                load_route_table(un, a, etid, kEpiThreads, route_tok, route_scl);
+            }
             wait_bar(tfull_bar(buf), use, abort_flag, a0.err);
-            named_bar_sync(1, kEpiThreads);                  // all threads decide together
-            if (*abort_flag) break;
+            // all threads decide together (and the route table is visible)
+            if (named_bar_or(1, kEpiThreads, *abort_flag != 0)) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
-            if (a.splits == 1) {
+            // a finalizing phase reduces every split's partial into out directly
+            const bool direct = a.splits == 1 || (MODE == MODE_FINAL && (!FUSED || ph == 1));
+            if (direct) {
 #pragma unroll 1
                 for (int c0 = c_first; c0 < un.ncols; c0 += c_step) {
                     float v0[16], v1[16];
@@ -750,6 +816,16 @@ cudaError_t launch_bt(int bt, const Maps& m, const KernelArgs& ka, int grid, cud
 
 // A single GEMM (fused = 0; mode 0 = GEMM1, 1 = GEMM2 with na tiles per unit)
 // or GEMM1 -> GEMM2 fused (fused = 1), of one weight format.
+// GEMM2 with the finalize in its epilogue (MODE_FINAL, f32 out): alone with
+// na tiles per unit, or as phase 1 of a fused launch (fused = 1, na = 2).
+template <bool MX>
+cudaError_t launch_gemm_final(int fused, int bt, int na, const Maps& m, const KernelArgs& ka, int grid,
+                              cudaStream_t s) {
+    if (fused) return launch_bt<2, MODE_FINAL, float, MX, true>(bt, m, ka, grid, s);
+    if (na == 2) return launch_bt<2, MODE_FINAL, float, MX, false>(bt, m, ka, grid, s);
+    return launch_bt<1, MODE_FINAL, float, MX, false>(bt, m, ka, grid, s);
+}
+
 template <bool MX>
 cudaError_t launch_gemm(int fused, int mode, int bt, int na, int out_dtype, const Maps& m, const KernelArgs& ka,
                         int grid, cudaStream_t s) {
@@ -771,6 +847,11 @@ cudaError_t launch_gemm_bf16(int fused, int mode, int bt, int na, int out_dtype,
                              const KernelArgs& ka, int grid, cudaStream_t s);
 cudaError_t launch_gemm_mxfp4(int fused, int mode, int bt, int na, int out_dtype, const Maps& m,
                               const KernelArgs& ka, int grid, cudaStream_t s);
+// Defined in gemm_final_bf16.cu and gemm_final_mxfp4.cu.
+cudaError_t launch_gemm_final_bf16(int fused, int bt, int na, const Maps& m, const KernelArgs& ka, int grid,
+                                   cudaStream_t s);
+cudaError_t launch_gemm_final_mxfp4(int fused, int bt, int na, const Maps& m, const KernelArgs& ka, int grid,
+                                    cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace moe

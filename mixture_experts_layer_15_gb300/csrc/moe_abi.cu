@@ -372,6 +372,52 @@ moe_status moe_experts(const moe_weights* w, const void* x_perm, const int32_t* 
                                           shared_dtype, routed_scaling_factor, out, out_dtype, err, stream));
 }
 
+moe_status moe_experts_fused_finalize(const moe_weights* w, const void* x_perm, const int32_t* expert_offsets,
+                                      int M, int top_k, const void* expert_weights, moe_dtype weights_dtype,
+                                      const int32_t* permuted_to_expanded, const void* shared_out,
+                                      moe_dtype shared_dtype, float routed_scaling_factor, float* out,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    const moe_status ws_ok = check_weights(w);
+    if (ws_ok != MOE_OK) return ws_ok;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    const moe_status a = check_finalize_args(expert_weights, weights_dtype, permuted_to_expanded, shared_out,
+                                             shared_dtype, out, MOE_DTYPE_F32);
+    if (a != MOE_OK) return a;
+    if (static_cast<const void*>(out) == shared_out || static_cast<const void*>(out) == expert_weights ||
+        static_cast<const void*>(out) == x_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (M == 0) return MOE_OK;
+    if (x_perm == nullptr || expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    const int rows = M * top_k;
+    const size_t need = moe::experts_workspace_bytes(w, rows, M, info);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    moe::ExpertsProblem p;
+    p.w = w;
+    p.x = x_perm;
+    p.rows_alloc = rows;
+    p.M = M;
+    p.offsets = expert_offsets;
+    p.single_rows = 0;
+    p.y = nullptr;
+    p.y_dtype = MOE_DTYPE_F32;
+    p.fin_out = out;
+    p.inverse = permuted_to_expanded;
+    p.fin_weights = expert_weights;
+    p.fin_weights_dtype = weights_dtype;
+    p.fin_shared = shared_out;
+    p.fin_shared_dtype = shared_dtype;
+    p.top_k = top_k;
+    p.rsf = routed_scaling_factor;
+    return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
+}
+
 size_t moe_shared_expert_workspace_size(int M, int K, int Ns) {
     if (M <= 0 || K <= 0 || Ns <= 0 || K % 128 != 0 || Ns % 128 != 0) return 0;
     moe_weights w{};

@@ -53,6 +53,9 @@ cudaError_t launch_finalize(const void* gemm2, int gemm2_dtype, int num_rows,
                             const void* weights, int weights_dtype, const int32_t* map,
                             int M, int top_k, int K, const void* shared, int shared_dtype,
                             float rsf, void* out, int out_dtype, int* err, cudaStream_t stream);
+// out[M, K] f32 = shared (shared_dtype) or 0, the start of the fused finalize.
+cudaError_t launch_out_init(const void* shared, int shared_dtype, int M, int K, float* out, const DeviceInfo& dev,
+                            cudaStream_t stream);
 
 // ---- grouped expert GEMMs (gemm.cu) --------------------------------------------
 // One grouped "gated MLP" problem: E groups of rows of `x` (bf16 [rows_alloc, K]),
@@ -65,8 +68,18 @@ struct ExpertsProblem {
     int M;                       // tokens (bounds the rows one group can have)
     const int32_t* offsets;      // [E+1] device, or nullptr
     int single_rows;             // rows of the single group when offsets == nullptr
-    void* y;                     // [rows_alloc, K] output (bf16 or f32)
+    void* y;                     // [rows_alloc, K] output (bf16 or f32); unused when fin_out is set
     int y_dtype;
+    // Finalize in the GEMM2 epilogue (fin_out != nullptr): fin_out [M, K] f32
+    // = fin_shared + rsf * sum over routes of w * y, f32 reductions.
+    float* fin_out = nullptr;
+    const int32_t* inverse = nullptr;     // permuted_to_expanded [rows_alloc]
+    const void* fin_weights = nullptr;    // [M * top_k], expanded order
+    int fin_weights_dtype = 0;
+    const void* fin_shared = nullptr;     // [M, K] or nullptr
+    int fin_shared_dtype = 0;
+    int top_k = 1;
+    float rsf = 1.0f;
 };
 
 void set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse);

@@ -42,14 +42,16 @@ class MoELayer:
     w1/w2 (and scales) hold the E_local local experts; ``expert_map`` (int32
     [E]) maps global expert ids to local ids (-1 = not local). Routing weights,
     gemm2_permuted and the output are stored in the given dtypes (float32 by
-    default: see the precision notes of the C ABI).
+    default: see the precision notes of the C ABI). ``fused_finalize`` (f32
+    output only) folds the finalize into GEMM2 (moe_experts_fused_finalize):
+    no gemm2_permuted round trip, the top-k reduction order is not fixed.
     """
 
     def __init__(self, *, K, N, E, top_k, w1, w2, w1_scale=None, w2_scale=None,
                  fmt=L.MOE_WEIGHTS_BF16, route="softmax", score_bias=None, n_group=1, topk_group=1,
                  routed_scaling_factor=1.0, expert_map=None, E_local=None, ws1=None, ws2=None,
                  weights_dtype=L.MOE_DTYPE_F32, gemm2_dtype=L.MOE_DTYPE_F32,
-                 out_dtype=L.MOE_DTYPE_F32):
+                 out_dtype=L.MOE_DTYPE_F32, fused_finalize=False):
         self.K, self.N, self.E, self.top_k = K, N, E, top_k
         self.E_local = E if E_local is None else E_local
         self.w1, self.w2, self.w1_scale, self.w2_scale = w1, w2, w1_scale, w2_scale
@@ -63,6 +65,9 @@ class MoELayer:
         self.ws1, self.ws2 = ws1, ws2
         self.Ns = 0 if ws1 is None else ws1.shape[0] // 2
         self.weights_dtype, self.gemm2_dtype, self.out_dtype = weights_dtype, gemm2_dtype, out_dtype
+        if fused_finalize and out_dtype != L.MOE_DTYPE_F32:
+            raise ValueError("fused_finalize accumulates into an f32 output")
+        self.fused_finalize = bool(fused_finalize)
         self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale)
         self._bufs = {}
 
@@ -129,6 +134,11 @@ class MoELayer:
         # the sigmoid router folds the routed scale into its weights
         rsf = 1.0 if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else self.rsf
         wdt = L.MOE_DTYPE_F32 if wts.dtype == torch.float32 else L.MOE_DTYPE_BF16
+        if do_finalize and self.fused_finalize:
+            L.moe_experts_fused_finalize(self.cw, b.x_perm, b.offsets, M, self.top_k, wts, wdt, b.inverse,
+                                         b.shared, self.gemm2_dtype, rsf, b.out, b.exp_ws, b.exp_ws.numel(),
+                                         stream)
+            return b
         L.moe_experts(self.cw, b.x_perm, b.offsets, M, self.top_k, b.gemm2, self.gemm2_dtype,
                       1 if do_finalize else 0,
                       wts if do_finalize else None, wdt, b.pmap if do_finalize else None,

@@ -246,7 +246,7 @@ def test_route_permute_matches_two_calls(moe, name, M, masked):
 
 # ------------------------------------------------------------------ whole layer
 
-def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0):
+def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False):
     cfg = synth.CONFIGS[name]
     li = layer_inputs(name)
     x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
@@ -261,6 +261,8 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
             kw.update(w1_scale=li.w1_scale[keep].contiguous(), w2_scale=li.w2_scale[keep].contiguous())
     if bf16_storage:
         kw.update(weights_dtype=moe.MOE_DTYPE_BF16, gemm2_dtype=moe.MOE_DTYPE_BF16, out_dtype=moe.MOE_DTYPE_BF16)
+    if fused_finalize:
+        kw.update(fused_finalize=True)
     layer = make_layer(moe, name, li, **kw)
     b = layer.forward(x, logits)
     torch.cuda.synchronize()
@@ -305,12 +307,67 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
         t = tol(ref, rel, abs_)
         err = max_err(got, ref)
         assert err <= t, f"max|gpu-oracle| = {err:.4g} > {t:.4g}"
+        if fused_finalize:        # gemm2_permuted is not produced on this path
+            return layer, b, x, logits
         # each gathered expert output row (gemm2_permuted), same bar
         ty = tol(np.stack(list(ys.values())), rel, abs_)
         pm = b.pmap.cpu().numpy()
         worst = max(max_err(g2[pm[t_, j]], y) for (t_, j), y in ys.items())
         assert worst <= ty, f"gemm2_permuted row error {worst:.4g} > {ty:.4g}"
     return layer, b, x, logits
+
+
+# ------------------------------------------------------------------ finalize folded into GEMM2
+
+@pytest.mark.parametrize("name,M,masked", [("tiny", 16, False), ("tiny", 300, True), ("mixtral", 1, False),
+                                           ("mixtral", 64, False), ("mixtral", 1024, False),
+                                           ("qwen3", 32, False), ("qwen3", 2048, True),
+                                           ("deepseek", 64, False)])
+def test_fused_finalize_layer(moe, name, M, masked):
+    """moe_experts_fused_finalize: out within the oracle's bar, and equal to the
+    two-pass result (moe_experts + moe_finalize) up to the order of its f32
+    additions."""
+    layer, b, x, logits = _check_layer(moe, name, M, masked=masked, fused_finalize=True,
+                                       sample=16 if name == "deepseek" else None)
+    fused = b.out.clone()
+    layer.fused_finalize = False
+    b2 = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    check_no_device_error(moe)
+    two_pass = b2.out.double().cpu().numpy()
+    rms = float(np.sqrt(np.mean(two_pass ** 2)))
+    diff = float((fused.double().cpu() - b2.out.double().cpu()).abs().max())
+    assert diff <= 1e-4 * rms + 1e-6, f"fused vs two-pass finalize differ by {diff:.3g} (rms {rms:.3g})"
+
+
+def test_fused_finalize_bad_inverse_sets_device_error(moe):
+    """An out-of-range permuted_to_expanded entry is reported and skipped."""
+    cfg = synth.CONFIGS["tiny"]
+    li = layer_inputs("tiny")
+    M = 16
+    x, logits = synth.make_tokens(cfg, M, DEV, li)
+    layer = make_layer(moe, "tiny", li, fused_finalize=True)
+    b = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    good = b.out.clone()
+    R = int(b.offsets[-1])
+    b.inverse[R - 1] = 10 ** 6                                # out of [0, M*top_k)
+    L = moe
+    rsf = layer.rsf
+    L.moe_experts_fused_finalize(layer.cw, b.x_perm, b.offsets, M, cfg.top_k, b.topk_weights, L.MOE_DTYPE_F32,
+                                 b.inverse, None, L.MOE_DTYPE_F32, rsf, b.out, b.exp_ws, b.exp_ws.numel())
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == moe.MOE_ERR_DEVICE_INDEX
+    assert moe.moe_get_error() == 0
+    assert torch.isfinite(b.out).all()
+    # only the token of the corrupted row changed (beyond the f32 reordering
+    # the unordered additions allow)
+    t_bad = int(b.pmap.flatten().tolist().index(R - 1)) // cfg.top_k
+    d = (b.out - good).abs().max(dim=1).values
+    rms = float(good.pow(2).mean().sqrt())
+    others = torch.cat([d[:t_bad], d[t_bad + 1:]])
+    assert float(others.max()) <= 1e-5 * rms
+    assert float(d[t_bad]) > 1e-3 * rms
 
 
 @pytest.mark.parametrize("M", [16, 1, 5, 300])
