@@ -133,10 +133,15 @@ __global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int
     permute_single_chunk(ids, n, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, sm);
 }
 
-// Router and single-chunk permute in one kernel (small batches): every CTA
-// routes all M tokens (one warp per token, the router's own per-token code),
-// keeps the ids in shared memory, then permutes them. CTA 0 writes the ids
-// and weights.
+// Router and single-chunk permute in one kernel (small batches), launched in
+// clusters of G CTAs. The CTAs of a cluster split the tokens (one warp per
+// token, the router's own per-token code) and keep the routed ids in their
+// shared memory; after a cluster barrier every CTA reads the whole id list
+// through distributed shared memory, and after a second one (no CTA reads
+// another's shared memory past it) every CTA runs the same single-chunk
+// permute and copies its share of the rows. Clusters beyond the first redo
+// the routing (cheap at these sizes) and only add row-copy bandwidth; the
+// first cluster writes the ids and weights.
 template <int SLOTS, bool SIGMOID>
 __global__ void route_permute_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int M,
                                      int E, int top_k, int n_group, int topk_group, float rsf,
@@ -145,15 +150,20 @@ __global__ void route_permute_kernel(const float* __restrict__ logits, const flo
                                      const __nv_bfloat16* __restrict__ x, int K,
                                      int32_t* __restrict__ offsets, int32_t* __restrict__ map,
                                      int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
-                                     int* err) {
+                                     int G, int* err) {
     extern __shared__ int sm[];
     const int W = blockDim.x >> 5, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int* ids_s = sm;                                             // [blockDim] routed expert per route
-    float* bsc = reinterpret_cast<float*>(ids_s + blockDim.x);   // [W][E] sigmoid router scratch
+    const int n = M * top_k;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool first_cluster = static_cast<int>(blockIdx.x) < G;
+    int* ids_own = sm;                                           // [blockDim] routes this CTA routed
+    int* ids_all = ids_own + blockDim.x;                         // [blockDim] every route
+    float* bsc = reinterpret_cast<float*>(ids_all + blockDim.x); // [W][E] sigmoid router scratch
     int* rest = reinterpret_cast<int*>(bsc + (SIGMOID ? W * E : 0));
     pdl_wait();
     pdl_trigger();
-    for (int t = warp; t < M; t += W) {
+    const int GW = G * W;
+    for (int t = rank * W + warp; t < M; t += GW) {
         int id;
         float w;
         if (SIGMOID)
@@ -163,25 +173,56 @@ __global__ void route_permute_kernel(const float* __restrict__ logits, const flo
             route::route_token_softmax<SLOTS>(logits + static_cast<size_t>(t) * E, E, top_k, rsf, lane, id, w);
         if (lane < top_k) {
             const int o = t * top_k + lane;
-            ids_s[o] = id;
-            if (blockIdx.x == 0) {
+            ids_own[o] = id;
+            if (first_cluster) {
                 ids_out[o] = id;
                 store_from_f32(w_out, o, w, wdtype);
             }
         }
     }
-    __syncthreads();
-    permute_single_chunk(ids_s, M * top_k, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, rest);
+    __syncwarp();
+    cluster_sync_all();                                          // routed ids visible cluster-wide
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int owner = ((i / top_k) % GW) / W;                // the CTA whose warp routed token i / top_k
+        ids_all[i] = owner == rank ? ids_own[i] : ld_cluster_i32(ids_own + i, static_cast<uint32_t>(owner));
+    }
+    __syncwarp();
+    cluster_sync_all();                                          // remote reads done; ids_all visible
+    permute_single_chunk(ids_all, n, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, rest);
 }
 
 template <int SLOTS, bool SIGMOID>
-cudaError_t launch_route_permute_t(dim3 grid, dim3 block, size_t smem, cudaStream_t s, const float* logits,
-                                   const float* bias, int M, int E, int top_k, int n_group, int topk_group,
-                                   float rsf, int32_t* ids, void* w, int wdtype, const int32_t* emap, int E_l,
-                                   const __nv_bfloat16* x, int K, int32_t* offsets, int32_t* map, int32_t* inverse,
-                                   __nv_bfloat16* xp, int* err) {
-    return launch_pdl(route_permute_kernel<SLOTS, SIGMOID>, grid, block, smem, s, logits, bias, M, E, top_k,
-                      n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, x, K, offsets, map, inverse, xp, err);
+cudaError_t launch_route_permute_t(int clusters, int G, dim3 block, size_t smem, cudaStream_t s,
+                                   const float* logits, const float* bias, int M, int E, int top_k, int n_group,
+                                   int topk_group, float rsf, int32_t* ids, void* w, int wdtype,
+                                   const int32_t* emap, int E_l, const __nv_bfloat16* x, int K, int32_t* offsets,
+                                   int32_t* map, int32_t* inverse, __nv_bfloat16* xp, int* err) {
+    return launch_pdl_cluster(route_permute_kernel<SLOTS, SIGMOID>, dim3(clusters * G), block, smem, G, s, logits,
+                              bias, M, E, top_k, n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, x, K, offsets,
+                              map, inverse, xp, G, err);
+}
+
+// Launch shape of the fused kernel: W warps per CTA (one thread per route for
+// the permute, and enough warps that a cluster of G <= 8 CTAs routes every
+// token with one warp), and its shared memory.
+struct RoutePermuteShape {
+    int W, G;
+    size_t smem;
+};
+RoutePermuteShape route_permute_shape(int M, int top_k, int E, int E_l, int method) {
+    RoutePermuteShape r;
+    const int n = M * top_k;
+    int W = (n + 31) / 32;
+    const int per_cluster = (M + 7) / 8;                         // warps per CTA so 8 CTAs cover M tokens
+    if (W < per_cluster) W = per_cluster;
+    if (W < 1) W = 1;
+    r.W = W;
+    r.G = (M + W - 1) / W;
+    if (r.G > 8) r.G = 8;
+    if (r.G < 1) r.G = 1;
+    const bool sig = method == MOE_ROUTE_SIGMOID_GROUPED_TOPK;
+    r.smem = sizeof(int) * (2 * 32 * W + W * E_l + E_l + 1 + 32 * W + 33) + (sig ? sizeof(float) * W * E : 0);
+    return r;
 }
 
 // ---- several chunks ------------------------------------------------------------
@@ -207,12 +248,19 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchu
     pdl_wait();
     pdl_trigger();
     for (int e = threadIdx.x; e < E_l; e += blockDim.x) {
+        // the counts of 8 chunks are loaded before any is used, so the loads
+        // overlap instead of forming one long dependent chain
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            const size_t o = static_cast<size_t>(c) * E_l + e;
-            const int v = chunk_counts[o];
-            chunk_counts[o] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = c0 + i < nchunks ? chunk_counts[static_cast<size_t>(c0 + i) * E_l + e] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (c0 + i < nchunks) chunk_counts[static_cast<size_t>(c0 + i) * E_l + e] = run;
+                run += v[i];
+            }
         }
         total[e] = run;
     }
@@ -221,7 +269,15 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchu
     for (int e = threadIdx.x; e < E_l; e += blockDim.x) {
         const int base = total[e];
         offsets[e] = base;
-        for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<size_t>(c) * E_l + e] += base;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = c0 + i < nchunks ? chunk_counts[static_cast<size_t>(c0 + i) * E_l + e] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c0 + i < nchunks) chunk_counts[static_cast<size_t>(c0 + i) * E_l + e] = v[i] + base;
+        }
     }
     if (threadIdx.x == 0) offsets[E_l] = R;
 }
@@ -267,14 +323,9 @@ __global__ void permute_gather_kernel(const int32_t* __restrict__ offsets, int E
 
 bool route_permute_fusible(int M, int top_k, int E, int E_l, int method) {
     const int n = M * top_k;
-    const int Wmax = warps_per_chunk(E_l);
-    if (M > 64 || n > 32 * Wmax) return false;
-    int W = (n + 31) / 32;
-    W = W < (M < 16 ? M : 16) ? (M < 16 ? M : 16) : W;
-    if (W > Wmax) W = Wmax;
-    const size_t smem = sizeof(int) * (2 * 32 * W + W * E_l + E_l + 1 + 33) +
-                        (method == MOE_ROUTE_SIGMOID_GROUPED_TOPK ? sizeof(float) * W * E : 0);
-    return smem <= 48 * 1024;
+    if (M > 64 || n > 32 * warps_per_chunk(E_l)) return false;
+    const RoutePermuteShape r = route_permute_shape(M, top_k, E, E_l, method);
+    return r.W <= warps_per_chunk(E_l) && r.smem <= 48 * 1024;
 }
 
 cudaError_t launch_route_permute(const float* logits, int M, int E, int top_k, int method, const float* bias,
@@ -283,27 +334,27 @@ cudaError_t launch_route_permute(const float* logits, int M, int E, int top_k, i
                                  int32_t* map, int32_t* inverse, void* x_perm, int* err, const DeviceInfo& dev,
                                  cudaStream_t s) {
     const int n = M * top_k;
-    const int Wmax = warps_per_chunk(E_l);
-    int W = (n + 31) / 32;
-    W = W < (M < 16 ? M : 16) ? (M < 16 ? M : 16) : W;   // enough warps to route in few rounds
-    if (W > Wmax) W = Wmax;
+    const RoutePermuteShape r = route_permute_shape(M, top_k, E, E_l, method);
     const bool sig = method == MOE_ROUTE_SIGMOID_GROUPED_TOPK;
-    const size_t smem = sizeof(int) * (2 * 32 * W + W * E_l + E_l + 1 + 33) + (sig ? sizeof(float) * W * E : 0);
-    int grid = 1;
+    // clusters: one is enough to route; more add row-copy bandwidth (one warp per row)
+    int clusters = 1;
     if (x_perm != nullptr) {
-        grid = ceil_div(n, W);
-        grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
+        clusters = ceil_div(n, r.G * r.W);
+        const int cap = (2 * dev.sm_count) / r.G;
+        if (clusters > cap) clusters = cap;
+        if (clusters < 1) clusters = 1;
     }
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
+    const dim3 block(32 * r.W);
     const int slots = ceil_div(E, 32);
 #define MOE_RP(S)                                                                                            \
-    return sig ? launch_route_permute_t<S, true>(dim3(grid), dim3(32 * W), smem, s, logits, bias, M, E, top_k, \
+    return sig ? launch_route_permute_t<S, true>(clusters, r.G, block, r.smem, s, logits, bias, M, E, top_k,   \
                                                  n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, xb, K,   \
                                                  offsets, map, inverse, xp, err)                              \
-               : launch_route_permute_t<S, false>(dim3(grid), dim3(32 * W), smem, s, logits, bias, M, E,      \
-                                                  top_k, n_group, topk_group, rsf, ids, w, wdtype, emap, E_l,  \
-                                                  xb, K, offsets, map, inverse, xp, err)
+               : launch_route_permute_t<S, false>(clusters, r.G, block, r.smem, s, logits, bias, M, E, top_k, \
+                                                  n_group, topk_group, rsf, ids, w, wdtype, emap, E_l, xb, K,  \
+                                                  offsets, map, inverse, xp, err)
     if (slots <= 1) MOE_RP(1);
     if (slots <= 2) MOE_RP(2);
     if (slots <= 4) MOE_RP(4);

@@ -55,27 +55,18 @@ __device__ __forceinline__ float exp_spec(float t) {
     return __fmul_rn(p, two_n);
 }
 
+// 1/(1+e) correctly rounded: __frcp_rn gives the same bits as __fdiv_rn(1, .)
 __device__ __forceinline__ float sigmoid_spec(float x) {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_spec(-x)));
+    return __frcp_rn(__fadd_rn(1.0f, exp_spec(-x)));
 }
 
-// (key, id) order: a before b if a's key is larger, or equal with a lower id.
-// id >= E marks "no candidate" and loses to any candidate.
-__device__ __forceinline__ bool better(float ka, int ia, float kb, int ib, int E) {
-    if (ia >= E) return false;
-    if (ib >= E) return true;
-    return ka > kb || (ka == kb && ia < ib);
-}
-
-// Warp-wide arg-max of (key, id) with payload; every lane returns the winner.
-__device__ __forceinline__ void warp_argmax(float& key, int& id, float& pay, int E) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float k2 = __shfl_xor_sync(0xffffffffu, key, off);
-        const int i2 = __shfl_xor_sync(0xffffffffu, id, off);
-        const float p2 = __shfl_xor_sync(0xffffffffu, pay, off);
-        if (better(k2, i2, key, id, E)) { key = k2; id = i2; pay = p2; }
-    }
+// Order-preserving 32-bit image of a float32 selection key: a > b (as floats)
+// iff img(a) > img(b) (unsigned). -0.0 is folded onto +0.0 first, so the two
+// compare equal as floats do; NaN maps to 0, below every other key.
+__device__ __forceinline__ uint32_t key_image(float k) {
+    if (isnan(k)) return 0u;
+    const uint32_t u = __float_as_uint(__fadd_rn(k, 0.0f));       // -0.0 + 0.0 = +0.0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -86,31 +77,48 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // top_k selection rounds over the lane's SLOTS candidates. `key[s]` is the
 // selection key of expert lane + 32*s, `pay[s]` a value carried along,
-// `allowed` a bit mask of eligible slots. Lane j < top_k ends with the j-th
-// winner in (out_id, out_key, out_pay).
+// `allowed` a bit mask of eligible slots. Order: larger key first, equal keys
+// to the lower expert id. Each round takes the warp maximum of the key images
+// (one redux), then the lowest expert id holding it: the lowest slot whose
+// ballot is non-empty, and the lowest lane in that ballot. Lane j < top_k ends
+// with the j-th winner in (out_id, out_key, out_pay).
 template <int SLOTS>
 __device__ __forceinline__ void select_topk(const float (&key)[SLOTS], const float (&pay)[SLOTS],
                                             uint32_t allowed, int E, int top_k, int lane,
                                             int& out_id, float& out_key, float& out_pay) {
-    uint32_t taken = 0;
+    uint32_t img[SLOTS];
+    uint32_t live = 0;                                   // slots still selectable
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        img[s] = key_image(key[s]);
+        if (lane + 32 * s < E && ((allowed >> s) & 1u)) live |= 1u << s;
+    }
     out_id = E; out_key = -INFINITY; out_pay = 0.0f;
     for (int j = 0; j < top_k; ++j) {
-        float bk = -INFINITY, bp = 0.0f;
-        int bi = E;
+        uint32_t m = 0;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+            if (((live >> s) & 1u) && img[s] > m) m = img[s];
+        const uint32_t any = __ballot_sync(0xffffffffu, live != 0);
+        if (any == 0) break;                             // fewer candidates than top_k
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, m);
+        int win = -1;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
-            const int id = lane + 32 * s;
-            if (id < E && ((allowed >> s) & 1u) && !((taken >> s) & 1u) &&
-                better(key[s], id, bk, bi, E)) {
-                bk = key[s]; bi = id; bp = pay[s];
-            }
+            const uint32_t b = __ballot_sync(0xffffffffu, ((live >> s) & 1u) && img[s] == gmax);
+            if (win < 0 && b != 0) win = 32 * s + __ffs(b) - 1;
         }
-        warp_argmax(bk, bi, bp, E);
-        if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) { out_id = bi; out_key = bk; out_pay = bp; }
+        const int ws = win >> 5, wl = win & 31;
+        float wk = 0.0f, wp = 0.0f;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+            if (s == ws) { wk = key[s]; wp = pay[s]; }
+        wk = __shfl_sync(0xffffffffu, wk, wl);
+        wp = __shfl_sync(0xffffffffu, wp, wl);
+        if (lane == wl) live &= ~(1u << ws);
+        if (lane == j) { out_id = win; out_key = wk; out_pay = wp; }
     }
 }
-
 
 // One warp routes one token (the logits row `row`): lane j < top_k returns
 // the j-th selected expert and its weight.
@@ -158,7 +166,28 @@ __device__ __forceinline__ void route_token_sigmoid(const float* __restrict__ ro
     // group score: float32 sum of the group's two largest biased scores
     const int G = E / n_group;
     float gscore = -INFINITY;
-    if (lane < n_group) {
+    if (G == 32) {
+        // group g is slot g (experts 32g .. 32g+31): its two largest keys by
+        // warp reductions; the sum is of the same two floats as below
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            if (s >= n_group) break;
+            const uint32_t im = key_image(key[s]);
+            const uint32_t m1 = __reduce_max_sync(0xffffffffu, im);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, im == m1);
+            const int l1 = __ffs(b1) - 1;
+            const float f1 = __shfl_sync(0xffffffffu, key[s], l1);
+            float f2;
+            if (__popc(b1) >= 2) {
+                f2 = f1;
+            } else {
+                const uint32_t m2 = __reduce_max_sync(0xffffffffu, lane == l1 ? 0u : im);
+                const uint32_t b2 = __ballot_sync(0xffffffffu, lane != l1 && im == m2);
+                f2 = __shfl_sync(0xffffffffu, key[s], __ffs(b2) - 1);
+            }
+            if (lane == s) gscore = __fadd_rn(f1, f2);
+        }
+    } else if (lane < n_group) {
         float m1 = -INFINITY, m2 = -INFINITY;
         for (int i = 0; i < G; ++i) {
             const float v = b_row[lane * G + i];
@@ -168,14 +197,20 @@ __device__ __forceinline__ void route_token_sigmoid(const float* __restrict__ ro
         gscore = __fadd_rn(m1, m2);
     }
     __syncwarp();
-    // keep the topk_group best groups (ties to the lower group id)
+    // keep the topk_group best groups (ties to the lower group id); lane g < n_group
+    // holds group g's score
     uint32_t gtaken = 0;
-    for (int j = 0; j < topk_group; ++j) {
-        float k = (lane < n_group && !((gtaken >> lane) & 1u)) ? gscore : -INFINITY;
-        int gi = (lane < n_group && !((gtaken >> lane) & 1u)) ? lane : n_group;
-        float dummy = 0.0f;
-        warp_argmax(k, gi, dummy, n_group);
-        if (gi < n_group) gtaken |= 1u << gi;
+    {
+        const uint32_t gimg = key_image(gscore);
+        bool glive = lane < n_group;
+        for (int j = 0; j < topk_group; ++j) {
+            const uint32_t gmax = __reduce_max_sync(0xffffffffu, glive ? gimg : 0u);
+            const uint32_t b = __ballot_sync(0xffffffffu, glive && gimg == gmax);
+            if (b == 0) break;
+            const int gi = __ffs(b) - 1;
+            gtaken |= 1u << gi;
+            if (lane == gi) glive = false;
+        }
     }
     uint32_t allowed = 0;
 #pragma unroll
