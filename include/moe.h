@@ -364,8 +364,10 @@ moe_status moe_device_check(void);
  * tests): token tile width (16, 32, 64, 128 or 256), the split-K factor of
  * GEMM1 and GEMM2 (clamped so every split keeps at least one K-block), and
  * the number of 128-row weight tiles per GEMM2 work unit (1 or 2; 2 needs
- * K % 256 == 0), and whether GEMM1 and GEMM2 run as one fused launch (1) or
- * two launches (2). 0 restores the automatic choice. It applies to every later
+ * K % 256 == 0), and how GEMM1 and GEMM2 run: one fused launch (1), two
+ * launches (2), or two launches on CTA pairs (3: bf16 weights, 128- or
+ * 256-token tiles, no split-K; otherwise as 2). 0 restores the automatic
+ * choice. It applies to every later
  * call in the process, including the *_workspace_size() queries, so query the
  * workspace size after setting it. Not synchronised with concurrent calls. */
 moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles,

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace moe {
 namespace {
@@ -53,7 +54,7 @@ struct PlanOverride {
     int token_tile = 0;          // 0 = automatic
     int splits[2] = {0, 0};      // GEMM1, GEMM2; 0 = automatic
     int gemm2_na = 0;            // 128-row A tiles per GEMM2 unit (1 or 2); 0 = automatic
-    int fuse = 0;                // 0 = automatic, 1 = one fused launch, 2 = two launches
+    int fuse = 0;                // 0 = automatic, 1 = one fused launch, 2 = two launches, 3 = CTA pairs
 };
 PlanOverride g_override;
 
@@ -117,6 +118,7 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
     int bt;
     bool fused;
+    bool pair;
     int max_token_tiles;
     GemmPlan g1, g2;
     size_t off_act, off_p1, off_p2, total;
@@ -135,7 +137,37 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     // GEMM1 and GEMM2 in one launch when GEMM2 units take two A tiles and the
     // token-tile counters fit their region
     L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
-    L.fused = L.g2.na == 2 && L.max_token_tiles <= kMaxSplitTiles && g_override.fuse != 2;
+    L.fused = L.g2.na == 2 && L.max_token_tiles <= kMaxSplitTiles && g_override.fuse != 2 &&
+              g_override.fuse != 3;
+    // GEMM1 and GEMM2 on CTA pairs (two launches): bf16 weights, 128- or
+    // 256-token tiles, every unit whole (no split-K), 256-row GEMM2 units.
+    // Forced by the override (fuse = 3, with its tile width); chosen
+    // automatically with 256-token tiles when the experts average at least
+    // 256 rows, so that most tiles are full and the units fill the grid. The
+    // choice does not depend on `fin`, so the workspace query and the launch
+    // agree on the layout.
+    const bool pair_ok = w->format == MOE_WEIGHTS_BF16 && K % 256 == 0 && N % kBM == 0 &&
+                         g_override.gemm2_na != 1;
+    L.pair = false;
+    if (pair_ok && g_override.fuse == 3 && (L.bt == 128 || L.bt == 256) && L.g1.splits == 1 &&
+        L.g2.splits == 1 && L.g2.na == 2) {
+        L.pair = true;
+    } else if (pair_ok && g_override.fuse == 0 && g_override.token_tile == 0 && groups > 0 &&
+               rows_alloc / groups >= 256) {
+        const GemmPlan p1 = plan_gemm(0, 256, 2, N / kBM, K, rows_alloc, groups, sm_count);
+        const GemmPlan p2 = plan_gemm(1, 256, 2, K / (2 * kBM), N, rows_alloc, groups, sm_count);
+        if (p1.splits == 1 && p2.splits == 1) {
+            L.pair = true;
+            L.bt = 256;
+            L.g1 = p1;
+            L.g2 = p2;
+        }
+    }
+    if (L.pair) {
+        L.fused = false;
+        L.g1.splits = L.g2.splits = 1;                   // pair units are whole
+        L.g1.partial_bytes = L.g2.partial_bytes = 0;
+    }
     // four counter regions, kept zero between calls: split-K arrivals of
     // GEMM1 and GEMM2, token-tile ready and consumed counts
     size_t off = 4 * kMaxSplitTiles * sizeof(int);
@@ -248,6 +280,20 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
         // out = shared (or 0) first; the GEMM2 epilogue adds every route into it
         const cudaError_t e0 = launch_out_init(p.fin_shared, p.fin_shared_dtype, p.M, K, p.fin_out, dev, s);
         if (e0 != cudaSuccess) return e0;
+    }
+    if (L.pair) {
+        // the same units as the one-CTA plan; each CTA of a pair holds half of
+        // a unit's weight rows (64-row boxes for GEMM1's gate and up halves)
+        // and half of its token rows
+        CUtensorMap pa1, pa2, pb1, pb2;
+        if (!encode_bf16(&pa1, w->w1, K, E * 2 * N, 64) || !encode_bf16(&pa2, w->w2, N, E * K, kBM) ||
+            !encode_bf16(&pb1, p.x, K, p.rows_alloc, L.bt / 2) || !encode_bf16(&pb2, act, N, p.rows_alloc, L.bt / 2))
+            return cudaErrorInvalidValue;
+        const int pairs = dev.sm_count / 2;
+        cudaError_t e = gemm::launch_gemm_pair_bf16(gemm::MODE_SWIGLU, L.bt, MOE_DTYPE_BF16, pa1, pb1, a1, pairs, s);
+        if (e != cudaSuccess) return e;
+        return gemm::launch_gemm_pair_bf16(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, L.bt, p.y_dtype, pa2, pb2, a2,
+                                           pairs, s);
     }
     if (L.fused) {
         ka.nphase = 2;

@@ -157,7 +157,7 @@ moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_ge
         token_tile != 256)
         return MOE_ERR_INVALID_ARG;
     if (splits_gemm1 < 0 || splits_gemm1 > 64 || splits_gemm2 < 0 || splits_gemm2 > 64) return MOE_ERR_INVALID_ARG;
-    if (gemm2_tiles < 0 || gemm2_tiles > 2 || fuse < 0 || fuse > 2) return MOE_ERR_INVALID_ARG;
+    if (gemm2_tiles < 0 || gemm2_tiles > 2 || fuse < 0 || fuse > 3) return MOE_ERR_INVALID_ARG;
     moe::set_plan_override(token_tile, splits_gemm1, splits_gemm2, gemm2_tiles, fuse);
     return MOE_OK;
 }

@@ -340,6 +340,19 @@ def test_fused_finalize_layer(moe, name, M, masked):
     assert diff <= 1e-4 * rms + 1e-6, f"fused vs two-pass finalize differ by {diff:.3g} (rms {rms:.3g})"
 
 
+@pytest.mark.parametrize("name,M,bt,masked,fused", [("qwen3", 2048, 128, False, True), ("qwen3", 2048, 256, False, False),
+                                                   ("qwen3", 4096, 256, True, True), ("mixtral", 512, 256, False, True),
+                                                   ("mixtral", 512, 128, False, False)])
+def test_cta_pair_gemms(moe, name, M, bt, masked, fused):
+    """GEMM1 and GEMM2 on CTA pairs (forced by the plan override): the oracle's
+    bar, with the finalize folded into GEMM2 or as its own pass."""
+    moe.moe_set_plan_override(bt, 0, 0, 0, 3)
+    try:
+        _check_layer(moe, name, M, masked=masked, fused_finalize=fused)
+    finally:
+        moe.moe_set_plan_override(0, 0, 0, 0, 0)
+
+
 def test_fused_finalize_bad_inverse_sets_device_error(moe):
     """An out-of-range permuted_to_expanded entry is reported and skipped."""
     cfg = synth.CONFIGS["tiny"]
