@@ -164,19 +164,26 @@ def make_workload(cfg_name, device, only_m=None, experts=0):
     return cfg, li, layer, batches
 
 
-def launches_per_forward(cfg, M):
-    """Kernels one forward launches (mirrors the library's launch plan)."""
+def launches_per_forward(moe, cfg, layer, M, finalize="fused"):
+    """Kernels one forward launches: the router and permute (mirroring the
+    library's plan), the experts step as the library reports it
+    (moe_experts_launches, from the plan the call uses), and the finalize pass
+    or shared expert where they run."""
     w = max(1, min(32, 8192 // cfg.E))
     if M <= 64 and M * cfg.top_k <= 32 * w:
         n = 1                                                 # router + permute in one kernel
+    elif M * cfg.top_k <= 32 * w:
+        n = 2                                                 # router; single-chunk permute
     else:
-        n = 1 + (1 if M * cfg.top_k <= 32 * w else 4)         # router; permute fused or count/scan/scatter/gather
-    # grouped GEMM1 + GEMM2: one fused launch when GEMM2 units take two
-    # 128-row weight tiles (K % 256 == 0), else two launches
-    n += 1 if cfg.K % 256 == 0 else 2
-    n += 1                                                    # finalize, or the out-init of the fused finalize
+        n = 5                                                 # router; count/scan/scatter/gather
+    fused = finalize == "fused"
+    n += moe.moe_experts_launches(layer.cw, M, cfg.top_k, fused)
+    if not fused:
+        n += 1                                                # finalize pass
     if cfg.shared_N:
-        n += 1 if cfg.K % 256 == 0 else 2                     # shared expert (same kernel, one group)
+        # the shared expert: the same grouped kernels with one group of M rows
+        sw = moe.make_weights(moe.MOE_WEIGHTS_BF16, 1, cfg.K, layer.Ns, layer.ws1, layer.ws2)
+        n += moe.moe_experts_launches(sw, M, 1, False)
     return n
 
 
@@ -413,7 +420,7 @@ def run_gpu(args):
                    "l2": "timed steps: inputs larger than L2 (expert weights streamed every forward); per-M breakdown: a 1 GB read scrub before each sample (median of 20)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "sweep": per_m, "e2e": e2e,
-        "gpu_launches": args.steps * sum(launches_per_forward(cfg, M) for M in sweep),
+        "gpu_launches": args.steps * sum(launches_per_forward(moe, cfg, layer, M, args.finalize) for M in sweep),
         "clocks": clk,
     }
     if rank == 0:

@@ -302,6 +302,12 @@ moe_status moe_experts_fused_finalize(const moe_weights* w,
                                       float routed_scaling_factor, float* out,
                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The number of kernels that moe_experts_fused_finalize (fused_finalize = 1,
+ * counting the initialisation of out) or moe_experts with do_finalize = 0
+ * (fused_finalize = 0) launches for this batch size, from the same launch plan
+ * the calls use; 0 for invalid arguments or without a device. Host-only. */
+int moe_experts_launches(const moe_weights* w, int M, int top_k, int fused_finalize);
+
 /* ------------------------------------------------------------------------
  * moe_finalize -- apply the routing weights and reduce over top_k
  * (modular_kernel.py, FusedMoEPrepareAndFinalize.finalize), then the routed

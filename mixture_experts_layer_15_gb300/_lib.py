@@ -34,7 +34,7 @@ MOE_WEIGHTS_MXFP4 = 1
 EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
-    "moe_experts", "moe_experts_fused_finalize", "moe_finalize", "moe_shared_expert_workspace_size",
+    "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid",
@@ -82,6 +82,7 @@ _SIGS = {
                      _P, _I, _P, _Z, _P], _I),
     "moe_experts_fused_finalize": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
                                     _P, _Z, _P], _I),
+    "moe_experts_launches": ([ctypes.POINTER(moe_weights), _I, _I, _I], _I),
     "moe_finalize": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P], _I),
     "moe_shared_expert_workspace_size": ([_I, _I, _I], _Z),
     "moe_shared_expert": ([_P, _P, _I, _I, _P, _I, _P, _I, _P, _Z, _P], _I),
@@ -197,6 +198,10 @@ def moe_experts_fused_finalize(weights: moe_weights, x_perm, expert_offsets, M, 
         ctypes.byref(weights), _ptr(x_perm), _ptr(expert_offsets), M, top_k, _ptr(expert_weights), weights_dtype,
         _ptr(permuted_to_expanded), _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def moe_experts_launches(weights: moe_weights, M, top_k, fused_finalize) -> int:
+    return int(lib.moe_experts_launches(ctypes.byref(weights), M, top_k, 1 if fused_finalize else 0))
 
 
 def moe_finalize(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights, weights_dtype,

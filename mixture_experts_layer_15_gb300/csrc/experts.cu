@@ -149,8 +149,8 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     const bool pair_ok = w->format == MOE_WEIGHTS_BF16 && K % 256 == 0 && N % kBM == 0 &&
                          g_override.gemm2_na != 1;
     L.pair = false;
-    if (pair_ok && g_override.fuse == 3 && (L.bt == 128 || L.bt == 256) && L.g1.splits == 1 &&
-        L.g2.splits == 1 && L.g2.na == 2) {
+    if (pair_ok && g_override.fuse == 3 && (L.bt == 128 || L.bt == 256) && L.g1.splits == 1 && L.g2.na == 2 &&
+        plan_gemm(1, L.bt, 2, K / (2 * kBM), N, rows_alloc, groups, sm_count).splits == 1) {
         L.pair = true;
     } else if (pair_ok && g_override.fuse == 0 && g_override.token_tile == 0 && groups > 0 &&
                rows_alloc / groups >= 256) {
@@ -214,6 +214,11 @@ void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na, i
 
 size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev) {
     return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count).total;
+}
+
+int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {
+    const Layout L = make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, fin);
+    return (fin ? 1 : 0) + ((L.pair || !L.fused) ? 2 : 1);
 }
 
 cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*workspace_bytes*/, int* err,

@@ -418,6 +418,14 @@ moe_status moe_experts_fused_finalize(const moe_weights* w, const void* x_perm, 
     return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
 }
 
+int moe_experts_launches(const moe_weights* w, int M, int top_k, int fused_finalize) {
+    if (M <= 0 || top_k <= 0 || check_weights(w) != MOE_OK) return 0;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return 0;
+    DeviceInfo info;
+    if (!moe::current_device_info(&info)) return 0;
+    return moe::experts_launches(w, M * top_k, M, fused_finalize != 0, info);
+}
+
 size_t moe_shared_expert_workspace_size(int M, int K, int Ns) {
     if (M <= 0 || K <= 0 || Ns <= 0 || K % 128 != 0 || Ns % 128 != 0) return 0;
     moe_weights w{};

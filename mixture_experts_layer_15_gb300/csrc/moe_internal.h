@@ -84,6 +84,9 @@ struct ExpertsProblem {
 
 void set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse);
 size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev);
+// Kernels one experts call launches (fin: the finalize folded into GEMM2,
+// counting its out initialisation).
+int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev);
 cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t workspace_bytes,
                            int* err, const DeviceInfo& dev, cudaStream_t stream);
 
