@@ -392,13 +392,14 @@ def run_gpu(args):
     achieved = gemm_flops / gemm_secs / 1e12
     traffic = tcase = talg = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath) and not (args.m or args.experts):
+    if os.path.exists(tpath) and not (args.m or args.experts) and args.finalize == "fused":
         try:
             t = json.load(open(tpath)).get(args.config) or {}
             traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
         except Exception:
             traffic = None
-    roof = {"kernel": "grouped_gemm_kernel (GEMM1+silu_and_mul and GEMM2 in one launch per forward)",
+    roof = {"kernel": ("the experts step: grouped GEMM1+silu_and_mul and GEMM2 (with the folded finalize and "
+                       "its out-init): one fused one-CTA launch, or two CTA-pair launches at large M"),
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
             "frac": achieved / pk["bf16_sus"], "peak_kind": f"{pk['src']} bf16 sustained",
             "frac_of_burst": achieved / pk["bf16"], "traffic": traffic, "traffic_case": tcase,
