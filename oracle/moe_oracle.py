@@ -31,6 +31,20 @@ page fixes the precision:
   (modular_kernel.py ``FusedMoEPrepareAndFinalize.finalize``), then the
   routed scale and the shared-expert add (moe_output.py ``MoEOutput`` field
   comments).
+* expert_mlp's activation: ``silu_and_mul`` or ``gelu_and_mul`` (the two
+  activations of modular_kernel.py ``FusedMoEPermuteExpertsUnpermute
+  .activation``), GELU in its exact erf form; and the optional
+  ``activation_clamp`` of flashinfer_moe_ep.py ``build_fi_mega_config``,
+  which the pages pass through without defining (reading: the gate is
+  clamped from above and the up projection to [-c, c] before the activation).
+* experts_batched -- the same experts on the BatchedExperts activation format
+  (modular_kernel.py ``FusedMoEActivationFormat``: [experts, max tokens per
+  expert, hidden], with per-expert token counts).
+* add_rmsnorm / finalize_add_rmsnorm -- the consumer moe_output.py
+  ``MoEOutput`` names for an open reduction, the next layer's RMSNorm, with
+  the top-k reduction folded in: residual += out; y = residual /
+  sqrt(mean(residual^2) + eps) * gamma (RMSNorm as published by Zhang and
+  Sennrich, 2019, in its fused residual-add form).
 * e2m1 / E8M0 decode (flashinfer_moe_ep.py ``_E2M1_LUT`` and
   ``_dequant_fp4_ue8m0_gran32``): here the page fixes the arithmetic --
   an fp32 product of the table value and the scale, returned as bf16 -- and
@@ -51,7 +65,8 @@ __all__ = [
     "E2M1_TABLE", "e2m1_value", "ue8m0_scale", "dequant_mxfp4",
     "sigmoid_f32_spec", "route_softmax_topk", "route_sigmoid_grouped",
     "permute", "expert_mlp", "experts", "finalize", "shared_expert",
-    "moe_forward", "bf16_round",
+    "moe_forward", "bf16_round", "gelu_erf", "experts_batched", "add_rmsnorm",
+    "finalize_add_rmsnorm",
 ]
 
 # --------------------------------------------------------------------------
@@ -288,24 +303,43 @@ def permute(topk_ids: np.ndarray, E: int, expert_map=None):
 # Experts (GEMM1 -> silu_and_mul -> GEMM2), unweighted and unreduced
 # --------------------------------------------------------------------------
 
-def expert_mlp(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
+def gelu_erf(z) -> np.ndarray:
+    """GELU in its exact form, z * Phi(z) = z/2 * (1 + erf(z / sqrt 2)), with
+    Phi the standard normal CDF (erf from scipy.special)."""
+    from scipy.special import erf
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def expert_mlp(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, activation: str = "silu",
+               clamp=None) -> np.ndarray:
     """One expert on token rows x [T, K]: h = x W1^T [T, 2N]; the first N
-    columns are the gate, the last N the up projection (``silu_and_mul``:
-    output width half the input width); a = silu(gate) * up with
-    silu(z) = z / (1 + e^-z); y = a W2^T [T, K]. Float64."""
+    columns are the gate, the last N the up projection (the ``*_and_mul``
+    activations: output width half the input width). With ``clamp`` = c the
+    gate is clamped to at most c and up to [-c, c] first. Then
+    a = act(gate) * up, with silu(z) = z / (1 + e^-z) or gelu = gelu_erf;
+    y = a W2^T [T, K]. Float64."""
     x = np.asarray(x, dtype=np.float64)
     w1 = np.asarray(w1, dtype=np.float64)
     w2 = np.asarray(w2, dtype=np.float64)
     N = w1.shape[0] // 2
     h = x @ w1.T
     gate, up = h[:, :N], h[:, N:]
-    with np.errstate(over="ignore"):
-        a = gate / (1.0 + np.exp(-gate)) * up
+    if clamp is not None:
+        gate = np.minimum(gate, clamp)
+        up = np.clip(up, -clamp, clamp)
+    if activation == "silu":
+        with np.errstate(over="ignore"):
+            a = gate / (1.0 + np.exp(-gate)) * up
+    elif activation == "gelu":
+        a = gelu_erf(gate) * up
+    else:
+        raise ValueError(activation)
     return a @ w2.T
 
 
 def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
-            inverse: np.ndarray, top_k: int) -> np.ndarray:
+            inverse: np.ndarray, top_k: int, activation: str = "silu", clamp=None) -> np.ndarray:
     """``gemm2_permuted`` [R, K]: row p is the output of expert le (the p-th
     row falls in [offsets[le], offsets[le+1])) on token inverse[p] // top_k.
     ``w1``/``w2`` are the local experts' weights as float arrays."""
@@ -316,8 +350,23 @@ def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
         r0, r1 = int(offsets[le]), int(offsets[le + 1])
         if r1 > r0:
             toks = np.asarray(inverse[r0:r1], dtype=np.int64) // top_k
-            out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le])
+            out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le], activation, clamp)
     return out
+
+
+def experts_batched(xb: np.ndarray, counts: np.ndarray, w1: np.ndarray, w2: np.ndarray,
+                    activation: str = "silu", clamp=None) -> np.ndarray:
+    """The experts on the BatchedExperts format: xb [E, T_max, K], expert e's
+    tokens are rows 0 .. counts[e]-1 of xb[e]. Returns y [E, T_max, K] with
+    y[e, r] = the expert's output for r < counts[e], and 0 beyond."""
+    xb = np.asarray(xb, dtype=np.float64)
+    E, T, _ = xb.shape
+    y = np.zeros((E, T, w2.shape[1]), dtype=np.float64)
+    for e in range(E):
+        c = int(counts[e])
+        if c > 0:
+            y[e, :c] = expert_mlp(xb[e, :c], w1[e], w2[e], activation, clamp)
+    return y
 
 
 def shared_expert(x: np.ndarray, ws1: np.ndarray, ws2: np.ndarray) -> np.ndarray:
@@ -350,6 +399,24 @@ def finalize(gemm2_permuted: np.ndarray, expert_weights: np.ndarray, pmap: np.nd
         if shared is not None:
             out[t] += np.asarray(shared[t], dtype=np.float64)
     return out
+
+
+def add_rmsnorm(x: np.ndarray, residual: np.ndarray, gamma: np.ndarray, eps: float):
+    """RMSNorm with the residual add in front: r = residual + x;
+    y = r / sqrt(mean over the hidden dim of r^2 + eps) * gamma.
+    Returns (r, y), float64."""
+    r = np.asarray(residual, dtype=np.float64) + np.asarray(x, dtype=np.float64)
+    ms = np.mean(r * r, axis=-1, keepdims=True)
+    y = r / np.sqrt(ms + eps) * np.asarray(gamma, dtype=np.float64)
+    return r, y
+
+
+def finalize_add_rmsnorm(gemm2_permuted, expert_weights, pmap, residual, gamma, eps, shared=None,
+                         routed_scaling_factor: float = 1.0):
+    """finalize, then add_rmsnorm on its output: the next layer's RMSNorm
+    with the MoE's top-k reduction folded in. Returns (residual', y)."""
+    out = finalize(gemm2_permuted, expert_weights, pmap, shared, routed_scaling_factor)
+    return add_rmsnorm(out, residual, gamma, eps)
 
 
 def moe_forward(x, logits, w1, w2, top_k, route="softmax", score_bias=None,

@@ -362,3 +362,117 @@ def test_mxfp4_layer_equals_bf16_layer_on_dequantised_weights():
     logits = rng.standard_normal((M, E)).astype(np.float32)
     r = O.moe_forward(x, logits, w1, w2, k)
     assert np.isfinite(r["out"]).all()
+
+
+# ---------------------------------------------------------------- gelu_and_mul, activation_clamp
+
+def test_gelu_erf_values_and_odd_identity():
+    """GELU(1) = Phi(1) (the standard normal CDF at 1, 0.8413447460685429);
+    GELU(0) = 0; GELU(z) - GELU(-z) = z for every z (erf is odd); and the
+    values agree with Python's math.erf, a second implementation of erf."""
+    assert O.gelu_erf(1.0) == pytest.approx(0.8413447460685429, abs=1e-15)
+    assert O.gelu_erf(0.0) == 0.0
+    z = np.linspace(-8, 8, 1601)
+    np.testing.assert_allclose(O.gelu_erf(z) - O.gelu_erf(-z), z, rtol=0, atol=1e-13)
+    ref = np.array([0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0))) for v in z])
+    np.testing.assert_allclose(O.gelu_erf(z), ref, rtol=1e-14, atol=1e-15)
+
+
+def test_gelu_and_mul_expert_matches_torch():
+    """expert_mlp with the gelu activation against torch's exact GELU."""
+    rng = np.random.default_rng(41)
+    K, N = 24, 40
+    x = rng.standard_normal((9, K))
+    w1, w2 = _tiny_weights(rng, 1, K, N)
+    xt = torch.from_numpy(x)
+    g = xt @ torch.from_numpy(w1[0][:N]).T
+    u = xt @ torch.from_numpy(w1[0][N:]).T
+    want = (torch.nn.functional.gelu(g, approximate="none") * u) @ torch.from_numpy(w2[0]).T
+    np.testing.assert_allclose(O.expert_mlp(x, w1[0], w2[0], "gelu"), want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu"])
+def test_activation_clamp(act):
+    """The clamp bounds the gate from above and up to [-c, c] (torch.clamp as
+    the second implementation); a clamp above every value changes nothing."""
+    rng = np.random.default_rng(43)
+    K, N, c = 16, 24, 0.75
+    x = 3.0 * rng.standard_normal((11, K))
+    w1, w2 = _tiny_weights(rng, 1, K, N)
+    xt = torch.from_numpy(x)
+    g = torch.clamp(xt @ torch.from_numpy(w1[0][:N]).T, max=c)
+    u = torch.clamp(xt @ torch.from_numpy(w1[0][N:]).T, min=-c, max=c)
+    f = torch.nn.functional.silu if act == "silu" else (lambda v: torch.nn.functional.gelu(v, approximate="none"))
+    want = (f(g) * u) @ torch.from_numpy(w2[0]).T
+    got = O.expert_mlp(x, w1[0], w2[0], act, clamp=c)
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.abs(got - O.expert_mlp(x, w1[0], w2[0], act)).max() > 1e-3       # the clamp is active here
+    np.testing.assert_array_equal(O.expert_mlp(x, w1[0], w2[0], act, clamp=1e9),
+                                  O.expert_mlp(x, w1[0], w2[0], act))
+
+
+# ---------------------------------------------------------------- BatchedExperts format
+
+def test_experts_batched_equals_grouped():
+    """The batched layout computes, row for row, what the grouped experts()
+    computes on the same tokens in the permuted (expert-major) layout; rows
+    past each expert's count are zero."""
+    rng = np.random.default_rng(47)
+    E, T, K, N = 5, 7, 16, 24
+    counts = np.array([3, 0, 7, 1, 5])
+    w1, w2 = _tiny_weights(rng, E, K, N)
+    xb = rng.standard_normal((E, T, K))
+    yb = O.experts_batched(xb, counts, w1, w2, "gelu", clamp=2.0)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = np.concatenate([xb[e, :counts[e]] for e in range(E)])
+    inverse = np.arange(rows.shape[0], dtype=np.int32)               # top_k = 1: token p is row p
+    g = O.experts(rows, w1, w2, offsets, inverse, 1, "gelu", clamp=2.0)
+    for e in range(E):
+        np.testing.assert_array_equal(yb[e, :counts[e]], g[offsets[e]:offsets[e + 1]])
+        assert not yb[e, counts[e]:].any()
+
+
+# ---------------------------------------------------------------- residual add + RMSNorm
+
+def test_rmsnorm_worked_example():
+    """x = [1, 2, 3, 4], no residual, gamma = 1, eps = 0: the RMS is
+    sqrt(30/4) = sqrt(7.5), so y = x / 2.7386127875258306."""
+    r, y = O.add_rmsnorm(np.array([[1.0, 2.0, 3.0, 4.0]]), np.zeros((1, 4)), np.ones(4), 0.0)
+    np.testing.assert_array_equal(r, [[1.0, 2.0, 3.0, 4.0]])
+    np.testing.assert_allclose(y, [[0.3651483716701107, 0.7302967433402214, 1.0954451150103321,
+                                    1.4605934866804429]], rtol=1e-15)
+
+
+def test_rmsnorm_invariants():
+    """With gamma = 1 and eps = 0 every row of y has mean square 1; y does not
+    change when x and the residual are scaled by the same c > 0; gamma scales
+    y column by column; eps > 0 only shrinks the row norm."""
+    rng = np.random.default_rng(53)
+    x, res = rng.standard_normal((6, 32)), rng.standard_normal((6, 32))
+    gamma = rng.uniform(0.5, 2.0, 32)
+    r, y = O.add_rmsnorm(x, res, np.ones(32), 0.0)
+    np.testing.assert_allclose(r, x + res, rtol=0, atol=0)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(O.add_rmsnorm(3.5 * x, 3.5 * res, np.ones(32), 0.0)[1], y, rtol=1e-13)
+    np.testing.assert_allclose(O.add_rmsnorm(x, res, gamma, 0.0)[1], y * gamma, rtol=1e-14)
+    assert np.all(np.mean(O.add_rmsnorm(x, res, np.ones(32), 1e-2)[1] ** 2, axis=1) < 1.0)
+
+
+def test_finalize_add_rmsnorm_composition():
+    """finalize_add_rmsnorm = add_rmsnorm(finalize(...)): masked routes add
+    nothing (a NaN behind them does not leak), the shared output is added after
+    the routed scale, and the normalised rows have unit mean square."""
+    rng = np.random.default_rng(59)
+    M, k, K, R = 5, 2, 16, 10
+    g2 = rng.standard_normal((R, K))
+    w = rng.uniform(0.1, 1.0, (M, k))
+    pmap = rng.permutation(R)[:M * k].reshape(M, k).astype(np.int32)
+    pmap[1, 1] = -1
+    w[1, 1] = np.nan
+    shared, res = rng.standard_normal((M, K)), rng.standard_normal((M, K))
+    r, y = O.finalize_add_rmsnorm(g2, w, pmap, res, np.ones(K), 0.0, shared, 2.5)
+    assert np.isfinite(r).all() and np.isfinite(y).all()
+    for t in range(M):
+        want = shared[t] + res[t] + 2.5 * sum(w[t, j] * g2[pmap[t, j]] for j in range(k) if pmap[t, j] >= 0)
+        np.testing.assert_allclose(r[t], want, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)
