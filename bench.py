@@ -373,6 +373,88 @@ def other_config(moe, name, args, pk, dev, stream):
     return out
 
 
+def _median_time(fn, stream, scrub, reps=20):
+    """Median CUDA-event time of fn() on `stream`, each call after an L2 scrub."""
+    ts = []
+    for _ in range(reps):
+        scrub()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return statistics.median(ts)
+
+
+def next_rows(moe, pk, dev, stream):
+    """The rows built beyond the core path, each timed on its own at a full
+    size and set against its roofline: the finalize folded into the next
+    layer's residual add + RMSNorm (HBM-bound: k rows of gemm2_permuted, the
+    residual read and written, y written, all f32)."""
+    out = {}
+    buf = torch.zeros(256 << 20, dtype=torch.float32, device=dev)
+    scrub = lambda: l2_scrub(buf)
+    F = moe.MOE_DTYPE_F32
+    rows = []
+    for name in ("mixtral", "qwen3"):
+        cfg = synth.CONFIGS[name]
+        M, k, K = 8192, cfg.top_k, cfg.K
+        g = torch.Generator(device=dev).manual_seed(11)
+        g2 = torch.randn(M * k, K, generator=g, device=dev)
+        w = torch.rand(M, k, generator=g, device=dev)
+        pmap = torch.randperm(M * k, generator=g, device=dev).to(torch.int32).reshape(M, k)
+        res = torch.randn(M, K, generator=g, device=dev)
+        gamma = torch.rand(K, generator=g, device=dev) + 0.5
+        y = torch.empty(M, K, device=dev)
+        call = lambda: moe.moe_finalize_add_rmsnorm(g2, F, M * k, w, F, pmap, M, k, K, None, F, 1.0, res, F, gamma,
+                                                    F, 1e-6, y, F)
+        call()
+        torch.cuda.synchronize()
+        t = _median_time(call, stream, scrub)
+        nbytes = M * k * K * 4 + M * k * 8 + M * K * 12 + K * 4
+        rows.append({"workload": f"{name}-shaped, M={M}, top_k={k}, K={K}, f32", "ms": t * 1e3,
+                     "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
+                     "frac": nbytes / t / 1e9 / pk["hbm"], "bound": "hbm"})
+        del g2, w, pmap, res, gamma, y
+    out["finalize_add_rmsnorm"] = rows
+
+    # gelu_and_mul + activation_clamp in GEMM1's epilogue: the experts step
+    # (tensor-bound) on the Mixtral-shaped layer, beside the same step with SiLU
+    cfg = synth.CONFIGS["mixtral"]
+    M = 4096
+    li = synth.make_layer(cfg, dev)
+    x, logits = synth.make_tokens(cfg, M, dev, li)
+    batches = {M: (x, logits)}
+    act_rows = []
+    for act, clamp in (("silu", None), ("gelu", 1.0)):
+        layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2, activation=act,
+                             activation_clamp=clamp)
+        fwd = make_forward(moe, cfg, layer, batches, stream, "fused")
+        for _ in range(3):
+            fwd(M)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(20):
+            scrub()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fwd(M, (e0, e1))
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(ts)
+        flops = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+        act_rows.append({"workload": f"mixtral-shaped experts step, M={M}, {act}_and_mul"
+                                     + (f", clamp {clamp}" if clamp else ""),
+                         "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16_sus"],
+                         "bound": "tensor"})
+        del layer
+    out["activation"] = act_rows
+    del li, x, logits, batches
+    del buf
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import mixture_experts_layer_15_gb300 as moe
     rank, world = dist_init(args.gpus)
@@ -431,6 +513,7 @@ def run_gpu(args):
             torch.cuda.empty_cache()
             line["other_configs"] = {name: other_config(moe, name, args, pk, dev, stream)
                                      for name in args.others.split(",") if name and name != args.config}
+            line["next_rows"] = next_rows(moe, pk, dev, stream)
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

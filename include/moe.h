@@ -103,7 +103,17 @@ typedef struct moe_weights {
     const uint8_t* w1_scale;   /* MXFP4 only, else NULL */
     const void* w2;
     const uint8_t* w2_scale;   /* MXFP4 only, else NULL */
+    /* GEMM1's activation (FusedMoEPermuteExpertsUnpermute.activation):
+     * MOE_ACT_SILU (0, silu_and_mul) or MOE_ACT_GELU (1, gelu_and_mul, exact
+     * erf GELU), on the gate (rows 0..N-1 of W1) times the up projection. */
+    int activation;
+    /* activation_clamp (flashinfer_moe_ep.py, build_fi_mega_config): c > 0
+     * clamps the gate to at most c and the up projection to [-c, c] before
+     * the activation; 0 (or less) means no clamp. */
+    float activation_clamp;
 } moe_weights;
+
+enum { MOE_ACT_SILU = 0, MOE_ACT_GELU = 1 };
 
 /* ------------------------------------------------------------------------
  * moe_route -- the [Router] step (modular_kernel.py module header; its
@@ -220,6 +230,32 @@ moe_status moe_permute_noalloc(const int32_t* topk_ids, int M, int top_k, int E,
                                const void* x, int K,
                                int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
                                int32_t* permuted_to_expanded, void* x_perm, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_finalize_add_rmsnorm -- moe_finalize folded into its consumer, the next
+ * layer's residual add + RMSNorm (moe_output.py, MoEOutput: the consumer of an
+ * open reduction, typically the next layer's RMSNorm, can take the top-k
+ * reduction of an unfinalized routed output into the same kernel):
+ *
+ *   r[t]        = rsf * sum_j w[t,j] * gemm2_permuted[map[t,j]] + shared[t] + residual[t]
+ *   residual[t] <- r[t]
+ *   y[t]        = r[t] / sqrt(mean over K of r[t]^2 + eps) * gamma
+ *
+ *   gemm2_permuted .. routed_scaling_factor: as in moe_finalize.
+ *   residual   [M, K] in residual_dtype, read and overwritten with r (the
+ *              accumulation is f32; y is computed from the unrounded r).
+ *   gamma      [K] in gamma_dtype; eps >= 0 (MOE_ERR_INVALID_ARG otherwise).
+ *   y          [M, K] in y_dtype.
+ * K must be a multiple of 8 (MOE_ERR_ALIGNMENT) and at most 16384
+ * (MOE_ERR_UNSUPPORTED). y and residual may not alias each other or an input.
+ * ---------------------------------------------------------------------- */
+moe_status moe_finalize_add_rmsnorm(const void* gemm2_permuted, moe_dtype gemm2_dtype, int num_permuted_rows,
+                                    const void* expert_weights, moe_dtype weights_dtype,
+                                    const int32_t* expanded_idx_to_permuted_idx, int M, int top_k, int K,
+                                    const void* shared_out, moe_dtype shared_dtype, float routed_scaling_factor,
+                                    void* residual, moe_dtype residual_dtype, const void* gamma,
+                                    moe_dtype gamma_dtype, float eps, void* y, moe_dtype y_dtype,
+                                    cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_experts -- the experts: GEMM1, silu_and_mul, GEMM2, per local expert on

@@ -29,12 +29,15 @@ MOE_ROUTE_SOFTMAX_TOPK = 0
 MOE_ROUTE_SIGMOID_GROUPED_TOPK = 1
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_MXFP4 = 1
+MOE_ACT_SILU = 0
+MOE_ACT_GELU = 1
 
 #: every function the header declares (checked against include/moe.h by the tests)
 EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
-    "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize", "moe_shared_expert_workspace_size",
+    "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize",
+    "moe_finalize_add_rmsnorm", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid",
@@ -57,6 +60,8 @@ class moe_weights(ctypes.Structure):
         ("w1_scale", ctypes.c_void_p),
         ("w2", ctypes.c_void_p),
         ("w2_scale", ctypes.c_void_p),
+        ("activation", ctypes.c_int),
+        ("activation_clamp", ctypes.c_float),
     ]
 
 
@@ -84,6 +89,8 @@ _SIGS = {
                                     _P, _Z, _P], _I),
     "moe_experts_launches": ([ctypes.POINTER(moe_weights), _I, _I, _I], _I),
     "moe_finalize": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P], _I),
+    "moe_finalize_add_rmsnorm": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P, _I, _F, _P, _I, _P],
+                                 _I),
     "moe_shared_expert_workspace_size": ([_I, _I, _I], _Z),
     "moe_shared_expert": ([_P, _P, _I, _I, _P, _I, _P, _I, _P, _Z, _P], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
@@ -128,9 +135,10 @@ def status_string(status: int) -> str:
     return lib.moe_status_string(int(status)).decode()
 
 
-def make_weights(fmt, E_local, K, N, w1, w2, w1_scale=None, w2_scale=None) -> moe_weights:
+def make_weights(fmt, E_local, K, N, w1, w2, w1_scale=None, w2_scale=None, activation=0,
+                 activation_clamp=None) -> moe_weights:
     return moe_weights(int(fmt), int(E_local), int(K), int(N), _ptr(w1), _ptr(w1_scale), _ptr(w2),
-                       _ptr(w2_scale))
+                       _ptr(w2_scale), int(activation), float(activation_clamp or 0.0))
 
 
 def moe_route(logits, M, E, top_k, method, score_bias, n_group, topk_group, routed_scaling_factor,
@@ -198,6 +206,16 @@ def moe_experts_fused_finalize(weights: moe_weights, x_perm, expert_offsets, M, 
         ctypes.byref(weights), _ptr(x_perm), _ptr(expert_offsets), M, top_k, _ptr(expert_weights), weights_dtype,
         _ptr(permuted_to_expanded), _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def moe_finalize_add_rmsnorm(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights, weights_dtype,
+                             expanded_idx_to_permuted_idx, M, top_k, K, shared_out, shared_dtype,
+                             routed_scaling_factor, residual, residual_dtype, gamma, gamma_dtype, eps, y, y_dtype,
+                             stream=None):
+    _check("moe_finalize_add_rmsnorm", lib.moe_finalize_add_rmsnorm(
+        _ptr(gemm2_permuted), gemm2_dtype, num_permuted_rows, _ptr(expert_weights), weights_dtype,
+        _ptr(expanded_idx_to_permuted_idx), M, top_k, K, _ptr(shared_out), shared_dtype, routed_scaling_factor,
+        _ptr(residual), residual_dtype, _ptr(gamma), gamma_dtype, eps, _ptr(y), y_dtype, _stream(stream)))
 
 
 def moe_experts_launches(weights: moe_weights, M, top_k, fused_finalize) -> int:

@@ -258,6 +258,8 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a1.counters = counters;
     a1.max_tiles = L.g1.max_tiles;
     a1.err = err;
+    a1.act = w->activation;
+    a1.clamp = w->activation_clamp;
     GemmArgs& a2 = ka.g[1];
     a2 = a1;
     a2.kr = N;

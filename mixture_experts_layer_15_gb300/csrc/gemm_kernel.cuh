@@ -111,6 +111,10 @@ struct GemmArgs {
     int* counters;
     int max_tiles;
     int* err;
+    // MODE_SWIGLU: the activation (MOE_ACT_SILU / MOE_ACT_GELU) and the clamp
+    // (<= 0: none) applied to the gate and up values
+    int act;
+    float clamp;
     // MODE_FINAL only
     const int32_t* inverse;   // permuted_to_expanded [rows]
     const void* fw;           // routing weights [rows] (expanded order)
@@ -249,6 +253,18 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// GEMM1's activation on a (gate, up) pair: silu_and_mul or gelu_and_mul (exact
+// GELU, g/2 * (1 + erf(g / sqrt 2))), after the optional clamp: the gate to at
+// most c, up to [-c, c].
+__device__ __forceinline__ float act_mul(float g, float u, int act, float clamp) {
+    if (clamp > 0.0f) {
+        g = fminf(g, clamp);
+        u = fminf(fmaxf(u, -clamp), clamp);
+    }
+    if (act == MOE_ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+    return silu_mul(g, u);
+}
+
 template <typename OutT>
 __device__ __forceinline__ void store_out(OutT* p, float v);
 template <>
@@ -269,7 +285,7 @@ __device__ __forceinline__ void emit16(const Unit& un, const GemmArgs& a, int ro
         if (r < un.row_end) {
             const size_t rb = static_cast<size_t>(r) * a.out_ld;
             if (MODE == MODE_SWIGLU) {
-                store_out<OutT>(out + rb + un.wt * kBM + row_in_tile, silu_mul(v0[i], v1[i]));
+                store_out<OutT>(out + rb + un.wt * kBM + row_in_tile, act_mul(v0[i], v1[i], a.act, a.clamp));
             } else {
                 const int col = un.wt * a.wtile_rows + row_in_tile;
                 store_out<OutT>(out + rb + col, v0[i]);

@@ -272,7 +272,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                             const int r = un.row0 + c0 + i;
                             if (r < un.row_end)
                                 act[static_cast<size_t>(r) * a.out_ld + col] =
-                                    __float2bfloat16_rn(silu_mul(v[i], xg[i * 64 + l64]));
+                                    __float2bfloat16_rn(act_mul(v[i], xg[i * 64 + l64], a.act, a.clamp));
                         }
                     }
                     named_bar_sync(2 + grp, 128);             // the exchange buffer is free again

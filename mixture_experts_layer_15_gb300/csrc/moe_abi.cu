@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "moe_internal.h"
+#include <math.h>
 
 namespace moe {
 
@@ -84,6 +85,8 @@ moe_status check_weights(const moe_weights* w) {
     if (w == nullptr || w->w1 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
     if (w->E_local < 1 || w->E_local > 1024 || w->K <= 0 || w->N <= 0) return MOE_ERR_INVALID_ARG;
     if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (w->activation != MOE_ACT_SILU && w->activation != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
+    if (!(w->activation_clamp == w->activation_clamp) || w->activation_clamp == INFINITY) return MOE_ERR_INVALID_ARG;
     if (w->K % 128 != 0 || w->N % 128 != 0) return MOE_ERR_ALIGNMENT;
     if (!aligned16(w->w1) || !aligned16(w->w2)) return MOE_ERR_ALIGNMENT;
     if (w->format == MOE_WEIGHTS_MXFP4) {
@@ -323,6 +326,43 @@ moe_status moe_finalize(const void* gemm2_permuted, moe_dtype gemm2_dtype, int n
     return from_cuda(moe::launch_finalize(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights,
                                           weights_dtype, expanded_idx_to_permuted_idx, M, top_k, K, shared_out,
                                           shared_dtype, routed_scaling_factor, out, out_dtype, err, stream));
+}
+
+moe_status moe_finalize_add_rmsnorm(const void* gemm2_permuted, moe_dtype gemm2_dtype, int num_permuted_rows,
+                                    const void* expert_weights, moe_dtype weights_dtype,
+                                    const int32_t* expanded_idx_to_permuted_idx, int M, int top_k, int K,
+                                    const void* shared_out, moe_dtype shared_dtype, float routed_scaling_factor,
+                                    void* residual, moe_dtype residual_dtype, const void* gamma,
+                                    moe_dtype gamma_dtype, float eps, void* y, moe_dtype y_dtype,
+                                    cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    if (K <= 0 || num_permuted_rows < 0 || !valid_dtype(gemm2_dtype)) return MOE_ERR_INVALID_ARG;
+    if (!valid_dtype(residual_dtype) || !valid_dtype(gamma_dtype) || !valid_dtype(y_dtype)) return MOE_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps == INFINITY) return MOE_ERR_INVALID_ARG;
+    if (M == 0) return MOE_OK;
+    if (K % 8 != 0) return MOE_ERR_ALIGNMENT;
+    if (K > 16384) return MOE_ERR_UNSUPPORTED;
+    const moe_status a = check_finalize_args(expert_weights, weights_dtype, expanded_idx_to_permuted_idx,
+                                             shared_out, shared_dtype, y, y_dtype);
+    if (a != MOE_OK) return a;
+    if (residual == nullptr || gamma == nullptr) return MOE_ERR_INVALID_ARG;
+    if (num_permuted_rows > 0 && gemm2_permuted == nullptr) return MOE_ERR_INVALID_ARG;
+    if ((gemm2_permuted != nullptr && !aligned16(gemm2_permuted)) || !aligned16(residual) || !aligned16(gamma))
+        return MOE_ERR_ALIGNMENT;
+    // y and the residual are written; neither may alias an input or each other
+    const void* ins[4] = {gemm2_permuted, shared_out, expert_weights, gamma};
+    for (const void* q : ins)
+        if (q != nullptr && (q == y || q == residual)) return MOE_ERR_INVALID_ARG;
+    if (y == residual) return MOE_ERR_INVALID_ARG;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_finalize_rmsnorm(gemm2_permuted, gemm2_dtype, num_permuted_rows, expert_weights,
+                                                  weights_dtype, expanded_idx_to_permuted_idx, M, top_k, K,
+                                                  shared_out, shared_dtype, routed_scaling_factor, residual,
+                                                  residual_dtype, gamma, gamma_dtype, eps, y, y_dtype, err, stream));
 }
 
 moe_status moe_experts(const moe_weights* w, const void* x_perm, const int32_t* expert_offsets, int M,

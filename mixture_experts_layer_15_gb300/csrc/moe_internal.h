@@ -53,6 +53,12 @@ cudaError_t launch_finalize(const void* gemm2, int gemm2_dtype, int num_rows,
                             const void* weights, int weights_dtype, const int32_t* map,
                             int M, int top_k, int K, const void* shared, int shared_dtype,
                             float rsf, void* out, int out_dtype, int* err, cudaStream_t stream);
+// Finalize + residual add + RMSNorm (finalize_rmsnorm.cu); K % 8 == 0, K <= 16384.
+cudaError_t launch_finalize_rmsnorm(const void* gemm2, int gemm2_dtype, int num_rows, const void* weights,
+                                    int weights_dtype, const int32_t* map, int M, int top_k, int K,
+                                    const void* shared, int shared_dtype, float rsf, void* residual,
+                                    int residual_dtype, const void* gamma, int gamma_dtype, float eps, void* y,
+                                    int y_dtype, int* err, cudaStream_t stream);
 // out[M, K] f32 = shared (shared_dtype) or 0, the start of the fused finalize.
 cudaError_t launch_out_init(const void* shared, int shared_dtype, int M, int K, float* out, const DeviceInfo& dev,
                             cudaStream_t stream);

@@ -51,7 +51,7 @@ class MoELayer:
                  fmt=L.MOE_WEIGHTS_BF16, route="softmax", score_bias=None, n_group=1, topk_group=1,
                  routed_scaling_factor=1.0, expert_map=None, E_local=None, ws1=None, ws2=None,
                  weights_dtype=L.MOE_DTYPE_F32, gemm2_dtype=L.MOE_DTYPE_F32,
-                 out_dtype=L.MOE_DTYPE_F32, fused_finalize=False):
+                 out_dtype=L.MOE_DTYPE_F32, fused_finalize=False, activation="silu", activation_clamp=None):
         self.K, self.N, self.E, self.top_k = K, N, E, top_k
         self.E_local = E if E_local is None else E_local
         self.w1, self.w2, self.w1_scale, self.w2_scale = w1, w2, w1_scale, w2_scale
@@ -68,7 +68,8 @@ class MoELayer:
         if fused_finalize and out_dtype != L.MOE_DTYPE_F32:
             raise ValueError("fused_finalize accumulates into an f32 output")
         self.fused_finalize = bool(fused_finalize)
-        self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale)
+        act = {"silu": L.MOE_ACT_SILU, "gelu": L.MOE_ACT_GELU}[activation]
+        self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale, act, activation_clamp)
         self._bufs = {}
 
     def buffers(self, M: int) -> Buffers:

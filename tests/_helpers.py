@@ -56,7 +56,8 @@ class ExpertsF64:
         return s if self.scale is None else s[:-1] + (s[-1] * 2,)
 
 
-def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None, rsf=1.0):
+def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None, rsf=1.0, activation="silu",
+                  clamp=None):
     """Oracle output rows for ``tokens`` (and the expert output y of each of
     their routes): the experts and finalize of the oracle applied to the
     sub-problem made of those tokens' routes.
@@ -79,7 +80,7 @@ def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None,
     ys = {}
     for le, routes in by_expert.items():
         xt = x[[tokens[a] for a, _ in routes]]
-        y = O.expert_mlp(xt, w1[le], w2[le])
+        y = O.expert_mlp(xt, w1[le], w2[le], activation, clamp)
         for r, (a, j) in enumerate(routes):
             ys[(a, j)] = y[r]
     # sub-problem gemm2 rows and map, then the oracle's finalize

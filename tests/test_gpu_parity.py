@@ -246,7 +246,8 @@ def test_route_permute_matches_two_calls(moe, name, M, masked):
 
 # ------------------------------------------------------------------ whole layer
 
-def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False):
+def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False,
+                 activation="silu", clamp=None):
     cfg = synth.CONFIGS[name]
     li = layer_inputs(name)
     x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
@@ -263,6 +264,8 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
         kw.update(weights_dtype=moe.MOE_DTYPE_BF16, gemm2_dtype=moe.MOE_DTYPE_BF16, out_dtype=moe.MOE_DTYPE_BF16)
     if fused_finalize:
         kw.update(fused_finalize=True)
+    if activation != "silu" or clamp is not None:
+        kw.update(activation=activation, activation_clamp=clamp)
     layer = make_layer(moe, name, li, **kw)
     b = layer.forward(x, logits)
     torch.cuda.synchronize()
@@ -292,7 +295,7 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
     if li.ws1 is not None:
         shared = np.zeros((M, cfg.K))
         shared[toks] = O.shared_expert(xs[toks], li.ws1.double().cpu().numpy(), li.ws2.double().cpu().numpy())
-    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared)
+    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared, activation=activation, clamp=clamp)
     got = b.out.double().cpu().numpy()[toks]
     g2 = b.gemm2.double().cpu().numpy()
     rel = 3e-2 if cfg.weight_format == "mxfp4" else 1e-2
