@@ -449,6 +449,23 @@ def next_rows(moe, pk, dev, stream):
                          "bound": "tensor"})
         del layer
     out["activation"] = act_rows
+
+    # the BatchedExperts layout: [E, max_tokens, K] with every block full
+    T = 512
+    w = moe.make_weights(moe.MOE_WEIGHTS_BF16, cfg.E, cfg.K, cfg.N, li.w1, li.w2)
+    xb = torch.randn(cfg.E, T, cfg.K, device=dev).to(torch.bfloat16)
+    counts = torch.full((cfg.E,), T, dtype=torch.int32, device=dev)
+    yb = torch.empty(cfg.E, T, cfg.K, device=dev)
+    wsb = torch.zeros(max(moe.moe_experts_batched_workspace_size(w, T), 16), dtype=torch.uint8, device=dev)
+    call = lambda: moe.moe_experts_batched(w, xb, counts, T, yb, moe.MOE_DTYPE_F32, wsb, wsb.numel())
+    call()
+    torch.cuda.synchronize()
+    t = _median_time(call, stream, scrub)
+    flops = 6.0 * cfg.K * cfg.N * cfg.E * T
+    out["batched_experts"] = [{"workload": f"mixtral-shaped, E={cfg.E}, max_tokens={T}, all blocks full, f32 out",
+                               "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16_sus"],
+                               "bound": "tensor"}]
+    del xb, counts, yb, wsb
     del li, x, logits, batches
     del buf
     torch.cuda.empty_cache()

@@ -345,6 +345,31 @@ moe_status moe_experts_fused_finalize(const moe_weights* w,
 int moe_experts_launches(const moe_weights* w, int M, int top_k, int fused_finalize);
 
 /* ------------------------------------------------------------------------
+ * moe_experts_batched -- the experts on the BatchedExperts activation format
+ * (modular_kernel.py, FusedMoEActivationFormat: [num experts, max tokens per
+ * expert, hidden], with expert_num_tokens, the per-expert counts that
+ * FusedMoEPermuteExpertsUnpermute.apply receives in that format). The
+ * fixed-shape layout suits graph capture and batched dispatchers.
+ *
+ *   x                  bf16 [E_local, max_tokens, K]; expert e's tokens are
+ *                      rows 0 .. expert_num_tokens[e]-1 of block e.
+ *   expert_num_tokens  i32 [E_local] on the device; a count outside
+ *                      [0, max_tokens] sets MOE_ERR_DEVICE_INDEX and is
+ *                      clamped.
+ *   y                  [E_local, max_tokens, K] in y_dtype: row r of block e is
+ *                      W2[e] . act(W1[e] x[e, r]) for r < count_e (unweighted);
+ *                      rows past the count are not written.
+ *   workspace          at least moe_experts_batched_workspace_size() bytes,
+ *                      zero-filled before first use (as for moe_experts).
+ * The activation and clamp of `w` apply. GEMM1 and GEMM2 run as two launches.
+ * ---------------------------------------------------------------------- */
+size_t moe_experts_batched_workspace_size(const moe_weights* w, int max_tokens);
+
+moe_status moe_experts_batched(const moe_weights* w, const void* x, const int32_t* expert_num_tokens,
+                               int max_tokens, void* y, moe_dtype y_dtype, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_finalize -- apply the routing weights and reduce over top_k
  * (modular_kernel.py, FusedMoEPrepareAndFinalize.finalize), then the routed
  * scale and the shared-expert add (moe_output.py, MoEOutput: the shared

@@ -37,7 +37,7 @@ EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
     "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize",
-    "moe_finalize_add_rmsnorm", "moe_shared_expert_workspace_size",
+    "moe_finalize_add_rmsnorm", "moe_experts_batched_workspace_size", "moe_experts_batched", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid",
@@ -88,6 +88,8 @@ _SIGS = {
     "moe_experts_fused_finalize": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
                                     _P, _Z, _P], _I),
     "moe_experts_launches": ([ctypes.POINTER(moe_weights), _I, _I, _I], _I),
+    "moe_experts_batched_workspace_size": ([ctypes.POINTER(moe_weights), _I], _Z),
+    "moe_experts_batched": ([ctypes.POINTER(moe_weights), _P, _P, _I, _P, _I, _P, _Z, _P], _I),
     "moe_finalize": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P], _I),
     "moe_finalize_add_rmsnorm": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P, _I, _F, _P, _I, _P],
                                  _I),
@@ -216,6 +218,17 @@ def moe_finalize_add_rmsnorm(gemm2_permuted, gemm2_dtype, num_permuted_rows, exp
         _ptr(gemm2_permuted), gemm2_dtype, num_permuted_rows, _ptr(expert_weights), weights_dtype,
         _ptr(expanded_idx_to_permuted_idx), M, top_k, K, _ptr(shared_out), shared_dtype, routed_scaling_factor,
         _ptr(residual), residual_dtype, _ptr(gamma), gamma_dtype, eps, _ptr(y), y_dtype, _stream(stream)))
+
+
+def moe_experts_batched_workspace_size(weights: moe_weights, max_tokens) -> int:
+    return int(lib.moe_experts_batched_workspace_size(ctypes.byref(weights), max_tokens))
+
+
+def moe_experts_batched(weights: moe_weights, x, expert_num_tokens, max_tokens, y, y_dtype, workspace,
+                        workspace_bytes, stream=None):
+    _check("moe_experts_batched", lib.moe_experts_batched(
+        ctypes.byref(weights), _ptr(x), _ptr(expert_num_tokens), max_tokens, _ptr(y), y_dtype, _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
 
 
 def moe_experts_launches(weights: moe_weights, M, top_k, fused_finalize) -> int:

@@ -125,7 +125,9 @@ struct Layout {
 };
 
 // fin: GEMM2 finalizes in its epilogue (needs no more workspace than without)
-Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin = false) {
+// batched: the BatchedExperts layout, which runs as two one-CTA launches
+Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin = false,
+                   bool batched = false) {
     Layout L;
     const int K = w->K, N = w->N;
     L.bt = g_override.token_tile > 0 ? g_override.token_tile
@@ -138,7 +140,7 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     // token-tile counters fit their region
     L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
     L.fused = L.g2.na == 2 && L.max_token_tiles <= kMaxSplitTiles && g_override.fuse != 2 &&
-              g_override.fuse != 3;
+              g_override.fuse != 3 && !batched;
     // GEMM1 and GEMM2 on CTA pairs (two launches): bf16 weights, 128- or
     // 256-token tiles, every unit whole (no split-K), 256-row GEMM2 units.
     // Forced by the override (fuse = 3, with its tile width); chosen
@@ -147,7 +149,7 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     // choice does not depend on `fin`, so the workspace query and the launch
     // agree on the layout.
     const bool pair_ok = w->format == MOE_WEIGHTS_BF16 && K % 256 == 0 && N % kBM == 0 &&
-                         g_override.gemm2_na != 1;
+                         g_override.gemm2_na != 1 && !batched;
     L.pair = false;
     if (pair_ok && g_override.fuse == 3 && (L.bt == 128 || L.bt == 256) && L.g1.splits == 1 && L.g2.na == 2 &&
         plan_gemm(1, L.bt, 2, K / (2 * kBM), N, rows_alloc, groups, sm_count).splits == 1) {
@@ -212,8 +214,8 @@ void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na, i
     g_override.fuse = fuse;
 }
 
-size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev) {
-    return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count).total;
+size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev, bool batched) {
+    return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, false, batched).total;
 }
 
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {
@@ -226,9 +228,10 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     const moe_weights* w = p.w;
     const int K = w->K, N = w->N;
     const bool mx = w->format == MOE_WEIGHTS_MXFP4;
-    const int groups = p.offsets != nullptr ? w->E_local : 1;
+    const int groups = (p.offsets != nullptr || p.counts != nullptr) ? w->E_local : 1;
     const bool fin = p.fin_out != nullptr;
-    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count, fin);
+    const bool batched = p.counts != nullptr;
+    const Layout L = make_layout(w, p.rows_alloc, p.M, groups, dev.sm_count, fin, batched);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* counters = reinterpret_cast<int*>(ws);
     void* act = ws + L.off_act;
@@ -260,6 +263,8 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a1.err = err;
     a1.act = w->activation;
     a1.clamp = w->activation_clamp;
+    a1.counts = p.counts;
+    a1.batch_stride = p.batch_stride;
     GemmArgs& a2 = ka.g[1];
     a2 = a1;
     a2.kr = N;

@@ -96,6 +96,10 @@ enum { MODE_SWIGLU = 0, MODE_PLAIN = 1, MODE_FINAL = 2 };
 
 struct GemmArgs {
     const int32_t* offsets;   // [groups+1] or nullptr
+    // BatchedExperts layout (non-fused one-CTA launches): group g's rows are
+    // g*batch_stride .. + counts[g] - 1 (counts on the device), instead of offsets
+    const int32_t* counts;
+    int batch_stride;
     int single_rows;          // rows of the single group when offsets == nullptr
     int groups;
     int rows_alloc;           // rows allocated in the B operand and the output
@@ -178,7 +182,8 @@ struct Unit {
     int g, wt, s, row0, row_end, kb0, kb1, tile, ncols;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* offs, int BT,
+// Group g's rows are [offs[g], ends[g]) (ends = offs + 1 for packed groups).
+__device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* offs, const int* ends, int BT,
                                             const GemmArgs& a) {
     int lo = 0, hi = a.groups;                 // prefix[lo] <= u < prefix[hi]
     while (hi - lo > 1) {
@@ -190,7 +195,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
     int local = u - prefix[lo];
     un.s = local % a.splits;
     local /= a.splits;
-    const int beg = offs[lo], end = offs[lo + 1];
+    const int beg = offs[lo], end = ends[lo];
     const int ntt = (end - beg + BT - 1) / BT;
     const int tt = local % ntt;
     un.wt = local / ntt;
@@ -466,14 +471,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     pdl_wait();
     pdl_trigger();
     // group offsets (validated: non-decreasing, within the allocation)
+    const bool batched = !FUSED && a0.counts != nullptr;
     for (int g = tid; g <= groups; g += C::THREADS) {
-        int v = a0.offsets != nullptr ? __ldg(a0.offsets + g) : (g == 0 ? 0 : a0.single_rows);
+        int v = batched ? g * a0.batch_stride
+                        : (a0.offsets != nullptr ? __ldg(a0.offsets + g) : (g == 0 ? 0 : a0.single_rows));
         if (v < 0 || v > a0.rows_alloc) { set_error(a0.err, MOE_ERR_DEVICE_INDEX); v = v < 0 ? 0 : a0.rows_alloc; }
         offs[g] = v;
     }
     __syncthreads();
     for (int g = tid; g < groups; g += C::THREADS) {
-        int cnt = offs[g + 1] - offs[g];
+        int cnt;
+        if (batched) {
+            // batched rows: the group's count, at most its block (ttp holds the ends)
+            cnt = __ldg(a0.counts + g);
+            if (cnt < 0 || cnt > a0.batch_stride) {
+                set_error(a0.err, MOE_ERR_DEVICE_INDEX);
+                cnt = cnt < 0 ? 0 : a0.batch_stride;
+            }
+            ttp[g] = offs[g] + cnt;
+        } else {
+            cnt = offs[g + 1] - offs[g];
+        }
         if (cnt < 0) { set_error(a0.err, MOE_ERR_DEVICE_INDEX); cnt = 0; }
         const int ntt = (cnt + BT - 1) / BT;
         prefix0[g] = ntt * a0.n_wtiles * a0.splits;
@@ -502,9 +520,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     const uint32_t tmem_base = *tmem_slot;
 
     // unit u -> (phase, decoded unit)
+    const int* ends = batched ? ttp : offs + 1;
     auto unit_at = [&](int u, int& ph) -> Unit {
         ph = (FUSED && u >= units0) ? 1 : 0;
-        return ph ? decode_unit(u - units0, prefix1, offs, BT, ka.g[1]) : decode_unit(u, prefix0, offs, BT, a0);
+        return ph ? decode_unit(u - units0, prefix1, offs, ends, BT, ka.g[1])
+                  : decode_unit(u, prefix0, offs, ends, BT, a0);
     };
     // global index of a unit's token tile (fused launches)
     auto tile_index = [&](const Unit& un) { return ttp[un.g] + (un.row0 - offs[un.g]) / BT; };

@@ -151,7 +151,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t tmem_base = *tmem_slot;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     auto unit_at = [&](int u) {
-        Unit un = decode_unit(u, prefix, offs, BT, a);
+        Unit un = decode_unit(u, prefix, offs, offs + 1, BT, a);
         un.ncols = pair_cols(un, BT);
         return un;
     };

@@ -466,6 +466,48 @@ int moe_experts_launches(const moe_weights* w, int M, int top_k, int fused_final
     return moe::experts_launches(w, M * top_k, M, fused_finalize != 0, info);
 }
 
+size_t moe_experts_batched_workspace_size(const moe_weights* w, int max_tokens) {
+    if (max_tokens <= 0 || check_weights(w) != MOE_OK) return 0;
+    const long long rows = static_cast<long long>(w->E_local) * max_tokens;
+    if (rows >= (1LL << 30)) return 0;
+    DeviceInfo info;
+    if (!moe::current_device_info(&info)) info.sm_count = 152;
+    return moe::experts_workspace_bytes(w, static_cast<int>(rows), max_tokens, info, true);
+}
+
+moe_status moe_experts_batched(const moe_weights* w, const void* x, const int32_t* expert_num_tokens,
+                               int max_tokens, void* y, moe_dtype y_dtype, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    if (max_tokens < 0) return MOE_ERR_INVALID_ARG;
+    const moe_status ws_ok = check_weights(w);
+    if (ws_ok != MOE_OK) return ws_ok;
+    if (!valid_dtype(y_dtype)) return MOE_ERR_INVALID_ARG;
+    const long long rows = static_cast<long long>(w->E_local) * max_tokens;
+    if (rows >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (max_tokens == 0) return MOE_OK;
+    if (x == nullptr || expert_num_tokens == nullptr || y == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
+    if (x == y) return MOE_ERR_INVALID_ARG;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    const size_t need = moe::experts_workspace_bytes(w, static_cast<int>(rows), max_tokens, info, true);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    moe::ExpertsProblem p;
+    p.w = w;
+    p.x = x;
+    p.rows_alloc = static_cast<int>(rows);
+    p.M = max_tokens;
+    p.offsets = nullptr;
+    p.single_rows = 0;
+    p.y = y;
+    p.y_dtype = y_dtype;
+    p.counts = expert_num_tokens;
+    p.batch_stride = max_tokens;
+    return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
+}
+
 size_t moe_shared_expert_workspace_size(int M, int K, int Ns) {
     if (M <= 0 || K <= 0 || Ns <= 0 || K % 128 != 0 || Ns % 128 != 0) return 0;
     moe_weights w{};

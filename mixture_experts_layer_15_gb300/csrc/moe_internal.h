@@ -86,10 +86,15 @@ struct ExpertsProblem {
     int fin_shared_dtype = 0;
     int top_k = 1;
     float rsf = 1.0f;
+    // BatchedExperts layout: group g's rows are g*batch_stride .. + counts[g]-1
+    // (counts on the device); offsets is then unused.
+    const int32_t* counts = nullptr;
+    int batch_stride = 0;
 };
 
 void set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse);
-size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev);
+size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev,
+                               bool batched = false);
 // Kernels one experts call launches (fin: the finalize folded into GEMM2,
 // counting its out initialisation).
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev);

@@ -138,3 +138,48 @@ def test_layer_activation(moe, name, M, act, clamp, fused):
     CTA-pair GEMMs (Qwen3-shaped at M = 8192 runs on pairs), against the
     oracle's expert_mlp with the same activation, at the layer's bar."""
     _check_layer(moe, name, M, activation=act, clamp=clamp, fused_finalize=fused, sample=64 if M > 1000 else None)
+
+
+# ------------------------------------------------------------------ BatchedExperts format
+
+@pytest.mark.parametrize("name,T,act,rows_per_expert", [("tiny", 40, "silu", None), ("tiny", 300, "gelu", None),
+                                                        ("mixtral", 96, "silu", 6)])
+def test_experts_batched(moe, name, T, act, rows_per_expert):
+    """moe_experts_batched on [E, max_tokens, K] with ragged counts (0 and
+    max_tokens included) against the oracle's experts_batched; rows past each
+    count are left as they were."""
+    cfg = synth.CONFIGS[name]
+    li = synth.make_layer(cfg, DEV)
+    E, K = cfg.E, cfg.K
+    g = torch.Generator().manual_seed(T)
+    counts = torch.randint(0, T + 1, (E,), generator=g, dtype=torch.int32)
+    counts[0], counts[-1] = 0, T
+    xb = torch.randn(E, T, K, generator=g).to(torch.bfloat16)
+    w = moe.make_weights(moe.MOE_WEIGHTS_BF16, E, K, cfg.N, li.w1, li.w2,
+                         activation=moe.MOE_ACT_GELU if act == "gelu" else moe.MOE_ACT_SILU)
+    ws = torch.zeros(max(moe.moe_experts_batched_workspace_size(w, T), 16), dtype=torch.uint8, device=DEV)
+    y = torch.full((E, T, K), float("nan"), device=DEV)
+    for _ in range(2):                                                # twice: counters left at zero
+        moe.moe_experts_batched(w, xb.to(DEV), counts.to(DEV), T, y, moe.MOE_DTYPE_F32, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == 0
+    got = y.double().cpu().numpy()
+    w1 = [li.w1[e].double().cpu().numpy() for e in range(E)]
+    w2 = [li.w2[e].double().cpu().numpy() for e in range(E)]
+    xs = xb.double().numpy()
+    refs, gots = [], []
+    for e in range(E):
+        c = int(counts[e])
+        assert np.isnan(got[e, c:]).all()                             # untouched past the count
+        rows = list(range(c)) if rows_per_expert is None else sorted(set(np.linspace(0, c - 1, rows_per_expert,
+                                                                                   dtype=int).tolist()))
+        if c and rows:
+            if rows_per_expert is None:
+                ref = O.experts_batched(xs[e:e + 1], counts[e:e + 1].numpy(), np.stack([w1[e]]), np.stack([w2[e]]),
+                                        act)[0, :c]
+            else:
+                ref = O.expert_mlp(xs[e, rows], w1[e], w2[e], act)
+            refs.append(ref)
+            gots.append(got[e, rows])
+    ref, gv = np.concatenate(refs), np.concatenate(gots)
+    assert max_err(gv, ref) <= tol(ref)
