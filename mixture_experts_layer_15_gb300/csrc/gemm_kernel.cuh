@@ -361,12 +361,25 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t scale2, uint32_t (&
     const uint32_t lo_a = __byte_perm(kE2m1LoLo, kE2m1LoHi, sel_a);
     const uint32_t hi_b = __byte_perm(kE2m1HiLo, kE2m1HiHi, sel_b);
     const uint32_t lo_b = __byte_perm(kE2m1LoLo, kE2m1LoHi, sel_b);
-    // interleave (lo, hi) byte pairs into bf16 halves; OR in the sign bits
-    // (bit 3 of each code -> bit 15 of its bf16)
-    o[0] = __byte_perm(lo_a, hi_a, 0x5140) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-    o[1] = __byte_perm(lo_a, hi_a, 0x7362) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
-    o[2] = __byte_perm(lo_b, hi_b, 0x5140) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
-    o[3] = __byte_perm(lo_b, hi_b, 0x7362) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
+    // Signs: byte j of w holds elements 2j (low nibble, sign bit 3) and 2j+1
+    // (high nibble, sign bit 7); in w4 = w << 4 byte j's top bit is element
+    // 2j's sign. A byte permute in sign-replicate mode (selector bit 3) copies
+    // a byte's top bit over the whole output byte: bytes 1 and 3 of sgn_j get
+    // the signs of elements 2j and 2j+1, which the mask 0x80008000 keeps as
+    // bits 15 and 31 of the bf16 pair.
+    const uint32_t w4 = w << 4;
+    uint32_t mag[4];
+    mag[0] = __byte_perm(lo_a, hi_a, 0x5140);
+    mag[1] = __byte_perm(lo_a, hi_a, 0x7362);
+    mag[2] = __byte_perm(lo_b, hi_b, 0x5140);
+    mag[3] = __byte_perm(lo_b, hi_b, 0x7362);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // output byte 1 <- replicate(top bit of w4.byte j), byte 3 <- replicate(top bit of w.byte j)
+        uint32_t sgn;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sgn) : "r"(w), "r"(w4), "r"(((0x8u | j) << 12) | ((0x8u | (4 + j)) << 4)));
+        o[j] = mag[j] | (sgn & 0x80008000u);
+    }
     const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -440,10 +453,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             // MXFP4: the converters release the packed tile, the MMA the B tile
-            mbar_init(empty_bar(s), MX ? 1 + kConvThreads : 1);
+            // MXFP4: one arrival per converter warp frees the packed tile, the MMA the B tile
+            mbar_init(empty_bar(s), MX ? 1 + kConvThreads / 32 : 1);
         }
         for (int d = 0; d < C::DSTAGES; ++d) {
-            mbar_init(dfull_bar(d), kConvThreads);
+            mbar_init(dfull_bar(d), kConvThreads / 32);
             mbar_init(dempty_bar(d), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -778,10 +792,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     const uint8_t sc = st[NA * C::RAW_BYTES + t * C::SC_BYTES + r * 16 + sb];
                     decode_half(st + t * C::RAW_BYTES + r * 32 + h * 16, sc, dec + t * C::A_BYTES, r, h);
                 }
-                // generic-proxy shared-memory writes -> visible to the MMA (async proxy)
+                // generic-proxy shared-memory writes -> visible to the MMA (async
+                // proxy); then one arrival per warp, after all its lanes' writes
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(empty_bar(stage));
-                mbar_arrive(dfull_bar(dstage));
+                __syncwarp();
+                if ((tid & 31) == 0) {
+                    mbar_arrive(empty_bar(stage));
+                    mbar_arrive(dfull_bar(dstage));
+                }
                 if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                 if (++dstage == C::DSTAGES) { dstage = 0; dphase ^= 1u; }
             }
