@@ -445,6 +445,13 @@ moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_ge
  * written spec independently, and the two must agree bit for bit). */
 moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream);
 
+/* The kernels' bounded wait on a device counter, alone (a test hook for the
+ * failure path): one thread waits until flag[0] >= target for at most
+ * limit_ns nanoseconds (1 .. 2e9, else MOE_ERR_INVALID_ARG). If the wait runs
+ * out, the device error word gets MOE_ERR_DEVICE_TIMEOUT (read with
+ * moe_get_error) and the kernel returns; nothing traps. */
+moe_status moe_debug_bounded_wait(const int* flag, int target, unsigned long long limit_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

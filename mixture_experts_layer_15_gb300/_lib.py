@@ -40,7 +40,7 @@ EXPORTS = (
     "moe_finalize_add_rmsnorm", "moe_experts_batched_workspace_size", "moe_experts_batched", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
-    "moe_debug_sigmoid",
+    "moe_debug_sigmoid", "moe_debug_bounded_wait",
 )
 
 
@@ -100,6 +100,7 @@ _SIGS = {
     "moe_device_check": ([], _I),
     "moe_set_plan_override": ([_I, _I, _I, _I, _I], _I),
     "moe_debug_sigmoid": ([_P, _P, _I, _P], _I),
+    "moe_debug_bounded_wait": ([_P, _I, ctypes.c_ulonglong, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -268,6 +269,11 @@ def moe_device_check() -> int:
 def moe_set_plan_override(token_tile=0, splits_gemm1=0, splits_gemm2=0, gemm2_tiles=0, fuse=0):
     _check("moe_set_plan_override", lib.moe_set_plan_override(token_tile, splits_gemm1, splits_gemm2,
                                                               gemm2_tiles, fuse))
+
+
+def moe_debug_bounded_wait(flag, target, limit_ns, stream=None):
+    _check("moe_debug_bounded_wait", lib.moe_debug_bounded_wait(_ptr(flag), int(target), int(limit_ns),
+                                                                 _stream(stream)))
 
 
 def moe_debug_sigmoid(x, y, n, stream=None):

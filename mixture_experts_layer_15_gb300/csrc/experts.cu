@@ -218,6 +218,23 @@ size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, cons
     return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, false, batched).total;
 }
 
+namespace {
+// The kernels' bounded counter wait, alone (a test hook for the give-up path):
+// wait until *flag >= target for at most limit_ns; on expiry the error word
+// gets MOE_ERR_DEVICE_TIMEOUT and the kernel returns.
+__global__ void bounded_wait_kernel(const int* flag, int target, unsigned long long limit_ns, int* err) {
+    __shared__ int abort_flag;
+    abort_flag = 0;
+    gemm::wait_counter(flag, target, &abort_flag, err, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_debug_bounded_wait(const int* flag, int target, unsigned long long limit_ns, int* err,
+                                      cudaStream_t s) {
+    bounded_wait_kernel<<<1, 1, 0, s>>>(flag, target, limit_ns, err);
+    return cudaGetLastError();
+}
+
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {
     const Layout L = make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, fin);
     return (fin ? 1 : 0) + ((L.pair || !L.fused) ? 2 : 1);

@@ -231,8 +231,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Bounded wait until *p >= target (acquire, gpu scope). Same give-up rules as
-// wait_bar.
-__device__ __forceinline__ bool wait_counter(const int* p, int target, volatile int* abort_flag, int* err) {
+// wait_bar (limit_ns: the time limit).
+__device__ __forceinline__ bool wait_counter(const int* p, int target, volatile int* abort_flag, int* err,
+                                             uint64_t limit_ns = kWaitLimitNs) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
         int v;
@@ -240,7 +241,7 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, volatile 
         if (v >= target) return true;
         if ((i & 15u) == 15u) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 set_error(err, MOE_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -260,7 +261,10 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 // GEMM1's activation on a (gate, up) pair: silu_and_mul or gelu_and_mul (exact
 // GELU, g/2 * (1 + erf(g / sqrt 2))), after the optional clamp: the gate to at
-// most c, up to [-c, c].
+// most c, up to [-c, c]. Callers branch on act_is_plain() outside their
+// unrolled loops, so that the plain SiLU loop holds no erf (a branch inside
+// the loop is turned into selects that evaluate both activations).
+__device__ __forceinline__ bool act_is_plain(int act, float clamp) { return act == MOE_ACT_SILU && !(clamp > 0.0f); }
 __device__ __forceinline__ float act_mul(float g, float u, int act, float clamp) {
     if (clamp > 0.0f) {
         g = fminf(g, clamp);
@@ -284,13 +288,23 @@ template <int NA, int MODE, typename OutT>
 __device__ __forceinline__ void emit16(const Unit& un, const GemmArgs& a, int row_in_tile, int c0,
                                        const float (&v0)[16], const float (&v1)[16]) {
     OutT* out = static_cast<OutT*>(a.out);
+    if (MODE == MODE_SWIGLU && !act_is_plain(a.act, a.clamp)) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = un.row0 + c0 + i;
+            if (r < un.row_end)
+                store_out<OutT>(out + static_cast<size_t>(r) * a.out_ld + un.wt * kBM + row_in_tile,
+                                act_mul(v0[i], v1[i], a.act, a.clamp));
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int r = un.row0 + c0 + i;
         if (r < un.row_end) {
             const size_t rb = static_cast<size_t>(r) * a.out_ld;
             if (MODE == MODE_SWIGLU) {
-                store_out<OutT>(out + rb + un.wt * kBM + row_in_tile, act_mul(v0[i], v1[i], a.act, a.clamp));
+                store_out<OutT>(out + rb + un.wt * kBM + row_in_tile, silu_mul(v0[i], v1[i]));
             } else {
                 const int col = un.wt * a.wtile_rows + row_in_tile;
                 store_out<OutT>(out + rb + col, v0[i]);
@@ -557,22 +571,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 const CUtensorMap* tA = ph ? &tmA1 : &tmA0;
                 const CUtensorMap* tS = ph ? &tmS1 : &tmS0;
                 const CUtensorMap* tB = ph ? &tmB1 : &tmB0;
-                if (FUSED && ph == 1) {
-                    // the act rows of this token tile must be complete
-                    if (!wait_counter(ka.ready + tile_index(un), ka.g[0].n_wtiles, abort_flag, a0.err)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_global();
-                }
                 const int a_row = un.g * a.rows_per_group + un.wt * a.wtile_rows;
-                for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a0.err)) { ok = false; break; }
+                // the weight-side loads of k-block kb into ring slot `stage` (the
+                // slot's full barrier is armed for the whole stage, act included)
+                auto load_a = [&](int kb) {
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
                     if (MX) {
-                        // packed codes: 32 bytes per row per k-block; scales: the
-                        // 16-byte group of 8 k-blocks that holds this one
                         tma_load_2d(st, tA, kb * (kBK / 2), a_row, full_bar(stage));
                         tma_load_2d(st + NA * C::RAW_BYTES, tS, (kb >> 3) * 16, a_row, full_bar(stage));
                         if (NA == 2) {
@@ -584,6 +589,48 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         tma_load_2d(st, tA, kb * kBK, a_row, full_bar(stage));
                         if (NA == 2) tma_load_2d(st + C::A_BYTES, tA, kb * kBK, a_row + a.a1_offset, full_bar(stage));
                     }
+                };
+                int kb_start = un.kb0;
+                if (FUSED && ph == 1) {
+                    // The act rows of this token tile must be complete before they
+                    // are loaded, but the weight tiles do not depend on them: while
+                    // the tile is not ready, the weight loads of a long unit's first
+                    // k-blocks go out first (up to a ring's worth). Short units are
+                    // not started early: fetched whole, they would compete with the
+                    // GEMM1 tail that the act is waiting for.
+                    const int* rp = ka.ready + tile_index(un);
+                    int v;
+                    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(rp) : "memory");
+                    const int first_stage = stage;
+                    int pre = 0;
+                    if (v < ka.g[0].n_wtiles && un.kb1 - un.kb0 >= 4 * C::STAGES) {
+                        for (int kb = un.kb0; kb < un.kb1 && pre < C::STAGES; ++kb) {
+                            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a0.err)) { ok = false; break; }
+                            load_a(kb);
+                            issued |= 1u << stage;
+                            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                            ++pre;
+                        }
+                    }
+                    const bool got = ok && wait_counter(rp, ka.g[0].n_wtiles, abort_flag, a0.err);
+                    fence_proxy_async_global();
+                    // the act loads of those k-blocks; issued also when the wait gave up,
+                    // so that every armed barrier completes before the CTA leaves
+                    for (int i = 0, s2 = first_stage; i < pre; ++i) {
+                        tma_load_2d(sbase + s2 * C::STAGE_BYTES + C::B_OFF, tB, (un.kb0 + i) * kBK, un.row0,
+                                    full_bar(s2));
+                        if (++s2 == C::STAGES) s2 = 0;
+                    }
+                    if (!got) { ok = false; break; }
+                    kb_start = un.kb0 + pre;
+                }
+                for (int kb = kb_start; kb < un.kb1; ++kb) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a0.err)) { ok = false; break; }
+                    const uint32_t st = sbase + stage * C::STAGE_BYTES;
+                    // packed codes (MXFP4): 32 bytes per row per k-block; scales: the
+                    // 16-byte group of 8 k-blocks that holds this one
+                    load_a(kb);
                     tma_load_2d(st + C::B_OFF, tB, kb * kBK, un.row0, full_bar(stage));
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);

@@ -267,12 +267,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     if (q < 2) {
                         __nv_bfloat16* act = static_cast<__nv_bfloat16*>(a.out);
                         const int col = un.wt * a.wtile_rows + static_cast<int>(rank) * 64 + l64;
+                        if (act_is_plain(a.act, a.clamp)) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int r = un.row0 + c0 + i;
-                            if (r < un.row_end)
-                                act[static_cast<size_t>(r) * a.out_ld + col] =
-                                    __float2bfloat16_rn(act_mul(v[i], xg[i * 64 + l64], a.act, a.clamp));
+                            for (int i = 0; i < 16; ++i) {
+                                const int r = un.row0 + c0 + i;
+                                if (r < un.row_end)
+                                    act[static_cast<size_t>(r) * a.out_ld + col] =
+                                        __float2bfloat16_rn(silu_mul(v[i], xg[i * 64 + l64]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int r = un.row0 + c0 + i;
+                                if (r < un.row_end)
+                                    act[static_cast<size_t>(r) * a.out_ld + col] =
+                                        __float2bfloat16_rn(act_mul(v[i], xg[i * 64 + l64], a.act, a.clamp));
+                            }
                         }
                     }
                     named_bar_sync(2 + grp, 128);             // the exchange buffer is free again

@@ -175,6 +175,15 @@ moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t strea
     return from_cuda(moe::launch_debug_sigmoid(x, y, n, stream));
 }
 
+moe_status moe_debug_bounded_wait(const int* flag, int target, unsigned long long limit_ns, cudaStream_t stream) {
+    if (flag == nullptr || limit_ns == 0 || limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_debug_bounded_wait(flag, target, limit_ns, err, stream));
+}
+
 moe_status moe_route(const float* logits, int M, int E, int top_k, moe_route_method method,
                      const float* score_bias, int n_group, int topk_group, float routed_scaling_factor,
                      int32_t* topk_ids, void* topk_weights, moe_dtype weights_dtype, cudaStream_t stream) {

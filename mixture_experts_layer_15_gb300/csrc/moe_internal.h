@@ -29,6 +29,8 @@ cudaError_t launch_route(const float* logits, int M, int E, int top_k, int metho
                          int32_t* topk_ids, void* topk_weights, int weights_dtype,
                          int* err, cudaStream_t stream);
 cudaError_t launch_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream);
+cudaError_t launch_debug_bounded_wait(const int* flag, int target, unsigned long long limit_ns, int* err,
+                                      cudaStream_t stream);
 
 // ---- permute (permute.cu) ------------------------------------------------------
 size_t permute_workspace_bytes(int M, int top_k, int E_local);

@@ -244,6 +244,35 @@ def test_route_permute_matches_two_calls(moe, name, M, masked):
     check_no_device_error(moe)
 
 
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_gives_up_and_reports(moe):
+    """A wait on a flag that nothing sets runs out after its limit: the kernel
+    returns, the error word reads MOE_ERR_DEVICE_TIMEOUT, and the context stays
+    usable (the next calls run and report no error)."""
+    import time
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    moe.moe_debug_bounded_wait(flag, 1, 50_000_000)                  # 50 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert moe.moe_get_error() == moe.MOE_ERR_DEVICE_TIMEOUT
+    assert moe.moe_get_error() == 0                                 # cleared by the read
+    assert 0.04 <= dt < 5.0
+    flag.fill_(1)                                                   # satisfied: returns at once
+    moe.moe_debug_bounded_wait(flag, 1, 50_000_000)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == 0
+    with pytest.raises(moe.MoEError):
+        moe.moe_debug_bounded_wait(flag, 1, 0)
+    x = torch.linspace(-5, 5, 101, device=DEV)
+    y = torch.empty_like(x)
+    moe.moe_debug_sigmoid(x, y, x.numel())
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all() and moe.moe_get_error() == 0
+
+
 # ------------------------------------------------------------------ whole layer
 
 def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False,
