@@ -45,6 +45,17 @@ page fixes the precision:
   the top-k reduction folded in: residual += out; y = residual /
   sqrt(mean(residual^2) + eps) * gamma (RMSNorm as published by Zhang and
   Sennrich, 2019, in its fused residual-add form).
+* mxfp8_quantize / experts_mxfp8 -- the experts with quantised activations,
+  the ``quantize_input`` step that flashinfer_moe_ep.py ``build_fi_mega_config``
+  enables beside e2m1 + ue8m0-per-32 weights (``FI_MOE_EP_BACKEND_SPECS``,
+  the deep_gemm entry). The pages name the step but not its format; the
+  reading used here is the MX recipe of the weights applied to the
+  activations: FP8 E4M3 elements with one E8M0 scale per 32 consecutive
+  values along each GEMM's reduction axis (OCP Microscaling Formats v1.0:
+  scale 2^(floor(log2 amax) - 8), elements rounded to nearest-even and
+  saturated at the largest finite E4M3 value). The E4M3 codec is written
+  from the format's definition (sign, 4 exponent bits with bias 7, 3
+  mantissa bits, subnormals at exponent 0, no infinities).
 * e2m1 / E8M0 decode (flashinfer_moe_ep.py ``_E2M1_LUT`` and
   ``_dequant_fp4_ue8m0_gran32``): here the page fixes the arithmetic --
   an fp32 product of the table value and the scale, returned as bf16 -- and
@@ -66,7 +77,8 @@ __all__ = [
     "sigmoid_f32_spec", "route_softmax_topk", "route_sigmoid_grouped",
     "permute", "expert_mlp", "experts", "finalize", "shared_expert",
     "moe_forward", "bf16_round", "gelu_erf", "experts_batched", "add_rmsnorm",
-    "finalize_add_rmsnorm",
+    "finalize_add_rmsnorm", "E4M3_MAX", "e4m3_value", "e4m3_round", "mxfp8_scale_byte",
+    "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_qdq", "experts_mxfp8",
 ]
 
 # --------------------------------------------------------------------------
@@ -136,6 +148,96 @@ def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
     with np.errstate(over="ignore", invalid="ignore"):
         prod = (vals.reshape(rows, C // 32, 32) * sf[:, :, None]).reshape(rows, C)
     return bf16_round(prod).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# MXFP8 activations: FP8 E4M3 elements, one E8M0 scale per 32 values
+# --------------------------------------------------------------------------
+
+#: The largest finite E4M3 value, 1.75 * 2^8 (code 0x7E); E4M3 has no infinities.
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code) -> np.ndarray:
+    """E4M3 code(s) -> value(s), float64. Bit 7 is the sign, bits 6..3 the
+    exponent (bias 7), bits 2..0 the mantissa. Exponent field 0 holds the
+    subnormals m/8 * 2^-6; every other field the normals (1 + m/8) * 2^(e-7),
+    except S.1111.111, which is NaN."""
+    c = np.asarray(code, dtype=np.int64) & 0xFF
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Value(s) -> nearest E4M3 code(s), ties to the even code, magnitudes
+    above 448 saturated to 448 (NaN -> 0x7F). The quantum of a magnitude a is
+    2^(max(floor(log2 a), -6) - 3): the normals' binade spacing, and the
+    subnormals' fixed 2^-9 below 2^-6. a / quantum is exact in float64, so
+    numpy's half-to-even round is the rounding rule itself."""
+    v = np.asarray(v, dtype=np.float64)
+    sign = np.signbit(v)
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ex = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    ex = np.maximum(ex, -6.0)
+    q = np.exp2(ex - 3.0)
+    r = np.round(a / q) * q                       # rounded magnitude, still <= 448
+    # encode r: a carry into the next binade is a normal with mantissa 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        er = np.floor(np.log2(np.where(r > 0, r, 1.0)))
+    normal = r >= 2.0 ** -6
+    e_field = np.where(normal, er + 7.0, 0.0)
+    m_field = np.where(normal, np.round((r / np.exp2(er) - 1.0) * 8.0), np.round(r / 2.0 ** -9))
+    code = (e_field.astype(np.int64) << 3) | m_field.astype(np.int64)
+    code = np.where(sign, code | 0x80, code)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def mxfp8_scale_byte(amax) -> np.ndarray:
+    """E8M0 scale byte of blocks with largest magnitude ``amax`` (float32):
+    the scale is 2^(floor(log2 amax) - 8), 8 being E4M3's largest exponent,
+    so that amax / scale lies in [256, 512). On the float32 bit pattern,
+    floor(log2 amax) + 127 is the exponent field, hence byte = field - 8. The
+    byte is kept in 1..254, where every E8M0 decode gives 2^(byte - 127) (an
+    all-zero block gets byte 1 and codes 0)."""
+    a = np.abs(np.asarray(amax, dtype=np.float32))
+    field = (a.reshape(-1).view(np.uint32) >> np.uint32(23)).astype(np.int64) & 0xFF
+    return np.clip(field - 8, 1, 254).astype(np.uint8).reshape(a.shape)
+
+
+def mxfp8_quantize(x):
+    """x [..., C] (C a multiple of 32), taken as float32 -> (codes uint8
+    [..., C], scale bytes uint8 [..., C/32]): blocks of 32 consecutive
+    values along the last axis share one scale; each value becomes
+    e4m3_round(value / scale) (value / scale is an exact power-of-two
+    division)."""
+    x = np.asarray(x, dtype=np.float32)
+    C = x.shape[-1]
+    assert C % 32 == 0
+    blocks = x.reshape(x.shape[:-1] + (C // 32, 32)).astype(np.float64)
+    amax = np.abs(blocks).max(axis=-1).astype(np.float32)
+    sb = mxfp8_scale_byte(amax)
+    scale = np.exp2(sb.astype(np.float64) - 127.0)
+    codes = e4m3_round(blocks / scale[..., None])
+    return codes.reshape(x.shape), sb
+
+
+def mxfp8_dequantize(codes, scales) -> np.ndarray:
+    """(codes [..., C], scale bytes [..., C/32]) -> values [..., C], float64."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    C = codes.shape[-1]
+    vals = e4m3_value(codes).reshape(codes.shape[:-1] + (C // 32, 32))
+    scale = np.exp2(np.asarray(scales, dtype=np.float64) - 127.0)
+    return (vals * scale[..., None]).reshape(codes.shape)
+
+
+def mxfp8_qdq(x) -> np.ndarray:
+    """x as the GEMM consuming its MXFP8 form sees it: dequantize(quantize(x))."""
+    return mxfp8_dequantize(*mxfp8_quantize(x))
 
 
 # --------------------------------------------------------------------------
@@ -312,13 +414,19 @@ def gelu_erf(z) -> np.ndarray:
 
 
 def expert_mlp(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, activation: str = "silu",
-               clamp=None) -> np.ndarray:
+               clamp=None, qdq=None) -> np.ndarray:
     """One expert on token rows x [T, K]: h = x W1^T [T, 2N]; the first N
     columns are the gate, the last N the up projection (the ``*_and_mul``
     activations: output width half the input width). With ``clamp`` = c the
     gate is clamped to at most c and up to [-c, c] first. Then
     a = act(gate) * up, with silu(z) = z / (1 + e^-z) or gelu = gelu_erf;
-    y = a W2^T [T, K]. Float64."""
+    y = a W2^T [T, K]. Float64.
+
+    ``qdq`` (quantised activations): applied to x before GEMM1 and to a,
+    rounded to float32, before GEMM2 -- each GEMM then reads its activation
+    operand as its quantised form dequantised."""
+    if qdq is not None:
+        x = qdq(x)
     x = np.asarray(x, dtype=np.float64)
     w1 = np.asarray(w1, dtype=np.float64)
     w2 = np.asarray(w2, dtype=np.float64)
@@ -335,14 +443,18 @@ def expert_mlp(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, activation: str = 
         a = gelu_erf(gate) * up
     else:
         raise ValueError(activation)
+    if qdq is not None:
+        a = qdq(np.asarray(a, dtype=np.float32))
     return a @ w2.T
 
 
 def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
-            inverse: np.ndarray, top_k: int, activation: str = "silu", clamp=None) -> np.ndarray:
+            inverse: np.ndarray, top_k: int, activation: str = "silu", clamp=None,
+            qdq=None) -> np.ndarray:
     """``gemm2_permuted`` [R, K]: row p is the output of expert le (the p-th
     row falls in [offsets[le], offsets[le+1])) on token inverse[p] // top_k.
-    ``w1``/``w2`` are the local experts' weights as float arrays."""
+    ``w1``/``w2`` are the local experts' weights as float arrays; ``qdq`` as
+    in expert_mlp."""
     x = np.asarray(x, dtype=np.float64)
     R = int(offsets[-1])
     out = np.zeros((R, w2.shape[1]), dtype=np.float64)
@@ -350,8 +462,17 @@ def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
         r0, r1 = int(offsets[le]), int(offsets[le + 1])
         if r1 > r0:
             toks = np.asarray(inverse[r0:r1], dtype=np.int64) // top_k
-            out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le], activation, clamp)
+            out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le], activation, clamp, qdq)
     return out
+
+
+def experts_mxfp8(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
+                  inverse: np.ndarray, top_k: int, activation: str = "silu", clamp=None) -> np.ndarray:
+    """``experts`` with MXFP8 activations: every token row quantised per 32
+    along K before GEMM1, the activation output (float32) per 32 along N
+    before GEMM2; the weights as given (MXFP4 weights: their exact dequantised
+    values)."""
+    return experts(x, w1, w2, offsets, inverse, top_k, activation, clamp, qdq=mxfp8_qdq)
 
 
 def experts_batched(xb: np.ndarray, counts: np.ndarray, w1: np.ndarray, w2: np.ndarray,

@@ -476,3 +476,135 @@ def test_finalize_add_rmsnorm_composition():
         want = shared[t] + res[t] + 2.5 * sum(w[t, j] * g2[pmap[t, j]] for j in range(k) if pmap[t, j] >= 0)
         np.testing.assert_allclose(r[t], want, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- MXFP8 activations
+
+def test_e4m3_decode_matches_library_and_closed_forms():
+    """All 256 codes against torch's float8_e4m3fn decode (a library routine),
+    and the format's landmarks: 1.0, the largest finite value, the smallest
+    normal and subnormal, the NaN codes."""
+    codes = np.arange(256)
+    ours = O.e4m3_value(codes)
+    lib = torch.from_numpy(codes.astype(np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    fin = ~np.isnan(ours)
+    assert np.array_equal(ours[fin], lib[fin].astype(np.float64))
+    assert O.e4m3_value(0x38) == 1.0 and O.e4m3_value(0x7E) == O.E4M3_MAX == 448.0
+    assert O.e4m3_value(0x08) == 2.0 ** -6 and O.e4m3_value(0x01) == 2.0 ** -9
+    assert O.e4m3_value(0xB8) == -1.0
+    assert np.isnan(O.e4m3_value(0x7F)) and np.isnan(O.e4m3_value(0xFF))
+    assert np.isnan(ours).sum() == 2
+
+
+def test_e4m3_round_matches_library_including_ties():
+    """Every representable value, every midpoint between neighbours (the
+    ties), points just off the midpoints, and random values, against torch's
+    round-to-nearest-even float8_e4m3fn cast; saturation at 448 by its own
+    closed form (torch does not saturate)."""
+    vals = np.unique(O.e4m3_value(np.arange(256))[~np.isnan(O.e4m3_value(np.arange(256)))])
+    pos = vals[vals >= 0]
+    mids = (pos[1:] + pos[:-1]) / 2
+    probe = np.concatenate([vals, mids, -mids, mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20),
+                            np.random.default_rng(61).uniform(-448, 448, 20000)]).astype(np.float32)
+    ours = O.e4m3_round(probe)
+    lib = torch.from_numpy(probe).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+    # a tie goes to the even mantissa: 1 + 1/16 lies between 1.0 (m=0) and 1.125 (m=1)
+    assert O.e4m3_round(np.float32(1.0625)) == 0x38
+    assert O.e4m3_round(np.float32(1.1875)) == 0x3A          # between m=1 and m=2 -> m=2
+    for big, code in ((448.0, 0x7E), (463.9, 0x7E), (500.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE)):
+        assert O.e4m3_round(np.float32(big)) == code
+    assert O.e4m3_round(np.float32(2.0 ** -10)) == 0x00         # half the smallest subnormal: tie to 0
+    assert O.e4m3_round(np.float32(-0.0)) == 0x80
+
+
+@pytest.mark.parametrize("j", [-100, -7, 0, 3, 20, 100])
+def test_mxfp8_scale_rule_closed_form(j):
+    """For amax in [2^j, 2^(j+1)) the scale is 2^(j-8): amax / scale lies in
+    [256, 512); the byte is j + 119. Clamped to 1..254 at the ends."""
+    for f in (1.0, 1.3, 1.75, 1.999):
+        amax = np.float32(f * 2.0 ** j)
+        b = int(O.mxfp8_scale_byte(amax))
+        assert b == j + 119
+        assert 256 <= float(amax) / 2.0 ** (b - 127) < 512
+    assert int(O.mxfp8_scale_byte(np.float32(0.0))) == 1
+    assert int(O.mxfp8_scale_byte(np.float32(2.0 ** -130))) == 1
+    assert int(O.mxfp8_scale_byte(np.float32(3e38))) == 246          # exponent field 254
+
+
+def test_mxfp8_qdq_identity_on_representable_blocks():
+    """A block whose values are E4M3 values times 2^s, with its largest
+    magnitude in [256, 448] * 2^s, is its own quantisation: the scale rule
+    picks 2^s and every element is already on the grid."""
+    rng = np.random.default_rng(67)
+    grid = O.e4m3_value(np.arange(256))
+    grid = grid[~np.isnan(grid)]
+    rows = []
+    for s in (-20, -3, 0, 5):
+        for _ in range(8):
+            v = rng.choice(grid, 32)
+            v[rng.integers(32)] = rng.choice(grid[(np.abs(grid) >= 256)])
+            rows.append(v * 2.0 ** s)
+    x = np.array(rows).reshape(8, 4 * 32)
+    codes, sb = O.mxfp8_quantize(x)
+    assert np.array_equal(O.mxfp8_dequantize(codes, sb), x)
+
+
+def test_mxfp8_qdq_error_bound_and_block_axis():
+    """Each value's error is at most half a quantum of its binade: 2^-4 of its
+    magnitude for normals, 2^-10 * scale below 2^-6 * scale, and saturation
+    only within [448, 512) * scale. Blocks run along the last axis in groups
+    of 32: a huge value in one block leaves the next block's precision
+    alone, and transposing the input changes the result."""
+    rng = np.random.default_rng(71)
+    x = (rng.standard_normal((32, 256)) * np.exp(rng.uniform(-8, 8, (32, 1)))).astype(np.float32)
+    codes, sb = O.mxfp8_quantize(x)
+    q = O.mxfp8_dequantize(codes, sb)
+    scale = np.repeat(np.exp2(sb.astype(np.float64) - 127), 32, axis=1)
+    a = np.abs(x.astype(np.float64))
+    bound = np.where(a / scale >= 2.0 ** -6, 2.0 ** -4 * a, 2.0 ** -10 * scale)
+    bound = np.where(a / scale > 448, a - 448 * scale, bound)
+    assert np.all(np.abs(q - x) <= bound * (1 + 1e-12))
+    y = np.ones((1, 64), np.float32)
+    y[0, 0] = 1e6
+    y[0, 32:] = np.linspace(1, 2, 32, dtype=np.float32)
+    qy = O.mxfp8_qdq(y)
+    assert np.all(qy[0, 1:32] == 0.0)                     # swamped by 1e6 in their block
+    assert np.all(np.abs(qy[0, 32:] - y[0, 32:]) <= 2.0 ** -4 * y[0, 32:])
+    xt = np.ascontiguousarray(x[:, :32].T)
+    assert not np.array_equal(O.mxfp8_qdq(xt).T, q[:, :32])
+
+
+def test_experts_mxfp8_quantises_both_gemm_inputs():
+    """experts_mxfp8 = experts with MXFP8 quantisation of x [T, K] before GEMM1
+    and of the float32 activation output [T, N] before GEMM2, nothing else:
+    with an identity quantiser the result is experts' own (up to the float32
+    rounding of the activation), a recording
+    quantiser sees exactly those two operands, and the quantised result sits
+    within the first-order error bound of the exact one."""
+    rng = np.random.default_rng(73)
+    E, K, N, M, k = 3, 64, 96, 7, 2
+    w1 = rng.standard_normal((E, 2 * N, K)) / np.sqrt(K)
+    w2 = rng.standard_normal((E, K, N)) / np.sqrt(N)
+    x = O.bf16_round(rng.standard_normal((M, K))).astype(np.float64)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    offs, pmap, inv, _ = O.permute(ids, E)
+    exact = O.experts(x, w1, w2, offs, inv, k)
+    # identity quantiser: only the activation's float32 rounding remains
+    ident = O.experts(x, w1, w2, offs, inv, k, qdq=lambda a: np.asarray(a, np.float64))
+    np.testing.assert_allclose(ident, exact, rtol=1e-5, atol=1e-6 * np.abs(exact).max())
+    seen = []
+
+    def spy(a):
+        seen.append((np.asarray(a).shape, np.asarray(a).dtype))
+        return O.mxfp8_qdq(a)
+    spied = O.experts(x, w1, w2, offs, inv, k, qdq=spy)
+    got = O.experts_mxfp8(x, w1, w2, offs, inv, k)
+    assert np.array_equal(spied, got)
+    shapes = sorted({s for s, _ in seen})
+    assert all(s[1] in (K, N) for s in shapes) and {s[1] for s in shapes} == {K, N}
+    assert all(d == np.float32 for s, d in seen if s[1] == N)
+    # first-order bound: |dy| <= |W2| (|da|), |da| <= 2^-4 |a| + |d act / dh| |W1| |dx| (loose, x4)
+    rel = np.linalg.norm(got - exact) / np.linalg.norm(exact)
+    assert 1e-4 < rel < 0.1
