@@ -70,7 +70,9 @@ typedef enum moe_route_method {
 
 typedef enum moe_weight_format {
     MOE_WEIGHTS_BF16 = 0,          /* bf16 weights                                     */
-    MOE_WEIGHTS_MXFP4 = 1          /* e2m1 codes, two per byte, + one E8M0 byte per 32 */
+    MOE_WEIGHTS_MXFP4 = 1,         /* e2m1 codes, two per byte, + one E8M0 byte per 32 */
+    MOE_WEIGHTS_MXFP4_A8 = 2       /* MXFP4 weights, scales as moe_mx_prepare_scales
+                                      writes them; activations quantised to MXFP8   */
 } moe_weight_format;
 
 /*
@@ -90,6 +92,19 @@ typedef enum moe_weight_format {
  *          (flashinfer_moe_ep.py, _E2M1_LUT and _dequant_fp4_ue8m0_gran32).
  *          Scale bytes must lie in 1..254 and every decoded value must be a
  *          normal bf16 or zero (the kernels decode to bf16 before the MMA).
+ *   MXFP4_A8: the MXFP4 codes as above (w1, w2; 32-byte aligned); w1_scale
+ *          and w2_scale hold the same scales rearranged by
+ *          moe_mx_prepare_scales (w1: rows 2N, cols K; w2: rows K, cols N).
+ *          The experts then run with MXFP8 activations -- the quantize_input
+ *          step of flashinfer_moe_ep.py build_fi_mega_config, read as the
+ *          weights' MX recipe: every 32 consecutive values along a GEMM's
+ *          reduction axis share an E8M0 scale 2^(floor(log2 amax) - 8) (byte
+ *          kept in 1..254) and are rounded to E4M3 (nearest, ties to even,
+ *          saturated at 448) -- x_perm before GEMM1 and the activation output
+ *          before GEMM2; block-scaled tensor-core MMAs apply both scales.
+ *          Outputs therefore differ from the MXFP4 format's by the
+ *          activations' quantisation error. K % 256 == 0, N % 128 == 0;
+ *          moe_experts and moe_experts_fused_finalize only.
  *
  * K and N must be multiples of 128 (of 512 for MXFP4). All pointers 16-byte
  * aligned.
@@ -417,6 +432,30 @@ moe_status moe_shared_expert(const void* ws1, const void* ws2, int K, int Ns,
  * Diagnostics.
  * ---------------------------------------------------------------------- */
 /* Static text for a status code (never NULL). */
+/* ------------------------------------------------------------------------
+ * MXFP8 quantisation and the block-scaled weight layout
+ * ------------------------------------------------------------------------
+ * moe_mxfp8_quantize: x bf16 [rows, C] -> codes u8 [rows, C] (E4M3) and
+ * scales u8 [rows, C/32] (E8M0): the MXFP8 rule of MOE_WEIGHTS_MXFP4_A8
+ * (blocks of 32 consecutive values of a row; scale byte = clamp(exponent
+ * field of the block's largest magnitude - 8, 1, 254); code = E4M3 nearest to
+ * value * 2^(127 - byte), ties to even, saturated at 448). C % 128 == 0
+ * (MOE_ERR_ALIGNMENT); x and codes 16-byte aligned. rows == 0 is a no-op.
+ *
+ * moe_mx_prepared_scales_size / moe_mx_prepare_scales: the E8M0 scales of
+ * an MXFP4 matrix, u8 [E_local, rows, cols/32] row-major, rearranged for the
+ * block-scaled MMA: for each 128-row tile and 128-column block of a 512-byte
+ * atom, row r's four scale bytes at byte (r % 32) * 16 + ((r % 128) / 32) * 4.
+ * rows and cols multiples of 128 (MOE_ERR_ALIGNMENT); scales 4-byte aligned,
+ * out 16-byte aligned, of moe_mx_prepared_scales_size() bytes (0 for invalid
+ * sizes). A one-time weight preparation; asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+moe_status moe_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t stream);
+size_t moe_mx_prepared_scales_size(int E_local, int rows, int cols);
+moe_status moe_mx_prepare_scales(const uint8_t* scales, int E_local, int rows, int cols, uint8_t* out,
+                                 cudaStream_t stream);
+
 const char* moe_status_string(int status);
 
 /* Synchronizes `stream`, then returns and clears the device error word of the

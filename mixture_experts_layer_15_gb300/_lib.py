@@ -29,6 +29,7 @@ MOE_ROUTE_SOFTMAX_TOPK = 0
 MOE_ROUTE_SIGMOID_GROUPED_TOPK = 1
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_MXFP4 = 1
+MOE_WEIGHTS_MXFP4_A8 = 2
 MOE_ACT_SILU = 0
 MOE_ACT_GELU = 1
 
@@ -41,6 +42,7 @@ EXPORTS = (
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid", "moe_debug_bounded_wait",
+    "moe_mxfp8_quantize", "moe_mx_prepared_scales_size", "moe_mx_prepare_scales",
 )
 
 
@@ -101,6 +103,9 @@ _SIGS = {
     "moe_set_plan_override": ([_I, _I, _I, _I, _I], _I),
     "moe_debug_sigmoid": ([_P, _P, _I, _P], _I),
     "moe_debug_bounded_wait": ([_P, _I, ctypes.c_ulonglong, _P], _I),
+    "moe_mxfp8_quantize": ([_P, _I, _I, _P, _P, _P], _I),
+    "moe_mx_prepared_scales_size": ([_I, _I, _I], _Z),
+    "moe_mx_prepare_scales": ([_P, _I, _I, _I, _P, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -278,3 +283,17 @@ def moe_debug_bounded_wait(flag, target, limit_ns, stream=None):
 
 def moe_debug_sigmoid(x, y, n, stream=None):
     _check("moe_debug_sigmoid", lib.moe_debug_sigmoid(_ptr(x), _ptr(y), n, _stream(stream)))
+
+
+def moe_mxfp8_quantize(x, rows, C, codes, scales, stream=None):
+    _check("moe_mxfp8_quantize", lib.moe_mxfp8_quantize(_ptr(x), rows, C, _ptr(codes), _ptr(scales),
+                                                         _stream(stream)))
+
+
+def moe_mx_prepared_scales_size(E_local, rows, cols):
+    return lib.moe_mx_prepared_scales_size(E_local, rows, cols)
+
+
+def moe_mx_prepare_scales(scales, E_local, rows, cols, out, stream=None):
+    _check("moe_mx_prepare_scales", lib.moe_mx_prepare_scales(_ptr(scales), E_local, rows, cols, _ptr(out),
+                                                               _stream(stream)))

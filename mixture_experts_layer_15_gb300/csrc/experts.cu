@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "gemm_kernel.cuh"
+#include "gemm_mx8_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
 
 namespace moe {
@@ -47,6 +48,21 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
 bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     return encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, kBK, box_outer,
                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Packed e2m1 codes [outer, inner codes] (inner / 2 bytes per row) for the
+// block-scaled MMA: 128 codes x 128 rows per box, landing as 128-byte padded
+// rows under the 128-byte swizzle (16U4_ALIGN16B).
+bool encode_fp4(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+    auto fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner / 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemm::kMxBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ---- plan: token-tile width, split-K and workspace layout --------------------------
@@ -122,12 +138,47 @@ struct Layout {
     int max_token_tiles;
     GemmPlan g1, g2;
     size_t off_act, off_p1, off_p2, total;
+    // MXFP8 activations (MOE_WEIGHTS_MXFP4_A8): x codes and atoms, act codes and atoms
+    size_t off_xq = 0, off_xs = 0, off_aq = 0, off_as = 0;
 };
+
+// MXFP4 weights x MXFP8 activations: three launches (quantise x, GEMM1 with
+// the quantising epilogue, GEMM2), token tiles of at most 128 rows (one scale
+// atom per tile and k-block). Plans count k-blocks of 128 elements.
+Layout make_layout_a8(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin) {
+    Layout L;
+    const int K = w->K, N = w->N;
+    L.bt = g_override.token_tile > 0 ? g_override.token_tile : pick_bt(M, rows_alloc, groups, K, N, false);
+    if (L.bt > 128) L.bt = 128;
+    L.g1 = plan_gemm(0, L.bt, 2, N / kBM, K / 2, rows_alloc, groups, sm_count);
+    L.g2 = plan_gemm(1, L.bt, 2, K / (2 * kBM), N / 2, rows_alloc, groups, sm_count, fin);
+    L.fused = false;
+    L.pair = false;
+    L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
+    const size_t tiles = static_cast<size_t>(L.max_token_tiles);
+    size_t off = 4 * kMaxSplitTiles * sizeof(int);
+    L.off_act = 0;
+    L.off_xq = off;
+    off = align256(off + static_cast<size_t>(rows_alloc) * K);
+    L.off_xs = off;
+    off = align256(off + tiles * (K / gemm::kMxBK) * gemm::kAtom);
+    L.off_aq = off;
+    off = align256(off + static_cast<size_t>(rows_alloc) * N);
+    L.off_as = off;
+    off = align256(off + tiles * (N / gemm::kMxBK) * gemm::kAtom);
+    L.off_p1 = off;
+    off = align256(off + L.g1.partial_bytes);
+    L.off_p2 = off;
+    off = align256(off + L.g2.partial_bytes);
+    L.total = off;
+    return L;
+}
 
 // fin: GEMM2 finalizes in its epilogue (needs no more workspace than without)
 // batched: the BatchedExperts layout, which runs as two one-CTA launches
 Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin = false,
                    bool batched = false) {
+    if (w->format == MOE_WEIGHTS_MXFP4_A8) return make_layout_a8(w, rows_alloc, M, groups, sm_count, fin);
     Layout L;
     const int K = w->K, N = w->N;
     L.bt = g_override.token_tile > 0 ? g_override.token_tile
@@ -198,6 +249,85 @@ bool encode_weights(CUtensorMap* tmA, CUtensorMap* tmS, bool mx, const void* w, 
                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// The experts with MXFP8 activations: x_perm -> codes + atoms, GEMM1 (act
+// codes + atoms), GEMM2 (y, or the finalize into the f32 out).
+cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t* ws, int* err, const DeviceInfo& dev,
+                              cudaStream_t s) {
+    const moe_weights* w = p.w;
+    const int K = w->K, N = w->N;
+    const uint64_t E = static_cast<uint64_t>(w->E_local);
+    const bool fin = p.fin_out != nullptr;
+    uint8_t* xq = ws + L.off_xq;
+    uint8_t* xs = ws + L.off_xs;
+    uint8_t* aq = ws + L.off_aq;
+    uint8_t* as = ws + L.off_as;
+    int* counters = reinterpret_cast<int*>(ws);
+    CUtensorMap tA1, tB1, tA2, tB2;
+    if (!encode_fp4(&tA1, w->w1, K, E * 2 * N) || !encode_fp4(&tA2, w->w2, N, E * K) ||
+        !encode_2d(&tB1, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, p.rows_alloc, gemm::kMxBK, L.bt,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tB2, aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, p.rows_alloc, gemm::kMxBK, L.bt,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    gemm::Mx8Args m1{};
+    GemmArgs& a1 = m1.g;
+    a1.offsets = p.offsets;
+    a1.groups = w->E_local;
+    a1.rows_alloc = p.rows_alloc;
+    a1.kr = K;
+    a1.rows_per_group = 2 * N;
+    a1.n_wtiles = L.g1.n_wtiles;
+    a1.wtile_rows = kBM;
+    a1.a1_offset = N;
+    a1.splits = L.g1.splits;
+    a1.out_ld = N;
+    a1.out = aq;
+    a1.partials = reinterpret_cast<float*>(ws + L.off_p1);
+    a1.counters = counters;
+    a1.max_tiles = L.g1.max_tiles;
+    a1.err = err;
+    a1.act = w->activation;
+    a1.clamp = w->activation_clamp;
+    m1.sfa = w->w1_scale;
+    m1.sfb = xs;
+    m1.sfb_out = as;
+    m1.bt = L.bt;
+    m1.max_token_tiles = L.max_token_tiles;
+    gemm::Mx8Args m2 = m1;
+    GemmArgs& a2 = m2.g;
+    a2.kr = N;
+    a2.rows_per_group = K;
+    a2.n_wtiles = L.g2.n_wtiles;
+    a2.wtile_rows = 2 * kBM;
+    a2.a1_offset = kBM;
+    a2.splits = L.g2.splits;
+    a2.out_ld = K;
+    a2.out = fin ? static_cast<void*>(p.fin_out) : p.y;
+    a2.inverse = p.inverse;
+    a2.fw = p.fin_weights;
+    a2.fw_dtype = p.fin_weights_dtype;
+    a2.top_k = p.top_k;
+    a2.rsf = p.rsf;
+    a2.partials = reinterpret_cast<float*>(ws + L.off_p2);
+    a2.counters = counters + kMaxSplitTiles;
+    a2.max_tiles = L.g2.max_tiles;
+    m2.sfa = w->w2_scale;
+    m2.sfb = as;
+    m2.sfb_out = nullptr;
+    const int grid = dev.sm_count;
+    cudaError_t e;
+    if (fin) {
+        e = launch_out_init(p.fin_shared, p.fin_shared_dtype, p.M, K, p.fin_out, dev, s);
+        if (e != cudaSuccess) return e;
+    }
+    e = launch_mxfp8_quantize_tiles(p.x, p.rows_alloc, K, p.offsets, w->E_local, L.bt, L.max_token_tiles, xq, xs,
+                                    err, dev, s);
+    if (e != cudaSuccess) return e;
+    e = gemm::launch_gemm_mx8(gemm::MODE_SWIGLU, L.bt, MOE_DTYPE_BF16, tA1, tB1, m1, grid, s);
+    if (e != cudaSuccess) return e;
+    return gemm::launch_gemm_mx8(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, L.bt, p.y_dtype, tA2, tB2, m2, grid, s);
+}
+
 cudaError_t launch_one(bool mx, int fused, int mode, int bt, int na, int out_dtype, const gemm::Maps& m,
                        const gemm::KernelArgs& ka, int grid, cudaStream_t s) {
     return mx ? gemm::launch_gemm_mxfp4(fused, mode, bt, na, out_dtype, m, ka, grid, s)
@@ -236,6 +366,7 @@ cudaError_t launch_debug_bounded_wait(const int* flag, int target, unsigned long
 }
 
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {
+    if (w->format == MOE_WEIGHTS_MXFP4_A8) return (fin ? 1 : 0) + 3;
     const Layout L = make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, fin);
     return (fin ? 1 : 0) + ((L.pair || !L.fused) ? 2 : 1);
 }
@@ -253,8 +384,10 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     int* counters = reinterpret_cast<int*>(ws);
     void* act = ws + L.off_act;
 
-    gemm::Maps m;
     const uint64_t E = static_cast<uint64_t>(w->E_local);
+    if (w->format == MOE_WEIGHTS_MXFP4_A8) return launch_experts_a8(p, L, ws, err, dev, s);
+
+    gemm::Maps m;
     if (!encode_weights(&m.A[0], &m.S[0], mx, w->w1, w->w1_scale, K, E * 2 * N) ||
         !encode_weights(&m.A[1], &m.S[1], mx, w->w2, w->w2_scale, N, E * K) ||
         !encode_bf16(&m.B[0], p.x, K, p.rows_alloc, L.bt) || !encode_bf16(&m.B[1], act, N, p.rows_alloc, L.bt))

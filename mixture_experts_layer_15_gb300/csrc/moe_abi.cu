@@ -84,12 +84,20 @@ inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : 
 moe_status check_weights(const moe_weights* w) {
     if (w == nullptr || w->w1 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
     if (w->E_local < 1 || w->E_local > 1024 || w->K <= 0 || w->N <= 0) return MOE_ERR_INVALID_ARG;
-    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4 && w->format != MOE_WEIGHTS_MXFP4_A8)
+        return MOE_ERR_INVALID_ARG;
     if (w->activation != MOE_ACT_SILU && w->activation != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
     if (!(w->activation_clamp == w->activation_clamp) || w->activation_clamp == INFINITY) return MOE_ERR_INVALID_ARG;
     if (w->K % 128 != 0 || w->N % 128 != 0) return MOE_ERR_ALIGNMENT;
     if (!aligned16(w->w1) || !aligned16(w->w2)) return MOE_ERR_ALIGNMENT;
-    if (w->format == MOE_WEIGHTS_MXFP4) {
+    if (w->format == MOE_WEIGHTS_MXFP4_A8) {
+        // codes by 16U4 TMA (32-byte aligned); prepared scale atoms by bulk copies
+        if (w->w1_scale == nullptr || w->w2_scale == nullptr) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(w->w1_scale) || !aligned16(w->w2_scale)) return MOE_ERR_ALIGNMENT;
+        if ((reinterpret_cast<uintptr_t>(w->w1) & 31) != 0 || (reinterpret_cast<uintptr_t>(w->w2) & 31) != 0)
+            return MOE_ERR_ALIGNMENT;
+        if (w->K % 256 != 0) return MOE_ERR_ALIGNMENT;
+    } else if (w->format == MOE_WEIGHTS_MXFP4) {
         if (w->w1_scale == nullptr || w->w2_scale == nullptr) return MOE_ERR_INVALID_ARG;
         if (!aligned16(w->w1_scale) || !aligned16(w->w2_scale)) return MOE_ERR_ALIGNMENT;
         // scale rows of K/32 and N/32 bytes must be 16-byte multiples for the TMA
@@ -163,6 +171,40 @@ moe_status moe_set_plan_override(int token_tile, int splits_gemm1, int splits_ge
     if (gemm2_tiles < 0 || gemm2_tiles > 2 || fuse < 0 || fuse > 3) return MOE_ERR_INVALID_ARG;
     moe::set_plan_override(token_tile, splits_gemm1, splits_gemm2, gemm2_tiles, fuse);
     return MOE_OK;
+}
+
+moe_status moe_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t stream) {
+    if (rows < 0 || C <= 0) return MOE_ERR_INVALID_ARG;
+    if (C % 128 != 0) return MOE_ERR_ALIGNMENT;
+    if (static_cast<long long>(rows) * C >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_mxfp8_quantize(x, rows, C, codes, scales, err, info, stream));
+}
+
+size_t moe_mx_prepared_scales_size(int E_local, int rows, int cols) {
+    if (E_local < 1 || rows <= 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0) return 0;
+    return static_cast<size_t>(E_local) * (rows / 128) * (cols / 128) * 512;
+}
+
+moe_status moe_mx_prepare_scales(const uint8_t* scales, int E_local, int rows, int cols, uint8_t* out,
+                                 cudaStream_t stream) {
+    if (E_local < 1 || rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_ALIGNMENT;
+    if (scales == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(scales) & 3) != 0 || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_mx_prepare_scales(scales, static_cast<long long>(E_local) * rows, cols, out, info,
+                                                   stream));
 }
 
 moe_status moe_debug_sigmoid(const float* x, float* y, int n, cudaStream_t stream) {
@@ -490,6 +532,7 @@ moe_status moe_experts_batched(const moe_weights* w, const void* x, const int32_
     if (max_tokens < 0) return MOE_ERR_INVALID_ARG;
     const moe_status ws_ok = check_weights(w);
     if (ws_ok != MOE_OK) return ws_ok;
+    if (w->format == MOE_WEIGHTS_MXFP4_A8) return MOE_ERR_UNSUPPORTED;
     if (!valid_dtype(y_dtype)) return MOE_ERR_INVALID_ARG;
     const long long rows = static_cast<long long>(w->E_local) * max_tokens;
     if (rows >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;

@@ -94,6 +94,19 @@ struct ExpertsProblem {
     int batch_stride = 0;
 };
 
+// ---- MXFP8 activations (mx8_quant.cu) ----------------------------------------------
+// x bf16 [rows, C] -> E4M3 codes [rows, C] + E8M0 scales [rows, C/32] (C % 128 == 0).
+cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
+                                  const DeviceInfo& dev, cudaStream_t stream);
+// The same for the grouped rows of x_perm, scales into the token-tile atoms
+// of the block-scaled GEMM (tiles of bt rows per group, at most max_tiles).
+cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
+                                        int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
+                                        const DeviceInfo& dev, cudaStream_t stream);
+// Weight scales [rows_total, cols/32] -> atoms [rows_total/128][cols/128][512].
+cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,
+                                     const DeviceInfo& dev, cudaStream_t stream);
+
 void set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse);
 size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev,
                                bool batched = false);

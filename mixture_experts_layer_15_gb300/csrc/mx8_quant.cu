@@ -1,0 +1,167 @@
+// MXFP8 quantisation of activation rows and the scale layout of the
+// block-scaled GEMMs.
+//
+// quantize_input (flashinfer_moe_ep.py, build_fi_mega_config), read as the
+// MX recipe of the e2m1 + ue8m0-per-32 weights applied to the activations:
+// every block of 32 consecutive values of a row shares the E8M0 scale
+// 2^(floor(log2 amax) - 8) (8 = E4M3's largest exponent; the byte kept in
+// 1..254), and each value becomes the E4M3 code nearest to value / scale
+// (ties to even, saturated at 448) -- cvt.rn.satfinite.e4m3 on the exact
+// power-of-two product. HBM-bound: one warp per row, 16-byte loads.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "gemm_mx8_kernel.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQThreads = 256;
+
+// ATOM = false: scales [rows, C/32] row-major. ATOM = true: the rows are
+// grouped (offsets, `groups` groups) and cut into token tiles of `bt` rows
+// per group; the scales go to the tile atoms the block-scaled GEMM reads
+// (tile t, k-block kb: atom t * (C/128) + kb; row n of the tile, chunk j at
+// byte (n % 32) * 16 + (n / 32) * 4 + j). Rows beyond offsets[groups] are
+// not touched; neither is anything when the groups need more than
+// `max_tiles` tiles.
+template <bool ATOM>
+__global__ void __launch_bounds__(kQThreads)
+mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint8_t* __restrict__ codes,
+                      uint8_t* __restrict__ scales, const int32_t* __restrict__ offsets, int groups, int bt,
+                      int rows_alloc, int max_tiles, int* err) {
+    __shared__ int s_offs[gemm::kMaxGroups + 1];
+    __shared__ int s_ttp[gemm::kMaxGroups + 1];
+    __shared__ int tmp[36];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int R = rows;
+    if (ATOM) {
+        for (int g = tid; g <= groups; g += kQThreads) {
+            int v = __ldg(offsets + g);
+            if (v < 0 || v > rows_alloc) { set_error(err, MOE_ERR_DEVICE_INDEX); v = v < 0 ? 0 : rows_alloc; }
+            s_offs[g] = v;
+        }
+        __syncthreads();
+        for (int g = tid; g < groups; g += kQThreads) {
+            const int cnt = s_offs[g + 1] - s_offs[g];
+            s_ttp[g] = cnt > 0 ? (cnt + bt - 1) / bt : 0;
+        }
+        __syncthreads();
+        const int ntiles = block_exclusive_scan(s_ttp, groups, tmp);
+        R = s_offs[groups];
+        if (ntiles > max_tiles) {                          // offsets not from a permute: touch nothing
+            if (tid == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
+            R = 0;
+        }
+    }
+    const int nkb = C / gemm::kMxBK;
+    const int nw = kQThreads / 32;
+    for (int p = blockIdx.x * nw + warp; p < R; p += gridDim.x * nw) {
+        int T = 0, n = 0;
+        if (ATOM) {
+            int lo = 0, hi = groups;                       // s_offs[lo] <= p < s_offs[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_offs[mid] <= p) lo = mid; else hi = mid;
+            }
+            const int local = p - s_offs[lo];
+            T = s_ttp[lo] + local / bt;
+            n = local % bt;
+        }
+        const __nv_bfloat16* xr = x + static_cast<size_t>(p) * C;
+        uint8_t* cr = codes + static_cast<size_t>(p) * C;
+        for (int c0 = 0; c0 < C; c0 += 256) {              // uniform over the warp
+            const int c = c0 + lane * 8;
+            const bool on = c < C;
+            float v[8];
+            if (on) {
+                Vec8<__nv_bfloat16>::load(xr + c, v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+            }
+            float am = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+            // a block of 32 = 4 lanes x 8 values
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            const uint32_t sb = gemm::mx8_scale_byte(__float_as_uint(am));
+            const float inv = gemm::mx8_inv_scale(sb);
+            if (on) {
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    lo |= static_cast<uint32_t>(gemm::e4m3_rn(v[i] * inv)) << (8 * i);
+                    hi |= static_cast<uint32_t>(gemm::e4m3_rn(v[4 + i] * inv)) << (8 * i);
+                }
+                *reinterpret_cast<uint2*>(cr + c) = make_uint2(lo, hi);
+                if ((lane & 3) == 0) {
+                    if (ATOM)
+                        scales[(static_cast<size_t>(T) * nkb + c / gemm::kMxBK) * gemm::kAtom +
+                               gemm::atom_byte(n, (c % gemm::kMxBK) / 32)] = static_cast<uint8_t>(sb);
+                    else
+                        scales[static_cast<size_t>(p) * (C / 32) + c / 32] = static_cast<uint8_t>(sb);
+                }
+            }
+        }
+    }
+}
+
+// Scales [rows_total, cols/32] (row-major, one byte per 32 values) -> the
+// atoms [rows_total/128][cols/128][512] of the block-scaled GEMM: row r of
+// tile r/128, k-block kb: its four bytes (chunks 0..3) at byte
+// (r % 32) * 16 + ((r % 128) / 32) * 4 of atom (r/128, kb).
+__global__ void mx_prepare_scales_kernel(const uint8_t* __restrict__ sc, long long rows_total, int cols,
+                                         uint8_t* __restrict__ out) {
+    const int nkb = cols / gemm::kMxBK;
+    const long long total = rows_total * nkb;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = i / nkb;
+        const int kb = static_cast<int>(i % nkb);
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sc + row * (cols / 32) + kb * 4);
+        const int r = static_cast<int>(row % gemm::kBM);
+        *reinterpret_cast<uint32_t*>(out + ((row / gemm::kBM) * nkb + kb) * gemm::kAtom + (r & 31) * 16 +
+                                     ((r >> 5) << 2)) = w;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
+                                  const DeviceInfo& dev, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    const int nw = kQThreads / 32;
+    int grid = (rows + nw - 1) / nw;
+    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    return launch_pdl(mxfp8_quantize_kernel<false>, dim3(grid), dim3(kQThreads), 0, s,
+                      static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
+                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err);
+}
+
+cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
+                                        int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
+                                        const DeviceInfo& dev, cudaStream_t s) {
+    const int nw = kQThreads / 32;
+    int grid = (rows_alloc + nw - 1) / nw;
+    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    if (grid < 1) grid = 1;
+    return launch_pdl(mxfp8_quantize_kernel<true>, dim3(grid), dim3(kQThreads), 0, s,
+                      static_cast<const __nv_bfloat16*>(x), rows_alloc, C, codes, atoms, offsets, groups, bt,
+                      rows_alloc, max_tiles, err);
+}
+
+cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,
+                                     const DeviceInfo& dev, cudaStream_t s) {
+    const long long total = rows_total * (cols / gemm::kMxBK);
+    if (total == 0) return cudaSuccess;
+    long long grid = (total + 255) / 256;
+    if (grid > 16LL * dev.sm_count) grid = 16LL * dev.sm_count;
+    mx_prepare_scales_kernel<<<static_cast<int>(grid), 256, 0, s>>>(scales, rows_total, cols, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

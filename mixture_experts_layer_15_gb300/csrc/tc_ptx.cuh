@@ -241,5 +241,65 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
     return r != 0;
 }
 
+// ---- block-scaled MMA (kind::mxf8f6f4) ------------------------------------------------
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size a
+// multiple of 16), completion as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// D[tmem] (+)= (A * sA) (B * sB)^T with one E8M0 scale per 32 reduction
+// elements of each row of A and B (scale_vec::1X), K = 32 per instruction.
+// The scales are read from TMEM at sfa / sfb (even column addresses); the
+// instruction descriptor's scale ids pick the byte of each 32-bit scale word.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Element formats of kind::mxf8f6f4 operands.
+enum { MX_E4M3 = 0, MX_E2M1 = 5 };
+
+// Instruction descriptor, kind::mxf8f6f4 with E8M0 scales: fp32 accumulator,
+// A and B K-major, shape M x N; `sf_id` (0..3) selects byte sf_id of the A
+// and B scale words, i.e. the 32-element chunk of a 128-element k-block.
+__host__ __device__ constexpr uint32_t idesc_mx(int atype, int btype, int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4)            // B scale id
+           | (static_cast<uint32_t>(atype) << 7)          // A format
+           | (static_cast<uint32_t>(btype) << 10)         // B format
+           | (static_cast<uint32_t>(N >> 3) << 17)        // N / 8
+           | (1u << 23)                                   // scale format: E8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)        // M / 16
+           | (static_cast<uint32_t>(sf_id) << 29);        // A scale id
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte block stored row after row
+// (no swizzle: 8-row core matrices of 128 bytes, 128 bytes apart).
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Copy a 512-byte scale atom from shared memory into TMEM columns
+// taddr .. taddr+3: row r (16 bytes) goes to lane r of each of the four
+// 32-lane subpartitions (32x128b, replicated .warpx4). Issued by one thread;
+// ordered before the MMAs this thread issues after it.
+__device__ __forceinline__ void tmem_copy_atom(uint32_t taddr, uint32_t saddr) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(rows16_desc(saddr))
+                 : "memory");
+}
+
 }  // namespace ptx
 }  // namespace moe

@@ -45,6 +45,10 @@ class MoELayer:
     default: see the precision notes of the C ABI). ``fused_finalize`` (f32
     output only) folds the finalize into GEMM2 (moe_experts_fused_finalize):
     no gemm2_permuted round trip, the top-k reduction order is not fixed.
+    With ``fmt`` = MOE_WEIGHTS_MXFP4_A8 the MXFP4 weights are given as for
+    MOE_WEIGHTS_MXFP4 (codes + row-major E8M0 scales); the layer rearranges
+    the scales once (moe_mx_prepare_scales) and the experts run with MXFP8
+    activations on the block-scaled tensor cores.
     """
 
     def __init__(self, *, K, N, E, top_k, w1, w2, w1_scale=None, w2_scale=None,
@@ -69,8 +73,18 @@ class MoELayer:
             raise ValueError("fused_finalize accumulates into an f32 output")
         self.fused_finalize = bool(fused_finalize)
         act = {"silu": L.MOE_ACT_SILU, "gelu": L.MOE_ACT_GELU}[activation]
+        if fmt == L.MOE_WEIGHTS_MXFP4_A8:
+            w1_scale = self._prepare_scales(w1_scale, 2 * N, K)
+            w2_scale = self._prepare_scales(w2_scale, K, N)
+            self.w1_scale, self.w2_scale = w1_scale, w2_scale
         self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale, act, activation_clamp)
         self._bufs = {}
+
+    def _prepare_scales(self, scales, rows, cols):
+        out = torch.empty(L.moe_mx_prepared_scales_size(self.E_local, rows, cols), dtype=torch.uint8,
+                          device=scales.device)
+        L.moe_mx_prepare_scales(scales, self.E_local, rows, cols, out)
+        return out
 
     def buffers(self, M: int) -> Buffers:
         b = self._bufs.get(M)

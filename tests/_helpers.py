@@ -57,13 +57,14 @@ class ExpertsF64:
 
 
 def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None, rsf=1.0, activation="silu",
-                  clamp=None):
+                  clamp=None, qdq=None):
     """Oracle output rows for ``tokens`` (and the expert output y of each of
     their routes): the experts and finalize of the oracle applied to the
     sub-problem made of those tokens' routes.
 
     x: float64 [M, K]; ids int [M, k]; weights float64 [M, k]; w1/w2 indexable
-    per local expert; shared: float64 [M, K] or None.
+    per local expert; shared: float64 [M, K] or None; qdq: the activations'
+    quantisation (oracle.expert_mlp), or None.
     Returns (out [T, K], y dict {(t, j): [K]}).
     """
     tokens = list(tokens)
@@ -80,7 +81,7 @@ def oracle_tokens(x, ids, weights, w1, w2, tokens, expert_map=None, shared=None,
     ys = {}
     for le, routes in by_expert.items():
         xt = x[[tokens[a] for a, _ in routes]]
-        y = O.expert_mlp(xt, w1[le], w2[le], activation, clamp)
+        y = O.expert_mlp(xt, w1[le], w2[le], activation, clamp, qdq)
         for r, (a, j) in enumerate(routes):
             ys[(a, j)] = y[r]
     # sub-problem gemm2 rows and map, then the oracle's finalize

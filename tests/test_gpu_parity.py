@@ -276,7 +276,7 @@ def test_bounded_wait_gives_up_and_reports(moe):
 # ------------------------------------------------------------------ whole layer
 
 def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False,
-                 activation="silu", clamp=None):
+                 activation="silu", clamp=None, a8=False):
     cfg = synth.CONFIGS[name]
     li = layer_inputs(name)
     x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
@@ -295,6 +295,8 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
         kw.update(fused_finalize=True)
     if activation != "silu" or clamp is not None:
         kw.update(activation=activation, activation_clamp=clamp)
+    if a8:                        # MXFP4 weights x MXFP8 activations (block-scaled MMAs)
+        kw.update(fmt=moe.MOE_WEIGHTS_MXFP4_A8)
     layer = make_layer(moe, name, li, **kw)
     b = layer.forward(x, logits)
     torch.cuda.synchronize()
@@ -318,16 +320,19 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
     else:
         toks = sample_tokens(M, sample or 256)
     xs = x.to(torch.float64).cpu().numpy()
+    # the oracle dequantises the row-major scale bytes (the A8 layer keeps its
+    # rearranged copy to itself)
     w1 = ExpertsF64(kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale))
     w2 = ExpertsF64(kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale))
     shared = None
     if li.ws1 is not None:
         shared = np.zeros((M, cfg.K))
         shared[toks] = O.shared_expert(xs[toks], li.ws1.double().cpu().numpy(), li.ws2.double().cpu().numpy())
-    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared, activation=activation, clamp=clamp)
+    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared, activation=activation, clamp=clamp,
+                            qdq=O.mxfp8_qdq if a8 else None)
     got = b.out.double().cpu().numpy()[toks]
     g2 = b.gemm2.double().cpu().numpy()
-    rel = 3e-2 if cfg.weight_format == "mxfp4" else 1e-2
+    rel = 3e-2 if (cfg.weight_format == "mxfp4" and not a8) else 1e-2
     abs_ = 0.0 if cfg.weight_format == "mxfp4" else 1e-3
     if bf16_storage:
         refb = O.bf16_round(ref).astype(np.float64)
