@@ -143,7 +143,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg_name, device, only_m=None, experts=0):
+def make_workload(cfg_name, device, only_m=None, experts=0, mxfp8_act=False):
     import dataclasses
     import mixture_experts_layer_15_gb300 as moe
     cfg = synth.CONFIGS[cfg_name]
@@ -154,6 +154,8 @@ def make_workload(cfg_name, device, only_m=None, experts=0):
         cfg = dataclasses.replace(cfg, **kw)
     li = synth.make_layer(cfg, device)
     fmt = moe.MOE_WEIGHTS_MXFP4 if cfg.weight_format == "mxfp4" else moe.MOE_WEIGHTS_BF16
+    if mxfp8_act and cfg.weight_format == "mxfp4":
+        fmt = moe.MOE_WEIGHTS_MXFP4_A8
     layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
                          w1_scale=li.w1_scale, w2_scale=li.w2_scale, fmt=fmt,
                          route="softmax" if cfg.route == "softmax" else "sigmoid",
@@ -187,9 +189,11 @@ def launches_per_forward(moe, cfg, layer, M, finalize="fused"):
     return n
 
 
-def roofline_layer(cfg, M, touched, pk, sustained=True):
+def roofline_layer(cfg, M, touched, pk, sustained=True, routed_mult=1.0):
     """Slower of touched-expert weight bytes at HBM bandwidth and FLOPs at
-    the bf16 tensor peak; returns (seconds, bytes, flops)."""
+    the bf16 tensor peak (the routed experts' FLOPs at routed_mult x that
+    peak: 2, the nominal fp8 : bf16 ratio, for MXFP8 activations); returns
+    (seconds, bytes, flops, tensor seconds)."""
     bpw = 2.0 if cfg.weight_format == "bf16" else (0.5 + 1.0 / 32.0)
     wbytes = touched * 3.0 * cfg.K * cfg.N * bpw
     flops = 6.0 * cfg.K * cfg.N * M * cfg.top_k
@@ -197,7 +201,9 @@ def roofline_layer(cfg, M, touched, pk, sustained=True):
         wbytes += 3.0 * cfg.K * cfg.shared_N * 2.0
         flops += 6.0 * cfg.K * cfg.shared_N * M
     tc = (pk["bf16_sus"] if sustained else pk["bf16"]) * 1e12
-    return max(wbytes / (pk["hbm"] * 1e9), flops / tc), wbytes, flops
+    fr = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+    t_tc = fr / (tc * routed_mult) + (flops - fr) / tc
+    return max(wbytes / (pk["hbm"] * 1e9), t_tc), wbytes, flops, t_tc
 
 
 def make_forward(moe, cfg, layer, batches, stream, finalize="fused"):
@@ -332,14 +338,15 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
                 torch.cuda.synchronize()
                 acc.append(e0.elapsed_time(e1) / 1e3)
         tm, tgm = statistics.median(tf), statistics.median(tg)
-        troof, wbytes, flops = roofline_layer(cfg, M, touched[M], pk)
+        mult = 2.0 if layer.fmt == moe.MOE_WEIGHTS_MXFP4_A8 else 1.0
+        troof, wbytes, flops, t_tc = roofline_layer(cfg, M, touched[M], pk, routed_mult=mult)
         gf = 6.0 * cfg.K * cfg.N * M * cfg.top_k
         gemm_flops += gf
         gemm_secs += tgm
         rec = {"M": M, "tokens_per_s": M / tm, "ms": tm * 1e3, "gemm_ms": tgm * 1e3,
                "touched_experts": touched[M], "roofline_ms": troof * 1e3,
                "roofline_frac": troof / tm,
-               "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= flops / (pk["bf16_sus"] * 1e12) else "tensor",
+               "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= t_tc else "tensor",
                "gemm_tflops": gf / tgm / 1e12}
         if M <= graph_max_m:
             tgr, err = graph_time(forward, M, stream, scrub, reps)
@@ -467,9 +474,72 @@ def next_rows(moe, pk, dev, stream):
                                "bound": "tensor"}]
     del xb, counts, yb, wsb
     del li, x, logits, batches
+    torch.cuda.empty_cache()
+    out["mxfp8_activations"] = a8_rows(moe, pk, dev, stream, scrub)
     del buf
     torch.cuda.empty_cache()
     return out
+
+
+def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192)):
+    """The DeepSeek-shaped layer with its MXFP4 routed experts on MXFP8
+    activations (block-scaled MMAs, MOE_WEIGHTS_MXFP4_A8) beside the same
+    layer on bf16 activations: the whole forward (route + permute, shared
+    expert, experts with the folded finalize) per M, median of 20 scrubbed
+    runs, and the experts step alone. Roofline: touched weight bytes at HBM
+    bandwidth vs FLOPs at the tensor peak of each path's MMAs (the routed
+    experts at the fp8 peak = measured bf16 sustained x 2, the nominal
+    fp8 : bf16 ratio, on the A8 path; bf16 otherwise; the shared expert bf16)."""
+    cfg = synth.CONFIGS["deepseek"]
+    li = synth.make_layer(cfg, dev)
+    batches = {M: synth.make_tokens(cfg, M, dev, li) for M in sweep}
+    rows = []
+    for fmt, tag in ((moe.MOE_WEIGHTS_MXFP4, "bf16 activations (decode to bf16, kind::f16)"),
+                     (moe.MOE_WEIGHTS_MXFP4_A8, "MXFP8 activations (kind::mxf8f6f4 block-scaled)")):
+        layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
+                             w1_scale=li.w1_scale, w2_scale=li.w2_scale, fmt=fmt, route="sigmoid",
+                             score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                             routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2)
+        fwd = make_forward(moe, cfg, layer, batches, stream, "fused")
+        for M in sweep:
+            for _ in range(3):
+                fwd(M)
+        torch.cuda.synchronize()
+        for M in sweep:
+            tf, tg = [], []
+            for _ in range(20):
+                for which, acc in ((0, tf), (1, tg)):
+                    scrub()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    if which == 0:
+                        e0.record(stream)
+                        fwd(M)
+                        e1.record(stream)
+                    else:
+                        fwd(M, (e0, e1))
+                    torch.cuda.synchronize()
+                    acc.append(e0.elapsed_time(e1) / 1e3)
+            t, tgm = statistics.median(tf), statistics.median(tg)
+            touched = int((layer.buffers(M).offsets.diff() > 0).sum().item())
+            wbytes = touched * 3.0 * cfg.K * cfg.N * (0.5 + 1.0 / 32.0) + 3.0 * cfg.K * cfg.shared_N * 2.0
+            fr = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+            fs = 6.0 * cfg.K * cfg.shared_N * M
+            p_routed = pk["bf16_sus"] * (2.0 if fmt == moe.MOE_WEIGHTS_MXFP4_A8 else 1.0) * 1e12
+            t_tc = fr / p_routed + fs / (pk["bf16_sus"] * 1e12)
+            t_hbm = wbytes / (pk["hbm"] * 1e9)
+            troof = max(t_tc, t_hbm)
+            rows.append({"workload": f"deepseek-shaped layer, M={M}, {tag}", "M": M, "ms": t * 1e3,
+                         "experts_ms": tgm * 1e3, "experts_tflops": fr / tgm / 1e12,
+                         "tokens_per_s": M / t, "roofline_ms": troof * 1e3, "frac": troof / t,
+                         "bound": "hbm" if t_hbm >= t_tc else "tensor"})
+        st = moe.moe_get_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the MXFP8 rows: {moe.status_string(st)}")
+        del layer, fwd
+        torch.cuda.empty_cache()
+    del li, batches
+    torch.cuda.empty_cache()
+    return rows
 
 
 def run_gpu(args):
@@ -478,7 +548,7 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     stream = torch.cuda.current_stream()
-    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts)
+    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts, args.mxfp8_act)
     sweep = sorted(batches)
     forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
     warm_up(moe, layer, sweep, forward, args.warmup)
@@ -491,7 +561,7 @@ def run_gpu(args):
     achieved = gemm_flops / gemm_secs / 1e12
     traffic = tcase = talg = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath) and not (args.m or args.experts) and args.finalize == "fused":
+    if os.path.exists(tpath) and not (args.m or args.experts or args.mxfp8_act) and args.finalize == "fused":
         try:
             t = json.load(open(tpath)).get(args.config) or {}
             traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
@@ -525,7 +595,7 @@ def run_gpu(args):
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(cfg, li, batches, args)
-        if args.others and not args.m and not args.experts:
+        if args.others and not args.m and not args.experts and not args.mxfp8_act:
             del layer, batches
             torch.cuda.empty_cache()
             line["other_configs"] = {name: other_config(moe, name, args, pk, dev, stream)
@@ -720,6 +790,9 @@ def main():
                     help="other configs measured after the headline one and reported beside it ('' = none)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: keep the first N experts of the config (not the benchmark workload)")
+    ap.add_argument("--mxfp8-act", action="store_true",
+                    help="profiling only: MXFP4 configs run their experts on MXFP8 activations "
+                         "(MOE_WEIGHTS_MXFP4_A8; not the benchmark workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
