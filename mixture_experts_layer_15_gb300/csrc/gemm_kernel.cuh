@@ -680,13 +680,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     const uint32_t sA0 = MX ? sbase + C::OFF_DEC + dstage * C::DSTAGE_BYTES : st;
                     const uint32_t sB = st + C::B_OFF;
+                    // step kk starts 32 bytes further into each 128-byte row: +2 in the
+                    // descriptors' 16-byte address field (tiles are 1024-byte aligned)
+                    const uint64_t dA0 = sw128_kmajor_desc(sA0), dB = sw128_kmajor_desc(sB);
+                    const uint64_t dA1 = sw128_kmajor_desc(sA0 + C::A_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bdesc = sw128_kmajor_desc(sB + kk * 32);
                         const uint32_t acc = (kb > un.kb0 || kk > 0) ? 1u : 0u;
-                        mma_f16(d, sw128_kmajor_desc(sA0 + kk * 32), bdesc, idesc, acc);
-                        if (NA == 2)
-                            mma_f16(d + BT, sw128_kmajor_desc(sA0 + C::A_BYTES + kk * 32), bdesc, idesc, acc);
+                        mma_f16(d, dA0 + 2 * kk, dB + 2 * kk, idesc, acc);
+                        if (NA == 2) mma_f16(d + BT, dA1 + 2 * kk, dB + 2 * kk, idesc, acc);
                     }
                     mma_commit(empty_bar(stage));            // ring slot free once these MMAs finish
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }

@@ -296,22 +296,27 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + buf * C::ACC_COLS;
+                // the chunk-kk instruction descriptor is idesc0 with scale id kk in both id fields
+                const uint32_t idesc0 = idesc_mx(MX_E2M1, MX_E4M3, kBM, un.ncols, 0);
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
                     const uint32_t sf = tmem_base + C::SF_BASE + stage * C::SF_COLS;
-                    tmem_copy_atom(sf, st + C::OFF_SF);                    // A0 scales: columns sf .. sf+3
-                    tmem_copy_atom(sf + 4, st + C::OFF_SF + kAtom);        // A1 scales
-                    tmem_copy_atom(sf + 8, st + C::OFF_SF + 2 * kAtom);    // B scales
-                    const uint32_t sA0 = st, sA1 = st + C::A_BYTES, sB = st + 2 * C::A_BYTES;
+                    const uint64_t dsf = rows16_desc(st + C::OFF_SF);       // atoms 512 bytes apart: +32
+                    tmem_copy_atom(sf, dsf);                                // A0 scales: columns sf .. sf+3
+                    tmem_copy_atom(sf + 4, dsf + kAtom / 16);               // A1 scales
+                    tmem_copy_atom(sf + 8, dsf + 2 * kAtom / 16);           // B scales
+                    // chunk kk starts 32 bytes further into each 128-byte row: +2 in the
+                    // descriptors' 16-byte address field
+                    const uint64_t dA0 = sw128_kmajor_desc(st), dA1 = sw128_kmajor_desc(st + C::A_BYTES);
+                    const uint64_t dB = sw128_kmajor_desc(st + 2 * C::A_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kMxBK / 32; ++kk) {
-                        const uint32_t idesc = idesc_mx(MX_E2M1, MX_E4M3, kBM, un.ncols, kk);
-                        const uint64_t bdesc = sw128_kmajor_desc(sB + kk * 32);
+                        const uint32_t idesc = idesc0 | (static_cast<uint32_t>(kk) << 4) | (static_cast<uint32_t>(kk) << 29);
                         const uint32_t acc = (kb > un.kb0 || kk > 0) ? 1u : 0u;
-                        mma_mx(d, sw128_kmajor_desc(sA0 + kk * 32), bdesc, idesc, sf, sf + 8, acc);
-                        mma_mx(d + BT, sw128_kmajor_desc(sA1 + kk * 32), bdesc, idesc, sf + 4, sf + 8, acc);
+                        mma_mx(d, dA0 + 2 * kk, dB + 2 * kk, idesc, sf, sf + 8, acc);
+                        mma_mx(d + BT, dA1 + 2 * kk, dB + 2 * kk, idesc, sf + 4, sf + 8, acc);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }

@@ -212,10 +212,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     tc_fence_after();
                     const uint32_t sA = sbase + stage * C::STAGE_BYTES;
                     const uint32_t sB = sA + C::A_BYTES;
+                    // step kk: +32 bytes, +2 in the descriptors' 16-byte address field
+                    const uint64_t dA = sw128_kmajor_desc(sA), dB = sw128_kmajor_desc(sB);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint32_t acc = (kb > un.kb0 || kk > 0) ? 1u : 0u;
-                        mma_f16_pair(d, sw128_kmajor_desc(sA + kk * 32), sw128_kmajor_desc(sB + kk * 32), idesc, acc);
+                        mma_f16_pair(d, dA + 2 * kk, dB + 2 * kk, idesc, acc);
                     }
                     mma_commit_pair(empty_bar(stage), 0x3);   // both CTAs' ring slots free
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }

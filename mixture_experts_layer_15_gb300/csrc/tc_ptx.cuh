@@ -292,13 +292,12 @@ __device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
     return d;
 }
 
-// Copy a 512-byte scale atom from shared memory into TMEM columns
-// taddr .. taddr+3: row r (16 bytes) goes to lane r of each of the four
-// 32-lane subpartitions (32x128b, replicated .warpx4). Issued by one thread;
-// ordered before the MMAs this thread issues after it.
-__device__ __forceinline__ void tmem_copy_atom(uint32_t taddr, uint32_t saddr) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(rows16_desc(saddr))
-                 : "memory");
+// Copy a 512-byte scale atom, given by its rows16_desc, from shared memory
+// into TMEM columns taddr .. taddr+3: row r (16 bytes) goes to lane r of each
+// of the four 32-lane subpartitions (32x128b, replicated .warpx4). Issued by
+// one thread; ordered before the MMAs this thread issues after it.
+__device__ __forceinline__ void tmem_copy_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 }  // namespace ptx
