@@ -31,10 +31,16 @@
 // warp's 32 lanes hold 32 consecutive features of a token, which is one MX
 // block of GEMM2's reduction, so its scale is one warp max-reduction.
 //
-// CTA warps (persistent, one CTA per SM): warp 0 TMA producer, warp 1 TMEM
-// allocator + MMA/scale-copy issuer, warps 2..9 epilogue. TMEM holds the
-// accumulators (double-buffered when they leave room) and, per ring stage,
-// twelve scale columns (A0, A1, B atoms).
+// CTA warps (persistent, one CTA per SM): warp 0 TMA producer; warps 1 and
+// 2 the MMA issuers, one per A tile (warp 1 also allocates TMEM); warps
+// 3..10 epilogue. One thread issuing every MMA and scale copy of a k-block
+// bounds the kernel (its issue rate, not the tensor pipe, sets the pace at
+// these tile shapes), so each A tile has its own issuing thread: it copies
+// its A atom and its own copy of the B atom (a copy by one thread is not
+// ordered before another thread's MMAs) and commits to the ring and
+// accumulator barriers, which count both. TMEM holds the accumulators
+// (double-buffered when they leave room) and, per ring stage and issuer,
+// eight scale columns (its A atom, its B atom).
 #pragma once
 
 #include <cuda_fp8.h>
@@ -51,7 +57,8 @@ template <int BT>
 struct Cfg8 {
     static constexpr int EPI_WARPS = 8;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-    static constexpr int THREADS = 64 + EPI_THREADS;
+    static constexpr int THREADS = 96 + EPI_THREADS;
+    static constexpr int ISSUERS = 2;                      // MMA-issuing warps (one per A tile)
     static constexpr int A_BYTES = kBM * kMxBK;            // padded e2m1 tile in shared memory
     static constexpr int A_TX = kBM * kMxBK / 2;           // its transaction bytes (packed codes)
     static constexpr int B_BYTES = BT * kMxBK;
@@ -60,7 +67,7 @@ struct Cfg8 {
     static constexpr int STAGE_TX = 2 * A_TX + B_BYTES + 3 * kAtom;
     static constexpr int STAGES_FIT = (kSmemBudget - 20 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int SF_COLS = 12;                     // TMEM scale columns per stage
+    static constexpr int SF_COLS = 16;                     // TMEM scale columns per stage (8 per issuer)
     static constexpr int ACC_COLS = 2 * BT;
     static constexpr int NBUF = (2 * ACC_COLS + STAGES * SF_COLS <= 512) ? 2 : 1;
     static constexpr int SF_BASE = NBUF * ACC_COLS;
@@ -198,13 +205,13 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), C::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
+            mbar_init(tfull_bar(b), C::ISSUERS);
             mbar_init(tempty_bar(b), kEpiThreads);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar, C::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -282,8 +289,9 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ================= scale copies + MMA issuer =================
+    } else if (warp <= C::ISSUERS) {
+        // ================= scale copies + MMA issuers (warp 1: A0, warp 2: A1) =================
+        const int h = warp - 1;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -295,28 +303,27 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a.err)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + buf * C::ACC_COLS;
+                const uint32_t d = tmem_base + buf * C::ACC_COLS + h * BT;
                 // the chunk-kk instruction descriptor is idesc0 with scale id kk in both id fields
                 const uint32_t idesc0 = idesc_mx(MX_E2M1, MX_E4M3, kBM, un.ncols, 0);
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = sbase + stage * C::STAGE_BYTES;
-                    const uint32_t sf = tmem_base + C::SF_BASE + stage * C::SF_COLS;
+                    // this issuer's columns: its A atom at sf, its copy of the B atom at sf + 4
+                    const uint32_t sf = tmem_base + C::SF_BASE + stage * C::SF_COLS + 8 * h;
                     const uint64_t dsf = rows16_desc(st + C::OFF_SF);       // atoms 512 bytes apart: +32
-                    tmem_copy_atom(sf, dsf);                                // A0 scales: columns sf .. sf+3
-                    tmem_copy_atom(sf + 4, dsf + kAtom / 16);               // A1 scales
-                    tmem_copy_atom(sf + 8, dsf + 2 * kAtom / 16);           // B scales
+                    tmem_copy_atom(sf, dsf + h * (kAtom / 16));             // A_h scales: columns sf .. sf+3
+                    tmem_copy_atom(sf + 4, dsf + 2 * kAtom / 16);           // B scales
                     // chunk kk starts 32 bytes further into each 128-byte row: +2 in the
                     // descriptors' 16-byte address field
-                    const uint64_t dA0 = sw128_kmajor_desc(st), dA1 = sw128_kmajor_desc(st + C::A_BYTES);
+                    const uint64_t dA = sw128_kmajor_desc(st + h * C::A_BYTES);
                     const uint64_t dB = sw128_kmajor_desc(st + 2 * C::A_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kMxBK / 32; ++kk) {
                         const uint32_t idesc = idesc0 | (static_cast<uint32_t>(kk) << 4) | (static_cast<uint32_t>(kk) << 29);
                         const uint32_t acc = (kb > un.kb0 || kk > 0) ? 1u : 0u;
-                        mma_mx(d, dA0 + 2 * kk, dB + 2 * kk, idesc, sf, sf + 8, acc);
-                        mma_mx(d + BT, dA1 + 2 * kk, dB + 2 * kk, idesc, sf + 4, sf + 8, acc);
+                        mma_mx(d, dA + 2 * kk, dB + 2 * kk, idesc, sf, sf + 4, acc);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -330,11 +337,11 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         }
         __syncwarp();
     } else {
-        // ================= epilogue (warps 2..9) =================
+        // ================= epilogue (warps 3..10) =================
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        const int etid = tid - 64;
-        const int c_first = 16 * ((warp - 2) >> 2);
+        const int etid = tid - 96;
+        const int c_first = 16 * ((warp - 3) >> 2);
         constexpr int c_step = 16 * (C::EPI_WARPS / 4);
         auto emit = [&](const Unit& un, int c0, const float (&v0)[16], const float (&v1)[16]) {
             if (MODE == MODE_SWIGLU) emit16_swiglu_mx8(un, m, q, lane, c0, tile_index(un), v0, v1);
