@@ -24,8 +24,9 @@
 // CTA warps, persistent (one CTA per SM):
 //   warp 0     TMA producer: A, B tiles of 64 reduction elements into a
 //              shared-memory ring (full/empty mbarriers);
-//   warp 1     TMEM allocator and MMA issuer (one thread), commits free ring
-//              slots and signals finished accumulators;
+//   warps 1..NA TMEM allocation (warp 1) and the MMA issuers, one thread per
+//              A tile of the unit, each committing free ring slots and
+//              finished accumulators (the barriers count every issuer);
 //   epilogue   8 warps (bf16 weights) or 4 (MXFP4): tcgen05.ld of the
 //              accumulators (warp w reads TMEM lanes 32*(w%4)..; with 8 warps
 //              the two warps of a lane quarter take alternate 16-column
@@ -143,7 +144,11 @@ struct KernelArgs {
 
 template <int BT, int NA, bool MX>
 struct Cfg {
-    static constexpr int THREADS = 64 + Warps<MX>::EPI_THREADS + Warps<MX>::CONV_THREADS;
+    // warp 0 producer, warps 1..NA one MMA issuer per A tile, then the epilogue
+    // (and converter) warps
+    static constexpr int ISSUERS = NA;
+    static constexpr int EPI_WARP0 = 1 + NA;
+    static constexpr int THREADS = 32 * EPI_WARP0 + Warps<MX>::EPI_THREADS + Warps<MX>::CONV_THREADS;
     static constexpr int A_BYTES = kBM * kBK * 2;                 // bf16 A tile (TMA'd or decoded)
     static constexpr int RAW_BYTES = kBM * kBK / 2;               // packed e2m1 A tile
     static constexpr int SC_BYTES = kBM * 16;                     // scale tile: 8 k-blocks of scales
@@ -468,17 +473,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             mbar_init(full_bar(s), 1);
             // MXFP4: the converters release the packed tile, the MMA the B tile
             // MXFP4: one arrival per converter warp frees the packed tile, the MMA the B tile
-            mbar_init(empty_bar(s), MX ? 1 + kConvThreads / 32 : 1);
+            mbar_init(empty_bar(s), MX ? C::ISSUERS + kConvThreads / 32 : C::ISSUERS);
         }
         for (int d = 0; d < C::DSTAGES; ++d) {
             mbar_init(dfull_bar(d), kConvThreads / 32);
-            mbar_init(dempty_bar(d), 1);
+            mbar_init(dempty_bar(d), C::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
+            mbar_init(tfull_bar(b), C::ISSUERS);
             mbar_init(tempty_bar(b), kEpiThreads);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar, C::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA0);
@@ -657,8 +662,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
+    } else if (warp <= C::ISSUERS) {
+        // ================= MMA issuers: warp 1 + h issues A tile h's MMAs =================
+        // (one thread issuing every MMA of a k-block set the pace at mid-size
+        // tiles; each issuer commits to the ring, decoded-ring, accumulator and
+        // drain barriers, which count every issuer)
+        const int h = warp - 1;
         if (lane == 0) {
             int stage = 0, dstage = 0;
             uint32_t phase = 0, dphase = 0;
@@ -672,7 +681,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a0.err)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + buf * C::ACC_COLS;
+                const uint32_t d = tmem_base + buf * C::ACC_COLS + h * BT;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, a0.err)) { ok = false; break; }
                     if (MX && !wait_bar(dfull_bar(dstage), dphase, abort_flag, a0.err)) { ok = false; break; }
@@ -682,13 +691,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     const uint32_t sB = st + C::B_OFF;
                     // step kk starts 32 bytes further into each 128-byte row: +2 in the
                     // descriptors' 16-byte address field (tiles are 1024-byte aligned)
-                    const uint64_t dA0 = sw128_kmajor_desc(sA0), dB = sw128_kmajor_desc(sB);
-                    const uint64_t dA1 = sw128_kmajor_desc(sA0 + C::A_BYTES);
+                    const uint64_t dA = sw128_kmajor_desc(sA0 + h * C::A_BYTES), dB = sw128_kmajor_desc(sB);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint32_t acc = (kb > un.kb0 || kk > 0) ? 1u : 0u;
-                        mma_f16(d, dA0 + 2 * kk, dB + 2 * kk, idesc, acc);
-                        if (NA == 2) mma_f16(d + BT, dA1 + 2 * kk, dB + 2 * kk, idesc, acc);
+                        mma_f16(d, dA + 2 * kk, dB + 2 * kk, idesc, acc);
                     }
                     mma_commit(empty_bar(stage));            // ring slot free once these MMAs finish
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -706,12 +713,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {}
         }
         __syncwarp();
-    } else if (warp < 2 + kEpiWarps) {
-        // ================= epilogue (warps 2..9) =================
+    } else if (warp < C::EPI_WARP0 + kEpiWarps) {
+        // ================= epilogue (the warps after the issuers) =================
         const int q = warp & 3;                              // TMEM lanes 32q..32q+31
         const int row_in_tile = q * 32 + lane;
-        const int etid = tid - 64;
-        const int c_first = 16 * ((warp - 2) >> 2);          // this warp's first 16-column chunk
+        const int etid = tid - 32 * C::EPI_WARP0;
+        const int c_first = 16 * ((warp - C::EPI_WARP0) >> 2);   // this warp's first 16-column chunk
         constexpr int c_step = 16 * (kEpiWarps / 4);
         // one unit's outputs from the accumulator values v0/v1 of columns [c0, c0+16)
         auto emit = [&](int ph, const Unit& un, const GemmArgs& a, int c0, const float (&v0)[16],
@@ -822,7 +829,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         // ================= converters (MXFP4 only: the warps after the epilogue) =================
         // two threads per weight row: h = 0 decodes elements 0..31 of the
         // k-block, h = 1 elements 32..63, each with its own scale byte
-        const int ct = tid - 64 - kEpiThreads;
+        const int ct = tid - 32 * C::EPI_WARP0 - kEpiThreads;
         const int r = ct >> 1, h = ct & 1;
         int stage = 0, dstage = 0;
         uint32_t phase = 0, dphase = 0;
