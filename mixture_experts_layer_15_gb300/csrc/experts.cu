@@ -74,14 +74,18 @@ struct PlanOverride {
 };
 PlanOverride g_override;
 
-// Token tile: about twice the average rows per group (a group never holds
-// more than M rows: a token routes to an expert once), at least 32. 256-row
-// tiles fill all 512 TMEM columns, which leaves the epilogue unoverlapped; they
-// pay off only when work units are long (both reductions >= 4096) or when each
-// decoded MXFP4 weight tile should serve as many tokens as possible.
+// Token tile: about twice the average rows per group, four times with 64 or
+// more groups (a group never holds more than M rows: a token routes to an
+// expert once), at least 32. With many experts the load per expert is
+// heavy-tailed, and a busy expert cut into several tiles streams its weights
+// once per tile. 256-row tiles fill all 512 TMEM columns, which leaves the
+// epilogue unoverlapped; they pay off only when work units are long (both
+// reductions >= 4096) or when each decoded MXFP4 weight tile should serve as
+// many tokens as possible.
 int pick_bt(int M, int rows_alloc, int groups, int K, int N, bool mx) {
     const int avg = (rows_alloc + groups - 1) / (groups > 0 ? groups : 1);
-    const int want = avg * 2 < M ? avg * 2 : M;
+    const int mult = groups >= 64 ? 4 : 2;
+    const int want = avg * mult < M ? avg * mult : M;
     const int cap = (mx || (K >= 4096 && N >= 4096)) ? 256 : 128;
     int bt = 32;
     while (bt < want && bt < cap) bt <<= 1;
