@@ -127,3 +127,32 @@ def test_workspace_sizes_are_host_computable(moe):
     assert moe.moe_permute_workspace_size(16, 2, 8) == 0     # one chunk: no scratch
     assert moe.moe_permute_workspace_size(8192, 8, 128) > 0
     assert moe.moe_shared_expert_workspace_size(64, 7168, 2048) > 64 * 2048 * 2
+
+
+def test_mxfp8_entries_validate_on_the_host(moe):
+    """The MXFP4-weight x MXFP8-activation format and its helpers: argument
+    rules that fail before any device is touched, and the host-computed
+    sizes (the scale atoms, the workspace with codes and atoms)."""
+    P = 0x1000                                               # 32-byte aligned, never dereferenced
+    A8 = moe.MOE_WEIGHTS_MXFP4_A8
+    # prepared scales: 512-byte atoms per 128 rows x 128 columns per expert
+    assert moe.moe_mx_prepared_scales_size(256, 4096, 7168) == 256 * 32 * 56 * 512
+    assert moe.moe_mx_prepared_scales_size(2, 100, 256) == 0
+    assert moe.moe_mx_prepared_scales_size(0, 128, 128) == 0
+    assert _status(moe.moe_mx_prepare_scales, P, 2, 100, 256, P) == moe.MOE_ERR_ALIGNMENT
+    assert _status(moe.moe_mx_prepare_scales, P + 2, 2, 128, 256, P) == moe.MOE_ERR_ALIGNMENT
+    assert _status(moe.moe_mx_prepare_scales, None, 2, 128, 256, P) == moe.MOE_ERR_INVALID_ARG
+    # the quantiser: C a multiple of 128, 16-byte aligned rows; rows = 0 is a no-op
+    assert _status(moe.moe_mxfp8_quantize, P, 4, 96, P, P) == moe.MOE_ERR_ALIGNMENT
+    assert _status(moe.moe_mxfp8_quantize, P + 8, 4, 128, P, P) == moe.MOE_ERR_ALIGNMENT
+    assert _status(moe.moe_mxfp8_quantize, P, -1, 128, P, P) == moe.MOE_ERR_INVALID_ARG
+    assert _status(moe.moe_mxfp8_quantize, P, 0, 128, None, None) == 0
+    # the weight format: prepared scales required, codes 32-byte aligned, K % 256 == 0
+    w = moe.make_weights(A8, 8, 7168, 2048, P, P, P, P)
+    assert moe.moe_experts_workspace_size(w, 64, 8) > 64 * 8 * (7168 + 2048)   # x and act codes
+    assert moe.moe_experts_workspace_size(moe.make_weights(A8, 8, 7168, 2048, P, P), 64, 8) == 0
+    assert moe.moe_experts_workspace_size(moe.make_weights(A8, 8, 7168, 2048, P + 16, P, P, P), 64, 8) == 0
+    assert moe.moe_experts_workspace_size(moe.make_weights(A8, 8, 384, 2048, P, P, P, P), 64, 8) == 0
+    F = moe.MOE_DTYPE_F32
+    # the BatchedExperts entry does not take the format
+    assert _status(moe.moe_experts_batched, w, P, P, 4, P + 4096, F, P, 1 << 30) == moe.MOE_ERR_UNSUPPORTED

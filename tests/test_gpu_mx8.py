@@ -253,6 +253,8 @@ def test_experts_a8_argument_checks(moe):
     assert moe.moe_experts_workspace_size(cw, 4, 1) == 0
     cw.K = 256
     assert moe.moe_experts_workspace_size(cw, 4, 1) > 0
+    assert moe.moe_experts_launches(cw, 4, 1, True) == 4     # out init, quantiser, GEMM1, GEMM2
+    assert moe.moe_experts_launches(cw, 4, 1, False) == 3
     ws = torch.zeros(16, dtype=torch.uint8, device=DEV)
     with pytest.raises(moe.MoEError) as e:
         moe.moe_experts_batched(cw, torch.zeros(E, 4, 256, dtype=torch.bfloat16, device=DEV),
