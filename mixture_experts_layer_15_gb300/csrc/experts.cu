@@ -295,7 +295,6 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     m1.sfa = w->w1_scale;
     m1.sfb = xs;
     m1.sfb_out = as;
-    m1.bt = L.bt;
     m1.max_token_tiles = L.max_token_tiles;
     gemm::Mx8Args m2 = m1;
     GemmArgs& a2 = m2.g;

@@ -98,7 +98,6 @@ struct Mx8Args {
     const uint8_t* sfa;       // weight atoms [(groups * rows_per_group) / 128][kr / 128][512]
     const uint8_t* sfb;       // activation atoms [token tiles][kr / 128][512]
     uint8_t* sfb_out;         // GEMM1: act atoms for GEMM2 [token tiles][N / 128][512]
-    int bt;                   // token tile rows (the atoms' tile)
     int max_token_tiles;      // token tiles the atom buffers hold
 };
 
