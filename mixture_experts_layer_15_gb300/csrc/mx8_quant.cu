@@ -22,9 +22,9 @@ constexpr int kQThreads = 256;
 // grouped (offsets, `groups` groups) and cut into token tiles of `bt` rows
 // per group; the scales go to the tile atoms the block-scaled GEMM reads
 // (tile t, k-block kb: atom t * (C/128) + kb; row n of the tile, chunk j at
-// byte (n % 32) * 16 + (n / 32) * 4 + j). Rows beyond offsets[groups] are
-// not touched; neither is anything when the groups need more than
-// `max_tiles` tiles.
+// byte (n % 32) * 16 + (n / 32) * 4 + j). Rows outside [offsets[0],
+// offsets[groups]) are not touched; neither is anything when the groups need
+// more than `max_tiles` tiles.
 template <bool ATOM>
 __global__ void __launch_bounds__(kQThreads)
 mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint8_t* __restrict__ codes,
@@ -36,7 +36,7 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int R = rows;
+    int R = rows, p0 = 0;
     if (ATOM) {
         for (int g = tid; g <= groups; g += kQThreads) {
             int v = __ldg(offsets + g);
@@ -50,6 +50,7 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
         }
         __syncthreads();
         const int ntiles = block_exclusive_scan(s_ttp, groups, tmp);
+        p0 = s_offs[0];                                    // rows below the first group belong to none
         R = s_offs[groups];
         if (ntiles > max_tiles) {                          // offsets not from a permute: touch nothing
             if (tid == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
@@ -58,7 +59,7 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
     }
     const int nkb = C / gemm::kMxBK;
     const int nw = kQThreads / 32;
-    for (int p = blockIdx.x * nw + warp; p < R; p += gridDim.x * nw) {
+    for (int p = p0 + blockIdx.x * nw + warp; p < R; p += gridDim.x * nw) {
         int T = 0, n = 0;
         if (ATOM) {
             int lo = 0, hi = groups;                       // s_offs[lo] <= p < s_offs[hi]

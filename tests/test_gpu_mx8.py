@@ -271,3 +271,31 @@ def test_layer_deepseek_a8(moe, M):
     activations: routing and map bit-exact over all tokens, outputs on a
     token sample against the oracle with the same activation quantisation."""
     _check_layer(moe, "deepseek", M, sample=8, a8=True)
+
+
+def test_experts_a8_offsets_not_starting_at_zero(moe):
+    """Caller-built offsets whose first group starts past row 0: the grouped
+    rows match the oracle's experts on those rows, and the rows outside every
+    group (before the first, after the last) are left untouched."""
+    E, K, N, k = 2, 256, 128, 1
+    p1, s1, p2, s2, _, _ = _random_mx_problem(E, K, N, 1, 1, seed=17)
+    rows = 10
+    g = torch.Generator().manual_seed(18)
+    xp = torch.randn(rows, K, generator=g).to(torch.bfloat16)
+    offs = np.array([2, 5, 9], np.int32)
+    cw, keep = _a8_weights(moe, p1, s1, p2, s2, E, K, N)
+    ws_n = moe.moe_experts_workspace_size(cw, rows, k)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device=DEV)
+    g2 = torch.full((rows, K), float("nan"), dtype=torch.float32, device=DEV)
+    moe.moe_experts(cw, xp.to(DEV), torch.from_numpy(offs).to(DEV), rows, k, g2, moe.MOE_DTYPE_F32, 0, None, 0,
+                    None, None, 0, 1.0, None, 0, ws, ws_n)
+    torch.cuda.synchronize()
+    _check_no_error(moe)
+    got = g2.double().cpu().numpy()
+    w1 = np.stack([O.dequant_mxfp4(p1[e].numpy(), s1[e].numpy()) for e in range(E)])
+    w2 = np.stack([O.dequant_mxfp4(p2[e].numpy(), s2[e].numpy()) for e in range(E)])
+    # the same problem with its rows moved to start at 0: rows 2..8, identity inverse
+    x = xp.double().numpy()[2:9]
+    ref, allow = _oracle_a8(x, w1, w2, offs - 2, np.arange(7), 1)
+    _assert_a8_close(got[2:9], ref, allow)
+    assert np.isnan(got[:2]).all() and np.isnan(got[9:]).all()
