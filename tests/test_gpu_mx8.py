@@ -206,6 +206,11 @@ def test_experts_a8_parity(moe, E, K, N, M, k, bt, splits):
         fused = torch.empty(M, K, dtype=torch.float32, device=DEV)
         moe.moe_experts_fused_finalize(cw, xp.to(DEV), offs_d, M, k, w_d, moe.MOE_DTYPE_F32, inv_d, None, 0, 1.0,
                                        fused, ws, ws_n)
+        # the same with a shared-expert output and a routed scale (the shared output is added after the scale)
+        shared = torch.randn(M, K, generator=torch.Generator().manual_seed(M)).to(DEV)
+        fused_sh = torch.empty(M, K, dtype=torch.float32, device=DEV)
+        moe.moe_experts_fused_finalize(cw, xp.to(DEV), offs_d, M, k, w_d, moe.MOE_DTYPE_F32, inv_d, shared,
+                                       moe.MOE_DTYPE_F32, 2.5, fused_sh, ws, ws_n)
         torch.cuda.synchronize()
         _check_no_error(moe)
     finally:
@@ -218,6 +223,9 @@ def test_experts_a8_parity(moe, E, K, N, M, k, bt, splits):
     allow_out = O.finalize(allow, np.abs(w.astype(np.float64)), pmap)     # sum_j |w| * allowance
     _assert_a8_close(out.double().cpu().numpy(), ref_out, allow_out)
     _assert_a8_close(fused.double().cpu().numpy(), ref_out, allow_out)
+    sh = shared.double().cpu().numpy()
+    ref_sh = O.finalize(ref, w.astype(np.float64), pmap, sh, 2.5)
+    _assert_a8_close(fused_sh.double().cpu().numpy() - sh, ref_sh - sh, 2.5 * allow_out)
     # the quantised path is not the unquantised one: its distance to the
     # W4A16 oracle is of the order of the E4M3 rounding (a few percent)
     ref16 = O.experts(x.double().numpy(), w1, w2, offs, inv, k)
