@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -97,7 +98,7 @@ class ClockSampler:
 
     def __init__(self, dev=0):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{dev}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"moe_bench_clocks_{os.getpid()}_{dev}.csv")
         sel = []
         try:
             u = str(torch.cuda.get_device_properties(dev).uuid)

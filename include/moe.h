@@ -221,24 +221,32 @@ moe_status moe_route_permute(const float* logits, int M, int E, int top_k,
 
 /* ------------------------------------------------------------------------
  * moe_permute_noalloc -- moe_permute for callers that cannot allocate device
- * memory (no counterpart on the pages: it exists for this library's users).
- * Some callers may not call cudaMalloc or hand the library a workspace: code
- * capturing into a fixed graph memory pool, runtimes whose allocator is
- * reserved, or real-time paths that must never allocate. This entry point
- * takes the same arguments as moe_permute minus the workspace and gives the
- * same results bit for bit; its scratch (the per-chunk expert histograms) is
- * a fixed 1 MiB array inside the library that every GPU loading the library
- * holds until the process exits.
+ * memory. The paper has no counterpart: it exists for this library's users.
+ * Some callers may neither call cudaMalloc nor hand the library a workspace:
+ * an inference engine that carves all device memory out of one arena at
+ * start-up and gives the libraries it hosts no allocator, a plugin loaded
+ * into a process whose allocator belongs to the host application, or a
+ * latency-critical path that must never reach cudaMalloc (which can
+ * synchronise the device). This entry point takes the same arguments as
+ * moe_permute minus the workspace and gives the same results bit for bit.
+ * Its scratch (the per-chunk expert histograms) is a fixed 1 MiB array inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.
  *  - Limit: moe_permute_workspace_size(M, top_k, E_local) must be at most
  *    1 MiB (for example M*top_k up to 2^21 routes at E_local = 128); larger
  *    problems return MOE_ERR_WORKSPACE and enqueue nothing.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
- *  - It calls no cudaMalloc, cudaFree or allocating routine.
- *  - All calls on one device share the array; nothing in it needs clearing
+ *  - The first call on each device does the set-up: with that device current
+ *    it looks up the array's device address (cudaGetSymbolAddress) and caches
+ *    it. Make that first call before any stream capture. A lookup that fails
+ *    returns MOE_ERR_CUDA and is tried again by the next call. The cached
+ *    address belongs to the device's primary context: cudaDeviceReset, or a
+ *    context of the caller's own, is not supported while the library is loaded.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - All calls on one device share the array. Nothing in it needs clearing
  *    between calls (every entry read is written first by the same call), but
- *    calls whose kernels overlap on the GPU race on it and give wrong maps.
+ *    calls whose kernels overlap on the GPU race on it and give wrong maps:
+ *    order them (one stream, or explicit events).
+ *  - Argument checks and status codes are those of moe_permute.
  * ---------------------------------------------------------------------- */
 moe_status moe_permute_noalloc(const int32_t* topk_ids, int M, int top_k, int E,
                                const int32_t* expert_map, int E_local,
@@ -458,9 +466,13 @@ moe_status moe_mx_prepare_scales(const uint8_t* scales, int E_local, int rows, i
 
 const char* moe_status_string(int status);
 
-/* Synchronizes `stream`, then returns and clears the device error word of the
- * current device: MOE_OK, MOE_ERR_DEVICE_INDEX or MOE_ERR_DEVICE_TIMEOUT
- * (MOE_ERR_CUDA if the synchronization itself failed). Not for the hot path. */
+/* Returns and clears the device error word of the current device: MOE_OK,
+ * MOE_ERR_DEVICE_INDEX or MOE_ERR_DEVICE_TIMEOUT (MOE_ERR_CUDA if a CUDA call
+ * failed). The read and the clear are one atomic exchange on the device,
+ * enqueued on `stream` after everything enqueued there before; the call then
+ * waits for it (it synchronizes `stream`). Not for the hot path, and not to be
+ * called from several host threads at once for one device (they share the
+ * slot the exchanged value is copied through). */
 moe_status moe_get_error(cudaStream_t stream);
 
 /* MOE_OK if the current device has compute capability 10.3. */

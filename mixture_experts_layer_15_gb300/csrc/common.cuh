@@ -47,6 +47,20 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Plain (stream-ordered) launch that returns the launch's own error code, so
+// no earlier, unrelated error of the caller is read or cleared.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // PDL launch of a kernel in thread-block clusters of `cluster` CTAs along x
 // (grid.x a multiple of it). Falls back to a plain cluster launch if the two
 // attributes cannot be combined.

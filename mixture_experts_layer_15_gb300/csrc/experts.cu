@@ -364,8 +364,7 @@ __global__ void bounded_wait_kernel(const int* flag, int target, unsigned long l
 
 cudaError_t launch_debug_bounded_wait(const int* flag, int target, unsigned long long limit_ns, int* err,
                                       cudaStream_t s) {
-    bounded_wait_kernel<<<1, 1, 0, s>>>(flag, target, limit_ns, err);
-    return cudaGetLastError();
+    return launch_plain(bounded_wait_kernel, dim3(1), dim3(1), 0, s, flag, target, limit_ns, err);
 }
 
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {

@@ -10,6 +10,7 @@
 // moe_get_error, which is documented to).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.h"
@@ -19,35 +20,55 @@ namespace moe {
 
 namespace {
 __device__ int g_error_word;     // first device-detected error since the last moe_get_error
+__device__ int g_error_taken;    // the value the last moe_get_error took out of g_error_word
 
+// One device's cached properties and symbol addresses. Only a complete,
+// successful set-up is cached: a lookup that failed (no device yet, a query
+// error) is retried by the next call.
 constexpr int kMaxDevices = 64;
 struct DevSlot {
-    std::once_flag once;
-    bool ok = false;
+    std::mutex mu;
+    std::atomic<bool> ok{false};
     DeviceInfo info;
     int* err = nullptr;
+    int* taken = nullptr;
 };
 DevSlot g_dev[kMaxDevices];
 
+// A CUDA runtime error that this code's own call returned is cleared here (it
+// is reported as a status); errors of other calls are left for their owner.
+inline bool cuda_ok(cudaError_t e) {
+    if (e == cudaSuccess) return true;
+    cudaGetLastError();
+    return false;
+}
+
 DevSlot* current_slot() {
     int d = -1;
-    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    if (!cuda_ok(cudaGetDevice(&d)) || d < 0 || d >= kMaxDevices) return nullptr;
     DevSlot* s = &g_dev[d];
-    std::call_once(s->once, [s, d] {
-        DeviceInfo i;
-        if (cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return;
-        cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, d);
-        cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
-        cudaDeviceGetAttribute(&i.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return;
-        s->info = i;
-        s->err = static_cast<int*>(p);
-        s->ok = true;
-    });
-    cudaGetLastError();   // clear any sticky-free error left by the queries
-    return s->ok ? s : nullptr;
+    if (s->ok.load(std::memory_order_acquire)) return s;
+    std::lock_guard<std::mutex> lock(s->mu);
+    if (s->ok.load(std::memory_order_relaxed)) return s;
+    DeviceInfo i;
+    void* e = nullptr;
+    void* t = nullptr;
+    if (!cuda_ok(cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, d)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, d)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, d)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&i.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d)) ||
+        !cuda_ok(cudaGetSymbolAddress(&e, g_error_word)) || !cuda_ok(cudaGetSymbolAddress(&t, g_error_taken)))
+        return nullptr;
+    s->info = i;
+    s->err = static_cast<int*>(e);
+    s->taken = static_cast<int*>(t);
+    s->ok.store(true, std::memory_order_release);
+    return s;
 }
+
+// Reads and clears the error word in one atomic step, so no error that a
+// kernel on another stream records at the same time can be lost.
+__global__ void take_error_kernel(int* err, int* taken) { *taken = atomicExch(err, 0); }
 }  // namespace
 
 bool current_device_info(DeviceInfo* info) {
@@ -60,6 +81,20 @@ bool current_device_info(DeviceInfo* info) {
 int* device_error_word() {
     DevSlot* s = current_slot();
     return s ? s->err : nullptr;
+}
+
+// moe_get_error's device part: enqueue the read-and-clear on `stream`, copy the
+// taken value back, wait for it.
+cudaError_t take_device_error(cudaStream_t stream, int* value) {
+    DevSlot* s = current_slot();
+    if (!s) return cudaErrorNoDevice;
+    void* args[] = {&s->err, &s->taken};
+    cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(take_error_kernel), dim3(1), dim3(1), args, 0,
+                                     stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(value, s->taken, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe
@@ -153,13 +188,9 @@ moe_status moe_get_error(cudaStream_t stream) {
     int* err = nullptr;
     const moe_status st = device_gate(&info, &err);
     if (st != MOE_OK) return st;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // everything enqueued on `stream` so far completes before the read
     int v = 0;
-    if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    if (v != 0) {
-        const int zero = 0;
-        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
-    }
+    if (moe::take_device_error(stream, &v) != cudaSuccess) return MOE_ERR_CUDA;
     return static_cast<moe_status>(v);
 }
 
@@ -263,17 +294,9 @@ moe_status moe_permute(const int32_t* topk_ids, int M, int top_k, int E, const i
                        int E_local, const void* x, int K, int32_t* expert_offsets,
                        int32_t* expanded_idx_to_permuted_idx, int32_t* permuted_to_expanded, void* x_perm,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (M < 0 || top_k <= 0 || E < 1 || E_local < 1 || E_local > 1024 || top_k > E) return MOE_ERR_INVALID_ARG;
-    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
-    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
-    if (x_perm != nullptr) {
-        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
-        if (K % 8 != 0 || !aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
-    }
-    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
-    if (M > 0 && (topk_ids == nullptr || expanded_idx_to_permuted_idx == nullptr ||
-                  permuted_to_expanded == nullptr))
-        return MOE_ERR_INVALID_ARG;
+    const moe_status a = moe::check_permute_args(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                                                 expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm);
+    if (a != MOE_OK) return a;
     const size_t need = moe::permute_workspace_bytes(M > 0 ? M : 1, top_k, E_local);
     if (M > 0 && need > 0 && (workspace == nullptr || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
     DeviceInfo info;
@@ -312,17 +335,10 @@ moe_status moe_route_permute(const float* logits, int M, int E, int top_k, moe_r
         return MOE_ERR_INVALID_ARG;
     }
     // ... and of moe_permute
-    if (E_local < 1 || E_local > 1024) return MOE_ERR_INVALID_ARG;
-    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
-    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
-    if (x_perm != nullptr) {
-        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
-        if (K % 8 != 0 || !aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
-    }
-    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
-    if (M > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr ||
-                  expanded_idx_to_permuted_idx == nullptr || permuted_to_expanded == nullptr))
-        return MOE_ERR_INVALID_ARG;
+    const moe_status a = moe::check_permute_args(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                                                 expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm);
+    if (a != MOE_OK) return a;
+    if (M > 0 && (logits == nullptr || topk_weights == nullptr)) return MOE_ERR_INVALID_ARG;
     const bool fused = M > 0 && moe::route_permute_fusible(M, top_k, E, E_local, method);
     const size_t need = moe::permute_workspace_bytes(M > 0 ? M : 1, top_k, E_local);
     if (M > 0 && !fused && need > 0 && (workspace == nullptr || workspace_bytes < need)) return MOE_ERR_WORKSPACE;

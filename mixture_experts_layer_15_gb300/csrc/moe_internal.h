@@ -23,6 +23,26 @@ bool current_device_info(DeviceInfo* info);
 // Address (device pointer) of the current device's error word.
 int* device_error_word();
 
+inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host checks of the permute's arguments, shared by moe_permute,
+// moe_permute_noalloc and the permute half of moe_route_permute: sizes and
+// ranges, required pointers, the row gather's alignment.
+inline moe_status check_permute_args(const int32_t* topk_ids, int M, int top_k, int E, const int32_t* expert_map,
+                                     int E_local, const void* x, int K, const int32_t* expert_offsets,
+                                     const int32_t* map, const int32_t* inverse, const void* x_perm) {
+    if (M < 0 || top_k <= 0 || E < 1 || E_local < 1 || E_local > 1024 || top_k > E) return MOE_ERR_INVALID_ARG;
+    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (x_perm != nullptr) {
+        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
+        if (K % 8 != 0 || !is_aligned16(x) || !is_aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+    }
+    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (M > 0 && (topk_ids == nullptr || map == nullptr || inverse == nullptr)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 // ---- router (router.cu) --------------------------------------------------------
 cudaError_t launch_route(const float* logits, int M, int E, int top_k, int method,
                          const float* score_bias, int n_group, int topk_group, float rsf,

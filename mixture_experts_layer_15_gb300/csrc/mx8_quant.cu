@@ -161,8 +161,8 @@ cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total
     if (total == 0) return cudaSuccess;
     long long grid = (total + 255) / 256;
     if (grid > 16LL * dev.sm_count) grid = 16LL * dev.sm_count;
-    mx_prepare_scales_kernel<<<static_cast<int>(grid), 256, 0, s>>>(scales, rows_total, cols, out);
-    return cudaGetLastError();
+    return launch_plain(mx_prepare_scales_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, scales, rows_total,
+                        cols, out);
 }
 
 }  // namespace moe

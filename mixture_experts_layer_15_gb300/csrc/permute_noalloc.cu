@@ -1,25 +1,32 @@
 // moe_permute_noalloc: the permute for callers that cannot allocate device
-// memory -- code that runs while a CUDA graph is being captured into a
-// pre-sized memory pool, an embedding runtime whose allocator is off limits
-// to libraries, or a real-time path that must never reach cudaMalloc. It
-// computes exactly what moe_permute computes, but the per-chunk expert
-// histograms that moe_permute keeps in the caller's workspace live in a
-// fixed array inside this library instead.
+// memory. Examples are an inference engine that carves all device memory out
+// of one arena at start-up and gives the libraries it hosts no allocator, a
+// plugin loaded into a process whose allocator belongs to the host
+// application, and a latency-critical path that must never reach cudaMalloc
+// (it can synchronise the device and has no bounded cost). It computes exactly
+// what moe_permute computes. The per-chunk expert histograms that moe_permute
+// keeps in the caller's workspace live in a fixed array inside this library
+// instead.
 //
 // The array is a file-scope static __device__ buffer of
 // kNoAllocScratchInts ints (1 MiB). Every GPU that loads the library holds
-// one copy of it until the process exits. Host code never names the array
-// as an address: on the first call on a device, with that device current,
-// cudaGetSymbolAddress gives the device pointer, which is cached per device
-// and passed to the kernels.
+// one copy of it until the process exits. Host code never passes the array's
+// name to a kernel: in host code that name stands for a host-side shadow, not
+// a device address. On the first call on a device, with that device current,
+// cudaGetSymbolAddress gives the device pointer. A successful lookup is
+// cached per device and passed to the kernels; a failed one is reported as
+// MOE_ERR_CUDA and tried again by the next call. The cache assumes the
+// device's primary context (the runtime API's default) for the life of the
+// process.
 //
 // The permute writes every scratch entry it later reads (the count kernel
 // fills the histograms before the scan reads them), so nothing has to be
 // cleared between calls. All calls on a device share the one array: two
-// calls whose kernels overlap on the GPU (different streams without
-// ordering, or concurrent graph launches) race on it and give wrong maps.
+// calls whose kernels overlap on the GPU (for example on two streams with no
+// ordering between them) race on it and give wrong maps.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.h"
@@ -32,25 +39,35 @@ static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
 struct ScratchSlot {
-    std::once_flag once;
-    int32_t* ptr = nullptr;
+    std::mutex mu;
+    std::atomic<int32_t*> ptr{nullptr};
 };
 ScratchSlot g_scratch[kMaxDevices];
 
-// Device pointer of this device's scratch array (set up once per device).
+// Device pointer of the current device's scratch array, or nullptr if the
+// lookup failed (then nothing is cached and the next call tries again).
 int32_t* scratch_for_current_device() {
     int d = -1;
-    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    if (cudaGetDevice(&d) != cudaSuccess) {
+        cudaGetLastError();                      // this call's own error, reported as a status
+        return nullptr;
+    }
+    if (d < 0 || d >= kMaxDevices) return nullptr;
     ScratchSlot* s = &g_scratch[d];
-    std::call_once(s->once, [s] {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_permute_scratch) == cudaSuccess) s->ptr = static_cast<int32_t*>(p);
-        else cudaGetLastError();
-    });
-    return s->ptr;
+    int32_t* p = s->ptr.load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+    std::lock_guard<std::mutex> lock(s->mu);
+    p = s->ptr.load(std::memory_order_relaxed);
+    if (p != nullptr) return p;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_permute_scratch) != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    p = static_cast<int32_t*>(addr);
+    s->ptr.store(p, std::memory_order_release);
+    return p;
 }
-
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -58,17 +75,9 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int M, int to
                                           const int32_t* expert_map, int E_local, const void* x, int K,
                                           int32_t* expert_offsets, int32_t* expanded_idx_to_permuted_idx,
                                           int32_t* permuted_to_expanded, void* x_perm, cudaStream_t stream) {
-    if (M < 0 || top_k <= 0 || E < 1 || E_local < 1 || E_local > 1024 || top_k > E) return MOE_ERR_INVALID_ARG;
-    if (expert_map == nullptr && E_local != E) return MOE_ERR_INVALID_ARG;
-    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
-    if (x_perm != nullptr) {
-        if (x == nullptr || K <= 0) return MOE_ERR_INVALID_ARG;
-        if (K % 8 != 0 || !aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
-    }
-    if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
-    if (M > 0 && (topk_ids == nullptr || expanded_idx_to_permuted_idx == nullptr ||
-                  permuted_to_expanded == nullptr))
-        return MOE_ERR_INVALID_ARG;
+    const moe_status a = moe::check_permute_args(topk_ids, M, top_k, E, expert_map, E_local, x, K, expert_offsets,
+                                                 expanded_idx_to_permuted_idx, permuted_to_expanded, x_perm);
+    if (a != MOE_OK) return a;
     // the fixed scratch bounds the problem size
     if (M > 0 && moe::permute_workspace_bytes(M, top_k, E_local) > kNoAllocScratchInts * sizeof(int32_t))
         return MOE_ERR_WORKSPACE;

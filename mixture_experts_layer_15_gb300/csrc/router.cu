@@ -93,8 +93,7 @@ cudaError_t launch_route(const float* logits, int M, int E, int top_k, int metho
 }
 
 cudaError_t launch_debug_sigmoid(const float* x, float* y, int n, cudaStream_t s) {
-    debug_sigmoid_kernel<<<ceil_div(n, 256), 256, 0, s>>>(x, y, n);
-    return cudaGetLastError();
+    return launch_plain(debug_sigmoid_kernel, dim3(ceil_div(n, 256)), dim3(256), 0, s, x, y, n);
 }
 
 }  // namespace moe

@@ -15,8 +15,10 @@ page fixes the precision:
 * route_softmax_topk / route_sigmoid_grouped -- the [Router] step. The pages
   name it and pass its outputs (``topk_ids``, ``topk_weights``;
   modular_kernel.py ``FusedMoEModularKernel.forward``) but never give its
-  math; the readings used here (softmax -> top-k -> renormalise, and sigmoid
-  + bias -> grouped top-k -> renormalise x scale) are listed in the design doc.
+  math. The readings used here: softmax -> top-k -> renormalise (the top_k
+  largest logits, ties to the lower id), and DeepSeek-V3's published rule,
+  sigmoid + bias -> grouped top-k -> renormalise x scale (a group scores the
+  sum of its two largest biased scores).
   Where floating point decides an integer (the sigmoid router's selection),
   the decision is taken in float32 with the written ``sigmoid_f32_spec``,
   the same spec the CUDA router implements independently.

@@ -156,3 +156,38 @@ def test_mxfp8_entries_validate_on_the_host(moe):
     F = moe.MOE_DTYPE_F32
     # the BatchedExperts entry does not take the format
     assert _status(moe.moe_experts_batched, w, P, P, 4, P + 4096, F, P, 1 << 30) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_permute_noalloc_validates_like_moe_permute(moe):
+    """The no-alloc permute shares moe_permute's host checks: the same bad
+    arguments give the same status, before any device is touched, plus its
+    own limit (a problem whose histograms exceed the fixed 1 MiB scratch)."""
+    P = 0x1000                                               # never dereferenced
+    na = lambda M, k, E, emap, El, ids=P, offs=P, pmap=P, inv=P, x=P, xp=P, K=128: _status(
+        moe.moe_permute_noalloc, ids, M, k, E, emap, El, x, K, offs, pmap, inv, xp)
+    wp = lambda M, k, E, emap, El, ids=P, offs=P, pmap=P, inv=P, x=P, xp=P, K=128: _status(
+        moe.moe_permute, ids, M, k, E, emap, El, x, K, offs, pmap, inv, xp, P, 1 << 30)
+    cases = [
+        dict(M=-1, k=2, E=8, emap=None, El=8),                      # num_tokens >= 0
+        dict(M=4, k=0, E=8, emap=None, El=8),                       # top_k > 0
+        dict(M=4, k=9, E=8, emap=None, El=8),                       # top_k <= E
+        dict(M=4, k=2, E=2048, emap=P, El=1025),                    # E_local <= 1024
+        dict(M=4, k=2, E=8, emap=None, El=4),                       # no map: E_local == E
+        dict(M=1 << 27, k=8, E=128, emap=None, El=128),             # M * top_k < 2^30
+        dict(M=4, k=2, E=8, emap=None, El=8, ids=None),             # required pointers
+        dict(M=4, k=2, E=8, emap=None, El=8, offs=None),
+        dict(M=4, k=2, E=8, emap=None, El=8, pmap=None),
+        dict(M=4, k=2, E=8, emap=None, El=8, inv=None),
+        dict(M=4, k=2, E=8, emap=None, El=8, x=None),               # x needed for x_perm
+        dict(M=4, k=2, E=8, emap=None, El=8, K=100),                # 16-byte row gather
+        dict(M=4, k=2, E=8, emap=None, El=8, x=P + 8),
+    ]
+    want = [moe.MOE_ERR_INVALID_ARG] * 5 + [moe.MOE_ERR_UNSUPPORTED] + [moe.MOE_ERR_INVALID_ARG] * 5 + \
+        [moe.MOE_ERR_ALIGNMENT] * 2
+    for c, w in zip(cases, want):
+        assert na(**c) == w, c
+        assert wp(**c) == w, c
+    # beyond the fixed scratch: 2^21 + 1024 routes at 128 local experts
+    M = (1 << 18) + 128
+    assert moe.moe_permute_workspace_size(M, 8, 128) > (1 << 20)
+    assert na(M, 8, 128, None, 128) == moe.MOE_ERR_WORKSPACE
