@@ -190,19 +190,22 @@ def launches_per_forward(moe, cfg, layer, M, finalize="fused"):
     return n
 
 
-def roofline_layer(cfg, M, touched, pk, sustained=True, routed_mult=1.0):
+def roofline_layer(cfg, M, touched, pk, sustained=False, routed_mult=1.0, routes=None):
     """Slower of touched-expert weight bytes at HBM bandwidth and FLOPs at
     the bf16 tensor peak (the routed experts' FLOPs at routed_mult x that
     peak: 2, the nominal fp8 : bf16 ratio, for MXFP8 activations); returns
-    (seconds, bytes, flops, tensor seconds)."""
+    (seconds, bytes, flops, tensor seconds). The burst peak by default: the
+    per-M calls are single calls timed in isolation. ``routes``: the routed
+    rows (M * top_k unless some experts are not local)."""
     bpw = 2.0 if cfg.weight_format == "bf16" else (0.5 + 1.0 / 32.0)
     wbytes = touched * 3.0 * cfg.K * cfg.N * bpw
-    flops = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+    R = M * cfg.top_k if routes is None else routes
+    flops = 6.0 * cfg.K * cfg.N * R
     if cfg.shared_N:
         wbytes += 3.0 * cfg.K * cfg.shared_N * 2.0
         flops += 6.0 * cfg.K * cfg.shared_N * M
     tc = (pk["bf16_sus"] if sustained else pk["bf16"]) * 1e12
-    fr = 6.0 * cfg.K * cfg.N * M * cfg.top_k
+    fr = 6.0 * cfg.K * cfg.N * R
     t_tc = fr / (tc * routed_mult) + (flops - fr) / tc
     return max(wbytes / (pk["hbm"] * 1e9), t_tc), wbytes, flops, t_tc
 
@@ -348,7 +351,8 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
                "touched_experts": touched[M], "roofline_ms": troof * 1e3,
                "roofline_frac": troof / tm,
                "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= t_tc else "tensor",
-               "gemm_tflops": gf / tgm / 1e12}
+               "gemm_tflops": gf / tgm / 1e12, "weight_bytes": wbytes, "gemm_flops": gf,
+               "peak_kind": "burst (single calls timed in isolation)"}
         if M <= graph_max_m:
             tgr, err = graph_time(forward, M, stream, scrub, reps)
             if tgr is not None:
@@ -364,8 +368,35 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
     return secs, per_m, gemm_flops, gemm_secs, clk
 
 
-def other_config(moe, name, args, pk, dev, stream):
-    """The same measurement on another config (reported beside the headline)."""
+def roofline_objects(per_m, pk, traffic=None, mult=1.0, kernel=None):
+    """The roofline report of one config's sweep, each regime against its own
+    peak (burst figures: every per-M call is timed alone):
+    - ``dominant``: the experts step at the largest M (the launch that takes
+      the most time): its algorithmic FLOPs (6 K N per routed row) over its
+      event-timed duration, against the tensor peak;
+    - ``hbm``: the HBM-bound batch sizes together: touched-expert weight bytes
+      over the whole forward's time, against the measured HBM bandwidth."""
+    big = max(per_m, key=lambda r: r["M"])
+    peak_t = pk["bf16"] * mult
+    ach = big["gemm_flops"] / (big["gemm_ms"] * 1e-3) / 1e12
+    dom = {"kernel": kernel or "the experts step (grouped GEMM1 + activation, GEMM2, folded finalize)",
+           "M": big["M"], "bound": "tensor", "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
+           "frac": ach / peak_t,
+           "peak_kind": f"{pk['src']} bf16 burst" + (" x 2 (fp8)" if mult != 1.0 else ""),
+           "traffic": traffic, "algorithmic": "6*K*N*routes FLOPs of the experts step at the largest M"}
+    hb = [r for r in per_m if r["bound"] == "hbm"]
+    out = {"dominant": dom}
+    if hb:
+        gbs = sum(r["weight_bytes"] for r in hb) / (sum(r["ms"] for r in hb) * 1e-3) / 1e9
+        out["hbm"] = {"M": [r["M"] for r in hb], "bound": "hbm", "achieved": gbs, "peak": pk["hbm"],
+                      "unit": "GB/s", "frac": gbs / pk["hbm"], "peak_kind": f"{pk['src']} HBM copy",
+                      "algorithmic": "touched-expert weight bytes of each whole forward"}
+    return out
+
+
+def other_config(moe, name, args, pk, dev, stream, cpu=False):
+    """The same measurement on another config (reported beside the headline),
+    with the oracle baseline on the host cores when ``cpu``."""
     cfg, li, layer, batches = make_workload(name, dev)
     sweep = sorted(batches)
     forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
@@ -375,10 +406,59 @@ def other_config(moe, name, args, pk, dev, stream):
     out = {"workload": f"{cfg.name}-shaped MoE layer (K={cfg.K}, N={cfg.N}, E={cfg.E}, top_k={cfg.top_k}, "
                        f"{cfg.weight_format} weights{', shared expert' if cfg.shared_N else ''})",
            "tokens_per_s": sum(sweep) * steps / secs, "steps": steps, "gemm_tflops": gf / gs / 1e12,
+           "roofline": roofline_objects(per_m, pk),
            "sweep": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()} for r in per_m]}
+    if cpu:
+        out["cpu_baseline"] = cpu_baselines(cfg, li, batches)
     del layer, li, batches
     torch.cuda.empty_cache()
     return out
+
+
+def masked_stress(moe, pk, dev, stream, M=4096):
+    """The deferred-finalize / masked-expert stress workload: the
+    Qwen3-shaped layer at M = 4096 with a seeded random half of the 128
+    experts non-local (their routes are -1 in the permute map), run as route +
+    permute, the experts with do_finalize = 0 (gemm2_permuted, f32), then a
+    separate finalize with a shared-expert output added (a seeded [M, K]
+    tensor standing in for the shared expert's output). Median of 20 forwards,
+    each after an L2 scrub; roofline over the local experts' routes."""
+    import mixture_experts_layer_15_gb300 as _m
+    cfg = synth.CONFIGS["qwen3"]
+    li = synth.make_layer(cfg, dev)
+    em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+    keep = torch.from_numpy(np.nonzero(em.numpy() >= 0)[0]).to(dev)
+    layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1[keep].contiguous(),
+                         w2=li.w2[keep].contiguous(), expert_map=em.to(dev), E_local=E_l)
+    x, logits = synth.make_tokens(cfg, M, dev, li)
+    del li
+    g = torch.Generator(device=dev).manual_seed(77)
+    shared = torch.randn(M, cfg.K, generator=g, device=dev)
+    F = _m.MOE_DTYPE_F32
+
+    def fwd():
+        b = layer.forward(x, logits, do_finalize=False)
+        moe.moe_finalize(b.gemm2, F, b.gemm2.shape[0], b.topk_weights, F, b.pmap, M, cfg.top_k, cfg.K, shared, F,
+                         1.0, b.out, F)
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize()
+    buf = torch.zeros(256 << 20, dtype=torch.float32, device=dev)
+    t = _median_time(fwd, stream, lambda: l2_scrub(buf))
+    st = moe.moe_get_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the masked stress row: {moe.status_string(st)}")
+    b = layer.buffers(M)
+    touched = int((b.offsets.diff() > 0).sum().item())
+    R = int(b.offsets[-1].item())
+    troof, wbytes, flops, t_tc = roofline_layer(cfg, M, touched, pk, routes=R)
+    del buf, layer, x, logits, shared
+    torch.cuda.empty_cache()
+    return {"workload": f"qwen3-shaped layer, M={M}, expert_map with {E_l} of {cfg.E} experts local, "
+                        "do_finalize=0, then moe_finalize with a shared-output add (f32)",
+            "ms": t * 1e3, "tokens_per_s": M / t, "local_routes": R, "touched_local_experts": touched,
+            "roofline_ms": troof * 1e3, "frac": troof / t, "peak_kind": "burst",
+            "bound": "hbm" if wbytes / (pk["hbm"] * 1e9) >= t_tc else "tensor"}
 
 
 def _median_time(fn, stream, scrub, reps=20):
@@ -453,8 +533,8 @@ def next_rows(moe, pk, dev, stream):
         flops = 6.0 * cfg.K * cfg.N * M * cfg.top_k
         act_rows.append({"workload": f"mixtral-shaped experts step, M={M}, {act}_and_mul"
                                      + (f", clamp {clamp}" if clamp else ""),
-                         "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16_sus"],
-                         "bound": "tensor"})
+                         "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16"],
+                         "bound": "tensor", "peak_kind": "bf16 burst"})
         del layer
     out["activation"] = act_rows
 
@@ -471,8 +551,8 @@ def next_rows(moe, pk, dev, stream):
     t = _median_time(call, stream, scrub)
     flops = 6.0 * cfg.K * cfg.N * cfg.E * T
     out["batched_experts"] = [{"workload": f"mixtral-shaped, E={cfg.E}, max_tokens={T}, all blocks full, f32 out",
-                               "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16_sus"],
-                               "bound": "tensor"}]
+                               "ms": t * 1e3, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / pk["bf16"],
+                               "bound": "tensor", "peak_kind": "bf16 burst"}]
     del xb, counts, yb, wsb
     del li, x, logits, batches
     torch.cuda.empty_cache()
@@ -489,8 +569,9 @@ def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192)):
     expert, experts with the folded finalize) per M, median of 20 scrubbed
     runs, and the experts step alone. Roofline: touched weight bytes at HBM
     bandwidth vs FLOPs at the tensor peak of each path's MMAs (the routed
-    experts at the fp8 peak = measured bf16 sustained x 2, the nominal
-    fp8 : bf16 ratio, on the A8 path; bf16 otherwise; the shared expert bf16)."""
+    experts at the fp8 peak = measured bf16 burst x 2, the nominal
+    fp8 : bf16 ratio, on the A8 path; bf16 otherwise; the shared expert bf16;
+    burst peaks, since every forward is timed alone)."""
     cfg = synth.CONFIGS["deepseek"]
     li = synth.make_layer(cfg, dev)
     batches = {M: synth.make_tokens(cfg, M, dev, li) for M in sweep}
@@ -525,8 +606,8 @@ def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192)):
             wbytes = touched * 3.0 * cfg.K * cfg.N * (0.5 + 1.0 / 32.0) + 3.0 * cfg.K * cfg.shared_N * 2.0
             fr = 6.0 * cfg.K * cfg.N * M * cfg.top_k
             fs = 6.0 * cfg.K * cfg.shared_N * M
-            p_routed = pk["bf16_sus"] * (2.0 if fmt == moe.MOE_WEIGHTS_MXFP4_A8 else 1.0) * 1e12
-            t_tc = fr / p_routed + fs / (pk["bf16_sus"] * 1e12)
+            p_routed = pk["bf16"] * (2.0 if fmt == moe.MOE_WEIGHTS_MXFP4_A8 else 1.0) * 1e12
+            t_tc = fr / p_routed + fs / (pk["bf16"] * 1e12)
             t_hbm = wbytes / (pk["hbm"] * 1e9)
             troof = max(t_tc, t_hbm)
             rows.append({"workload": f"deepseek-shaped layer, M={M}, {tag}", "M": M, "ms": t * 1e3,
@@ -559,22 +640,21 @@ def run_gpu(args):
     secs_max = max_over_ranks(secs, world)
     tokens_step = sum(sweep)
     value = tokens_step * args.steps * world / secs_max
-    achieved = gemm_flops / gemm_secs / 1e12
     traffic = tcase = talg = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath) and not (args.m or args.experts or args.mxfp8_act) and args.finalize == "fused":
+    big_m = max(sweep)
+    if os.path.exists(tpath) and not (args.experts or args.mxfp8_act) and args.finalize == "fused":
         try:
             t = json.load(open(tpath)).get(args.config) or {}
-            traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
+            if t.get("M") == big_m:            # counters of the launch the roofline describes
+                traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
         except Exception:
             traffic = None
-    roof = {"kernel": ("the experts step: grouped GEMM1+silu_and_mul and GEMM2 (with the folded finalize and "
-                       "its out-init): one fused one-CTA launch, or two CTA-pair launches at large M"),
-            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-            "frac": achieved / pk["bf16_sus"], "peak_kind": f"{pk['src']} bf16 sustained",
-            "frac_of_burst": achieved / pk["bf16"], "traffic": traffic, "traffic_case": tcase,
-            "traffic_algorithmic": talg,
-            "algorithmic": "6*K*N*routes FLOPs per forward over the sweep"}
+    objs = roofline_objects(per_m, pk, traffic=traffic,
+                            kernel=("the experts step at the largest M: grouped GEMM1 + silu_and_mul and GEMM2 "
+                                    "with the folded finalize (and its out-init); two CTA-pair launches here"))
+    roof = dict(objs["dominant"])
+    roof.update(traffic_case=tcase, traffic_algorithmic=talg)
 
     e2e = run_e2e(args, cfg, layer, batches, forward_fn=forward)
     line = {
@@ -590,17 +670,19 @@ def run_gpu(args):
                                 "separate pass over gemm2_permuted (deterministic order)"),
                    "l2": "timed steps: inputs larger than L2 (expert weights streamed every forward); per-M breakdown: a 1 GB read scrub before each sample (median of 20)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roof, "sweep": per_m, "e2e": e2e,
+        "roofline": roof, "roofline_hbm": objs.get("hbm"), "sweep": per_m, "e2e": e2e,
         "gpu_launches": args.steps * sum(launches_per_forward(moe, cfg, layer, M, args.finalize) for M in sweep),
         "clocks": clk,
     }
     if rank == 0:
-        line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(cfg, li, batches, args)
+        line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baselines(cfg, li, batches)
         if args.others and not args.m and not args.experts and not args.mxfp8_act:
             del layer, batches
             torch.cuda.empty_cache()
-            line["other_configs"] = {name: other_config(moe, name, args, pk, dev, stream)
+            line["other_configs"] = {name: other_config(moe, name, args, pk, dev, stream,
+                                                        cpu=not args.no_cpu_baseline)
                                      for name in args.others.split(",") if name and name != args.config}
+            line["masked_stress"] = masked_stress(moe, pk, dev, stream)
             line["next_rows"] = next_rows(moe, pk, dev, stream)
         print(json.dumps(line))
     if world > 1:
@@ -674,20 +756,26 @@ def run_e2e(args, cfg, layer, batches, forward_fn):
 # ------------------------------------------------------------------ CPU oracle
 
 class _F64Experts:
-    """Per-expert float64 copies of the weights, made once outside timing."""
+    """Per-expert float64 weights for the oracle. bf16 weights are converted
+    once, outside the timing; MXFP4 bytes are dequantised by the oracle on
+    every access (its own step from the packed bytes), unless ``cache``."""
 
-    def __init__(self, w, scale=None):
+    def __init__(self, w, scale=None, cache=None):
         import oracle as O
         self.cache = {}
+        self.keep = scale is None if cache is None else cache
         self.w, self.scale, self.O = w, scale, O
 
     def __getitem__(self, e):
-        if e not in self.cache:
-            if self.scale is None:
-                self.cache[e] = self.w[e].to(torch.float64).cpu().numpy()
-            else:
-                self.cache[e] = self.O.dequant_mxfp4(self.w[e].cpu().numpy(), self.scale[e].cpu().numpy())
-        return self.cache[e]
+        if e in self.cache:
+            return self.cache[e]
+        if self.scale is None:
+            v = self.w[e].to(torch.float64).cpu().numpy()
+        else:
+            v = self.O.dequant_mxfp4(self.w[e].cpu().numpy(), self.scale[e].cpu().numpy())
+        if self.keep:
+            self.cache[e] = v
+        return v
 
     @property
     def shape(self):
@@ -712,30 +800,80 @@ def _oracle_setup(cfg, li, batches):
     x, logits = batches[Mbig]
     xs = x.to(torch.float64).cpu().numpy()
     ls = logits.cpu().numpy()
-    ids, _ = (O.route_softmax_topk(ls[:64], cfg.top_k) if cfg.route == "softmax" else
-              O.route_sigmoid_grouped(ls[:64], li.score_bias.cpu().numpy(), cfg.top_k, cfg.n_group,
-                                      cfg.topk_group, cfg.routed_scaling_factor))
-    for e in sorted(set(ids.reshape(-1).tolist())):   # convert the weights the sample uses, untimed
-        w1[e], w2[e]
+    if li.w1_scale is None:
+        ids, _ = (O.route_softmax_topk(ls[:256], cfg.top_k) if cfg.route == "softmax" else
+                  O.route_sigmoid_grouped(ls[:256], li.score_bias.cpu().numpy(), cfg.top_k, cfg.n_group,
+                                          cfg.topk_group, cfg.routed_scaling_factor))
+        for e in sorted(set(ids.reshape(-1).tolist())):   # convert the bf16 weights the sample uses, untimed
+            w1[e], w2[e]
     return O, w1, w2, xs, ls
 
 
-def cpu_baseline(cfg, li, batches, args, budget_s=16.0):
-    """The oracle, as it stands, on a bounded sample of the largest batch:
-    its first S tokens through the whole layer (route, permute, experts,
-    finalize), S grown until the run takes about ``budget_s`` seconds."""
+def _blas_threads(n=None):
+    """Get (n None) or set the thread count of the OpenBLAS that numpy loaded,
+    through the setter it exports; None if no such library or symbol."""
+    import ctypes
+    libs = set()
+    for line in open("/proc/self/maps"):
+        f = line.split()[-1]
+        if f.startswith("/") and "openblas" in os.path.basename(f).lower():
+            libs.add(f)
+    for path in sorted(libs):
+        lib = ctypes.CDLL(path)
+        for pre in ("scipy_openblas", "openblas"):
+            for suf in ("64_", "_64", ""):
+                get, put = f"{pre}_get_num_threads{suf}", f"{pre}_set_num_threads{suf}"
+                if hasattr(lib, get) and hasattr(lib, put):
+                    if n is None:
+                        return int(getattr(lib, get)())
+                    getattr(lib, put)(ctypes.c_int(n))
+                    return n
+    return None
+
+
+def _time_oracle(cfg, li, batches, budget_s):
+    """The oracle, as it stands, on the first S tokens of the largest batch
+    through the whole layer; S grows until a run takes about budget_s / 4."""
     O, w1, w2, xs, ls = _oracle_setup(cfg, li, batches)
-    S, secs = 4, 0.0
+    n = min(xs.shape[0], 4096)
+    S, secs = min(n, 1 if li.w1_scale is not None else 4), 0.0
     while True:
         t = time.perf_counter()
         _oracle_forward(O, cfg, li, w1, w2, xs[:S], ls[:S])
         secs = time.perf_counter() - t
-        if secs * 4 > budget_s or S >= 4096:
+        if secs * 4 > budget_s or S >= n:
             break
-        S *= 4
-    return {"value": S / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {S} tokens of the M={max(batches)} batch through the whole layer "
-                      f"(numpy float64, all BLAS threads), {secs:.2f} s"}
+        S = min(n, S * (2 if li.w1_scale is not None else 4))
+    return S, secs
+
+
+def cpu_baselines(cfg, li, batches, budget_s=12.0):
+    """The oracle (numpy float64) timed on the host cores on a bounded sample
+    of this config's largest batch: with every core numpy's BLAS uses, and on
+    one core (BLAS set to one thread, the calling thread pinned to one CPU).
+    MXFP4 experts are dequantised by the oracle inside the timing."""
+    what = ("including the oracle's dequantisation of every touched MXFP4 expert"
+            if li.w1_scale is not None else "bf16 weights converted to float64 beforehand")
+    S, secs = _time_oracle(cfg, li, batches, budget_s)
+    n_all = _blas_threads() or os.cpu_count()
+    out = {"value": S / secs, "unit": UNIT, "cores": n_all, "kind": "oracle",
+           "sample": f"first {S} tokens of the M={max(batches)} {cfg.name} batch through the whole layer "
+                     f"(numpy float64, {what}), {secs:.2f} s"}
+    prev_aff = os.sched_getaffinity(0)
+    prev_thr = _blas_threads()
+    try:
+        set_ok = _blas_threads(1) == 1
+        os.sched_setaffinity(0, {min(prev_aff)})
+        S1, secs1 = _time_oracle(cfg, li, batches, budget_s)
+    finally:
+        os.sched_setaffinity(0, prev_aff)
+        if prev_thr:
+            _blas_threads(prev_thr)
+    out["one_core"] = {"value": S1 / secs1, "unit": UNIT, "cores": 1 if set_ok else None, "kind": "oracle",
+                       "sample": f"first {S1} tokens, {secs1:.2f} s, one CPU "
+                                 + ("(BLAS set to one thread)" if set_ok else
+                                    "(BLAS thread count could not be set: cores not known)")}
+    return out
 
 
 def run_reference(args):

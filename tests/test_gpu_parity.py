@@ -15,7 +15,8 @@ import torch
 
 import oracle as O
 import synth
-from _helpers import ExpertsF64, lib, max_err, oracle_tokens, sample_tokens, sample_tokens_few_experts, tol
+from _helpers import (ExpertsF64, lib, max_err, oracle_tokens, oracle_tokens_mxfp4, sample_tokens,
+                      sample_tokens_covering, sample_tokens_few_experts, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -276,7 +277,7 @@ def test_bounded_wait_gives_up_and_reports(moe):
 # ------------------------------------------------------------------ whole layer
 
 def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False,
-                 activation="silu", clamp=None, a8=False):
+                 activation="silu", clamp=None, a8=False, few_experts=False):
     cfg = synth.CONFIGS[name]
     li = layer_inputs(name)
     x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
@@ -314,22 +315,35 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
     assert np.array_equal(b.offsets.cpu().numpy(), r_offs)
     assert np.array_equal(b.pmap.cpu().numpy(), r_map)
 
-    # values on a token sample (all tokens when M <= sample size)
-    if cfg.weight_format == "mxfp4":
+    # values on a token sample (all tokens when M <= sample size). MXFP4
+    # experts: the sample covers every expert that any of the M tokens routes
+    # to, with at least `sample` (default 256) tokens; the oracle dequantises
+    # each of those experts once, in a pool of CPU workers.
+    cover = cfg.weight_format == "mxfp4" and not few_experts
+    if cover:
+        toks = sample_tokens_covering(rid, sample or 256, emap_np, seed=M)
+    elif cfg.weight_format == "mxfp4":
         toks = sample_tokens_few_experts(rid, sample or 16, budget=48, seed=M)
     else:
         toks = sample_tokens(M, sample or 256)
     xs = x.to(torch.float64).cpu().numpy()
-    # the oracle dequantises the row-major scale bytes (the A8 layer keeps its
-    # rearranged copy to itself)
-    w1 = ExpertsF64(kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale))
-    w2 = ExpertsF64(kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale))
     shared = None
     if li.ws1 is not None:
         shared = np.zeros((M, cfg.K))
         shared[toks] = O.shared_expert(xs[toks], li.ws1.double().cpu().numpy(), li.ws2.double().cpu().numpy())
-    ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared, activation=activation, clamp=clamp,
-                            qdq=O.mxfp8_qdq if a8 else None)
+    # the oracle dequantises the row-major scale bytes (the A8 layer keeps its
+    # rearranged copy to itself)
+    if cover:
+        ref, ys = oracle_tokens_mxfp4(xs, rid, rw, kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale),
+                                      kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale), toks, emap_np, shared,
+                                      activation=activation, clamp=clamp, mxfp8=a8)
+        if emap_np is None:       # every touched expert was evaluated
+            assert len({int(e) for e in rid[toks].reshape(-1)}) == len(np.unique(rid))
+    else:
+        w1 = ExpertsF64(kw.get("w1", li.w1), kw.get("w1_scale", li.w1_scale))
+        w2 = ExpertsF64(kw.get("w2", li.w2), kw.get("w2_scale", li.w2_scale))
+        ref, ys = oracle_tokens(xs, rid, rw, w1, w2, toks, emap_np, shared, activation=activation, clamp=clamp,
+                                qdq=O.mxfp8_qdq if a8 else None)
     got = b.out.double().cpu().numpy()[toks]
     g2 = b.gemm2.double().cpu().numpy()
     rel = 3e-2 if (cfg.weight_format == "mxfp4" and not a8) else 1e-2
@@ -364,8 +378,7 @@ def test_fused_finalize_layer(moe, name, M, masked):
     """moe_experts_fused_finalize: out within the oracle's bar, and equal to the
     two-pass result (moe_experts + moe_finalize) up to the order of its f32
     additions."""
-    layer, b, x, logits = _check_layer(moe, name, M, masked=masked, fused_finalize=True,
-                                       sample=16 if name == "deepseek" else None)
+    layer, b, x, logits = _check_layer(moe, name, M, masked=masked, fused_finalize=True)
     fused = b.out.clone()
     layer.fused_finalize = False
     b2 = layer.forward(x, logits)
@@ -436,14 +449,24 @@ def test_layer_qwen3(moe, M):
 
 @pytest.mark.parametrize("M", [1, 8, 64, 512, 4096, 8192])
 def test_layer_mixtral(moe, M):
-    _check_layer(moe, "mixtral", M, sample=128 if M > 64 else None)
+    _check_layer(moe, "mixtral", M)
+
+
+# the pages' storage dtype: bf16 routing weights, gemm2_permuted and output
+# (moe_output.py, UnfinalizedMoEOutput), against the oracle rounded to bf16
+@pytest.mark.parametrize("name,M", [("mixtral", 1), ("mixtral", 512), ("mixtral", 8192), ("qwen3", 32),
+                                    ("qwen3", 8192), ("deepseek", 64), ("deepseek", 1024)])
+def test_layer_bf16_storage(moe, name, M):
+    _check_layer(moe, name, M, bf16_storage=True)
 
 
 @pytest.mark.parametrize("M", [1, 64, 1024, 8192])
 def test_layer_deepseek_mxfp4(moe, M):
     """DeepSeek-V3-shaped layer: sigmoid grouped router, MXFP4 routed experts,
-    bf16 shared expert; 3e-2 * RMS against the oracle on the same bytes."""
-    _check_layer(moe, "deepseek", M, sample=16)
+    bf16 shared expert; 3e-2 * RMS against the oracle on the same bytes, on a
+    sample of at least 256 tokens (all of them at M <= 256) that reaches every
+    expert any token routes to."""
+    _check_layer(moe, "deepseek", M)
 
 
 def test_mxfp4_decode_all_codes(moe):
@@ -489,6 +512,43 @@ def test_masked_stress_deferred_finalize(moe):
     assert torch.equal(b2.gemm2[:R], g2_before[:R])                 # deterministic experts
     assert torch.equal(b2.out, fused)                               # deferred == fused, bitwise
     check_no_device_error(moe)
+
+    # The deferred triple consumed by a separate finalize + shared-expert add
+    # (moe_output.py, MoEOutput: whoever finalizes folds the shared output in,
+    # after the routed scale).
+    cfg = synth.CONFIGS["qwen3"]
+    M, k, K = 4096, cfg.top_k, cfg.K
+    F = moe.MOE_DTYPE_F32
+    g = torch.Generator(device=DEV).manual_seed(77)
+    shared = torch.randn(M, K, generator=g, device=DEV)
+    out_d = torch.full((M, K), float("nan"), device=DEV)
+    moe.moe_finalize(b2.gemm2, F, b2.gemm2.shape[0], b2.topk_weights, F, b2.pmap, M, k, K, shared, F, 1.0,
+                     out_d, F)
+    # the same finalize run by moe_experts(do_finalize = 1), bit for bit
+    out_f = torch.full((M, K), float("nan"), device=DEV)
+    g2_f = torch.empty_like(b2.gemm2)
+    moe.moe_experts(layer.cw, b2.x_perm, b2.offsets, M, k, g2_f, F, 1, b2.topk_weights, F, b2.pmap, shared, F,
+                    1.0, out_f, F, b2.exp_ws, b2.exp_ws.numel())
+    torch.cuda.synchronize()
+    check_no_device_error(moe)
+    assert torch.equal(out_d, out_f)
+    # the shared output is added once, after the routed sum
+    scale = float((b2.out.abs() + shared.abs()).max())
+    assert float((out_d - (b2.out + shared)).abs().max()) <= 2 ** -22 * scale
+    # and against the oracle on a token sample
+    li = layer_inputs("qwen3")
+    em, E_l = synth.masked_expert_map(cfg.E, seed=cfg.seed)
+    emap_np = em.numpy()
+    keep = torch.from_numpy(np.nonzero(emap_np >= 0)[0]).to(DEV)
+    rid, rw = O.route_softmax_topk(logits.cpu().numpy(), k)
+    toks = sample_tokens(M, 128, seed=5)
+    xs = x.to(torch.float64).cpu().numpy()
+    sh = np.zeros((M, K))
+    sh[toks] = shared.double().cpu().numpy()[toks]
+    ref, _ = oracle_tokens(xs, rid, rw, ExpertsF64(li.w1[keep].contiguous()), ExpertsF64(li.w2[keep].contiguous()),
+                           toks, emap_np, sh)
+    got = out_d.double().cpu().numpy()[toks]
+    assert max_err(got, ref) <= tol(ref), (max_err(got, ref), tol(ref))
 
 
 def test_complement_mask_additivity(moe):
