@@ -324,6 +324,55 @@ moe_status moe_experts(const moe_weights* w,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_experts_chunked -- the permute and the experts run chunk by chunk over
+ * the tokens, so that the scratch they need is sized by the chunk, not by M:
+ * activation chunking (modular_kernel.py, FusedMoEModularKernel.forward
+ * splits M into chunks of VLLM_FUSED_MOE_CHUNK_SIZE tokens when the experts
+ * object supports chunking, sizes workspace13 and workspace2 for one chunk
+ * -- FusedMoEPermuteExpertsUnpermute.workspace_shapes, whose first dimension
+ * must be the number of tokens -- and runs apply() on each chunk's
+ * activations and topk_ids, writing the chunk's rows of the output).
+ *
+ * For chunk c of tokens [t0, t1), t0 = c * chunk_tokens (the last chunk holds
+ * the ragged tail): the chunk's routes are permuted in the canonical order of
+ * moe_permute (expert-major, then expanded index), its experts run on its
+ * rows, and its unweighted GEMM2 rows land in gemm2_permuted rows
+ * [t0 * top_k, t0 * top_k + R_c). expanded_idx_to_permuted_idx[t, j] (t in
+ * the chunk) is t0 * top_k + the route's row within the chunk, or -1 for a
+ * non-local expert. With do_finalize = 1, moe_finalize then runs over all M
+ * tokens with that map into `out`.
+ *
+ *   x                 bf16 [M, K] token activations (not permuted).
+ *   topk_ids          i32 [M, top_k] global expert ids in [0, E).
+ *   expert_map, E     as in moe_permute (E_local = w->E_local).
+ *   chunk_tokens      >= 1 tokens per chunk; >= M gives one chunk (then the
+ *                     result is moe_permute + moe_experts, bit for bit).
+ *   expanded_idx_to_permuted_idx  out, i32 [M, top_k] (above).
+ *   gemm2_permuted    out, [M * top_k, K] in gemm2_dtype; rows that no map
+ *                     entry points to are not written.
+ *   do_finalize .. out_dtype: as in moe_experts.
+ *   workspace         moe_experts_chunked_workspace_size() bytes, zero-filled
+ *                     before first use (it holds the experts' counters: the
+ *                     moe_experts rule applies). Its size depends on M only
+ *                     through the tail chunk: at most that of chunk_tokens
+ *                     and M mod chunk_tokens tokens.
+ * Errors: those of moe_permute and moe_experts; chunk_tokens <= 0 ->
+ * MOE_ERR_INVALID_ARG. Per-route results equal those of the unchunked
+ * moe_permute + moe_experts up to the launch plan's split-K choice, which
+ * depends on the number of routes in a call (without split-K in both, bit for
+ * bit).
+ * ---------------------------------------------------------------------- */
+size_t moe_experts_chunked_workspace_size(const moe_weights* w, int M, int top_k, int chunk_tokens);
+
+moe_status moe_experts_chunked(const moe_weights* w, const void* x, const int32_t* topk_ids, int M, int top_k,
+                               int E, const int32_t* expert_map, int chunk_tokens,
+                               int32_t* expanded_idx_to_permuted_idx, void* gemm2_permuted, moe_dtype gemm2_dtype,
+                               int do_finalize, const void* expert_weights, moe_dtype weights_dtype,
+                               const void* shared_out, moe_dtype shared_dtype, float routed_scaling_factor,
+                               void* out, moe_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_experts_fused_finalize -- the experts with the finalize folded into
  * GEMM2 (moe_output.py, UnfinalizedMoEOutput: when the routed output is left
  * unfinalized, the top-k reduction can fold into the consumer that runs

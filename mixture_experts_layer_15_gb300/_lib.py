@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
     "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize",
+    "moe_experts_chunked_workspace_size", "moe_experts_chunked",
     "moe_finalize_add_rmsnorm", "moe_experts_batched_workspace_size", "moe_experts_batched", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
@@ -90,6 +91,9 @@ _SIGS = {
     "moe_experts_fused_finalize": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
                                     _P, _Z, _P], _I),
     "moe_experts_launches": ([ctypes.POINTER(moe_weights), _I, _I, _I], _I),
+    "moe_experts_chunked_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I, _I], _Z),
+    "moe_experts_chunked": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _I, _P, _I, _P, _P, _I, _I, _P, _I, _P,
+                             _I, _F, _P, _I, _P, _Z, _P], _I),
     "moe_experts_batched_workspace_size": ([ctypes.POINTER(moe_weights), _I], _Z),
     "moe_experts_batched": ([ctypes.POINTER(moe_weights), _P, _P, _I, _P, _I, _P, _Z, _P], _I),
     "moe_finalize": ([_P, _I, _I, _P, _I, _P, _I, _I, _I, _P, _I, _F, _P, _I, _P], _I),
@@ -205,6 +209,21 @@ def moe_experts(weights: moe_weights, x_perm, expert_offsets, M, top_k, gemm2_pe
                                           _ptr(expanded_idx_to_permuted_idx), _ptr(shared_out),
                                           shared_dtype, routed_scaling_factor, _ptr(out), out_dtype,
                                           _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def moe_experts_chunked_workspace_size(weights: moe_weights, M, top_k, chunk_tokens) -> int:
+    return int(lib.moe_experts_chunked_workspace_size(ctypes.byref(weights), M, top_k, chunk_tokens))
+
+
+def moe_experts_chunked(weights: moe_weights, x, topk_ids, M, top_k, E, expert_map, chunk_tokens,
+                        expanded_idx_to_permuted_idx, gemm2_permuted, gemm2_dtype, do_finalize, expert_weights,
+                        weights_dtype, shared_out, shared_dtype, routed_scaling_factor, out, out_dtype, workspace,
+                        workspace_bytes, stream=None):
+    _check("moe_experts_chunked", lib.moe_experts_chunked(
+        ctypes.byref(weights), _ptr(x), _ptr(topk_ids), M, top_k, E, _ptr(expert_map), chunk_tokens,
+        _ptr(expanded_idx_to_permuted_idx), _ptr(gemm2_permuted), gemm2_dtype, int(do_finalize),
+        _ptr(expert_weights), weights_dtype, _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
+        out_dtype, _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def moe_experts_fused_finalize(weights: moe_weights, x_perm, expert_offsets, M, top_k, expert_weights,

@@ -158,6 +158,38 @@ moe_status check_finalize_args(const void* weights, int wdtype, const int32_t* m
     return MOE_OK;
 }
 
+// Workspace of moe_experts_chunked for chunks of C tokens (the last chunk
+// holds the ragged tail of M): the permute scratch, the chunk's expert
+// offsets, its inverse map, its x_perm rows, then the experts workspace --
+// each sized for the larger of the two chunk shapes, 256-byte aligned.
+struct ChunkLayout {
+    size_t off_offs, off_inv, off_xp, off_exp, exp_bytes, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+ChunkLayout chunk_layout(const moe_weights* w, int M, int top_k, int C, const DeviceInfo& info) {
+    const int first = C < M ? C : M;
+    const int tail = M % first;
+    size_t perm = moe::permute_workspace_bytes(first, top_k, w->E_local);
+    size_t exp = moe::experts_workspace_bytes(w, first * top_k, first, info);
+    if (tail > 0) {
+        const size_t p2 = moe::permute_workspace_bytes(tail, top_k, w->E_local);
+        const size_t e2 = moe::experts_workspace_bytes(w, tail * top_k, tail, info);
+        perm = p2 > perm ? p2 : perm;
+        exp = e2 > exp ? e2 : exp;
+    }
+    const size_t rows = static_cast<size_t>(first) * top_k;
+    ChunkLayout L;
+    L.off_offs = align256(perm);
+    L.off_inv = align256(L.off_offs + sizeof(int32_t) * (w->E_local + 1));
+    L.off_xp = align256(L.off_inv + sizeof(int32_t) * rows);
+    L.off_exp = align256(L.off_xp + rows * w->K * 2);
+    L.exp_bytes = exp;
+    L.total = align256(L.off_exp + exp);
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -477,6 +509,83 @@ moe_status moe_experts(const moe_weights* w, const void* x_perm, const int32_t* 
     return from_cuda(moe::launch_finalize(gemm2_permuted, gemm2_dtype, rows, expert_weights, weights_dtype,
                                           expanded_idx_to_permuted_idx, M, top_k, w->K, shared_out,
                                           shared_dtype, routed_scaling_factor, out, out_dtype, err, stream));
+}
+
+size_t moe_experts_chunked_workspace_size(const moe_weights* w, int M, int top_k, int chunk_tokens) {
+    if (check_weights(w) != MOE_OK || M <= 0 || top_k <= 0 || chunk_tokens <= 0) return 0;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return 0;
+    DeviceInfo info;
+    if (!moe::current_device_info(&info)) info.sm_count = 152;
+    return chunk_layout(w, M, top_k, chunk_tokens, info).total;
+}
+
+moe_status moe_experts_chunked(const moe_weights* w, const void* x, const int32_t* topk_ids, int M, int top_k,
+                               int E, const int32_t* expert_map, int chunk_tokens,
+                               int32_t* expanded_idx_to_permuted_idx, void* gemm2_permuted, moe_dtype gemm2_dtype,
+                               int do_finalize, const void* expert_weights, moe_dtype weights_dtype,
+                               const void* shared_out, moe_dtype shared_dtype, float routed_scaling_factor,
+                               void* out, moe_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    if (M < 0 || top_k <= 0 || chunk_tokens <= 0) return MOE_ERR_INVALID_ARG;
+    const moe_status ws_ok = check_weights(w);
+    if (ws_ok != MOE_OK) return ws_ok;
+    if (do_finalize != 0 && do_finalize != 1) return MOE_ERR_INVALID_ARG;
+    if (!do_finalize && out != nullptr) return MOE_ERR_INVALID_ARG;     // a deferred output has no destination
+    if (!valid_dtype(gemm2_dtype)) return MOE_ERR_INVALID_ARG;
+    // the permute's rules (moe_permute), for the caller's buffers
+    if (E < 1 || top_k > E) return MOE_ERR_INVALID_ARG;
+    if (expert_map == nullptr && w->E_local != E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (M > 0 && (topk_ids == nullptr || expanded_idx_to_permuted_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (do_finalize) {
+        const moe_status a = check_finalize_args(expert_weights, weights_dtype, expanded_idx_to_permuted_idx,
+                                                 shared_out, shared_dtype, out, out_dtype);
+        if (a != MOE_OK) return a;
+        if (out == gemm2_permuted || out == shared_out || out == expert_weights || out == x)
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (M == 0) return MOE_OK;
+    if (x == nullptr || gemm2_permuted == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gemm2_permuted)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    const ChunkLayout L = chunk_layout(w, M, top_k, chunk_tokens, info);
+    if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* offs = reinterpret_cast<int32_t*>(ws + L.off_offs);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + L.off_inv);
+    void* xp = ws + L.off_xp;
+    const int K = w->K;
+    const size_t g2_row = static_cast<size_t>(K) * (gemm2_dtype == MOE_DTYPE_F32 ? 4 : 2);
+    const int C = chunk_tokens < M ? chunk_tokens : M;
+    for (int t0 = 0; t0 < M; t0 += C) {
+        const int Mc = M - t0 < C ? M - t0 : C;
+        const size_t r0 = static_cast<size_t>(t0) * top_k;     // first expanded index of the chunk
+        // the chunk's routes in canonical order; its map entries point at its
+        // rows of gemm2_permuted, [t0 * top_k, t0 * top_k + R_chunk)
+        cudaError_t e = moe::launch_permute(topk_ids + r0, Mc, top_k, E, expert_map, w->E_local,
+                                            static_cast<const uint8_t*>(x) + static_cast<size_t>(t0) * K * 2, K,
+                                            offs, expanded_idx_to_permuted_idx + r0, inv, xp, ws, err, info,
+                                            stream, static_cast<int>(r0));
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        moe::ExpertsProblem p;
+        p.w = w;
+        p.x = xp;
+        p.rows_alloc = Mc * top_k;
+        p.M = Mc;
+        p.offsets = offs;
+        p.single_rows = 0;
+        p.y = static_cast<uint8_t*>(gemm2_permuted) + r0 * g2_row;
+        p.y_dtype = gemm2_dtype;
+        e = moe::launch_experts(p, ws + L.off_exp, L.exp_bytes, err, info, stream);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (!do_finalize) return MOE_OK;
+    return from_cuda(moe::launch_finalize(gemm2_permuted, gemm2_dtype, M * top_k, expert_weights, weights_dtype,
+                                          expanded_idx_to_permuted_idx, M, top_k, K, shared_out, shared_dtype,
+                                          routed_scaling_factor, out, out_dtype, err, stream));
 }
 
 moe_status moe_experts_fused_finalize(const moe_weights* w, const void* x_perm, const int32_t* expert_offsets,

@@ -58,7 +58,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, int M, int top_k, int E,
                            const int32_t* expert_map, int E_local, const void* x, int K,
                            int32_t* expert_offsets, int32_t* map, int32_t* inverse,
                            void* x_perm, void* workspace, int* err, const DeviceInfo& dev,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int map_base = 0);
 
 // Router + single-chunk permute in one kernel (small batches); same results as
 // launch_route followed by launch_permute.

@@ -17,6 +17,11 @@
 // One chunk (M*top_k <= 32*W): a single kernel; every CTA recomputes the tiny
 // sort in shared memory and copies its share of the rows.
 // Several chunks: count -> scan -> scatter -> gather (4 launches).
+//
+// map_base (0 for moe_permute) is added to every non-negative map entry: the
+// chunked experts permute each chunk of tokens on its own and point its map
+// entries at the chunk's rows of the caller's gemm2_permuted. The offsets,
+// the inverse map and x_perm stay relative to the chunk.
 #include "router_device.cuh"
 
 namespace moe {
@@ -90,7 +95,8 @@ __device__ __forceinline__ void permute_single_chunk(const int32_t* ids, int n, 
                                                      const __nv_bfloat16* __restrict__ x, int K,
                                                      int32_t* __restrict__ offsets, int32_t* __restrict__ map,
                                                      int32_t* __restrict__ inverse,
-                                                     __nv_bfloat16* __restrict__ x_perm, int* err, int* sm) {
+                                                     __nv_bfloat16* __restrict__ x_perm, int* err, int* sm,
+                                                     int map_base = 0) {
     const int W = blockDim.x >> 5;
     int* hist = sm;                          // [W][E_l]
     int* total = hist + W * E_l;             // [E_l + 1]
@@ -107,7 +113,7 @@ __device__ __forceinline__ void permute_single_chunk(const int32_t* ids, int n, 
         for (int e = tid; e < E_l; e += blockDim.x) offsets[e] = total[e];
         if (tid == 0) offsets[E_l] = R;
         if (tid < n) {
-            map[tid] = p;
+            map[tid] = p >= 0 ? p + map_base : -1;
             if (p >= 0) inverse[p] = tid;
         }
     }
@@ -128,9 +134,9 @@ __global__ void permute_fused_kernel(const int32_t* __restrict__ ids, int n, int
                                      const __nv_bfloat16* __restrict__ x, int K,
                                      int32_t* __restrict__ offsets, int32_t* __restrict__ map,
                                      int32_t* __restrict__ inverse, __nv_bfloat16* __restrict__ x_perm,
-                                     int* err) {
+                                     int* err, int map_base) {
     extern __shared__ int sm[];
-    permute_single_chunk(ids, n, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, sm);
+    permute_single_chunk(ids, n, top_k, E, emap, E_l, x, K, offsets, map, inverse, x_perm, err, sm, map_base);
 }
 
 // Router and single-chunk permute in one kernel (small batches), launched in
@@ -285,7 +291,7 @@ __global__ void permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchu
 __global__ void permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
                                        const int32_t* __restrict__ emap, int E_l,
                                        const int32_t* __restrict__ chunk_base,
-                                       int32_t* __restrict__ map, int32_t* __restrict__ inverse) {
+                                       int32_t* __restrict__ map, int32_t* __restrict__ inverse, int map_base) {
     extern __shared__ int sm[];
     const int W = blockDim.x >> 5;
     int* hist = sm;
@@ -298,7 +304,7 @@ __global__ void permute_scatter_kernel(const int32_t* __restrict__ ids, int n, i
     int p = -1;
     if (le >= 0)
         p = chunk_base[static_cast<size_t>(blockIdx.x) * E_l + le] + hist[(threadIdx.x >> 5) * E_l + le] + rank;
-    map[i] = p;
+    map[i] = p >= 0 ? p + map_base : -1;
     if (p >= 0) inverse[p] = i;
 }
 
@@ -375,7 +381,7 @@ size_t permute_workspace_bytes(int M, int top_k, int E_local) {
 cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const int32_t* emap,
                            int E_l, const void* x, int K, int32_t* offsets, int32_t* map,
                            int32_t* inverse, void* x_perm, void* ws, int* err,
-                           const DeviceInfo& dev, cudaStream_t s) {
+                           const DeviceInfo& dev, cudaStream_t s, int map_base) {
     const int n = M * top_k;
     const int W = warps_per_chunk(E_l);
     const int threads = 32 * W;
@@ -394,7 +400,7 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
             grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
         }
         return launch_pdl(permute_fused_kernel, dim3(grid), dim3(t1), smem, s, ids, n, top_k, E, emap, E_l,
-                          xb, K, offsets, map, inverse, xp, err);
+                          xb, K, offsets, map, inverse, xp, err, map_base);
     }
     int32_t* chunk = static_cast<int32_t*>(ws);
     const size_t smem_h = sizeof(int) * (W * E_l + E_l);
@@ -405,7 +411,7 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
                    offsets);
     if (e != cudaSuccess) return e;
     e = launch_pdl(permute_scatter_kernel, dim3(nchunks), dim3(threads), smem_h, s, ids, n, E, emap, E_l,
-                   static_cast<const int32_t*>(chunk), map, inverse);
+                   static_cast<const int32_t*>(chunk), map, inverse, map_base);
     if (e != cudaSuccess || x_perm == nullptr) return e;
     const int rows_per_block = 8;   // 256 threads, one warp per row
     int grid = ceil_div(n, rows_per_block);

@@ -80,7 +80,7 @@ __all__ = [
     "permute", "expert_mlp", "experts", "finalize", "shared_expert",
     "moe_forward", "bf16_round", "gelu_erf", "experts_batched", "add_rmsnorm",
     "finalize_add_rmsnorm", "E4M3_MAX", "e4m3_value", "e4m3_round", "mxfp8_scale_byte",
-    "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_qdq", "experts_mxfp8",
+    "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_qdq", "experts_mxfp8", "experts_chunked",
 ]
 
 # --------------------------------------------------------------------------
@@ -466,6 +466,31 @@ def experts(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,
             toks = np.asarray(inverse[r0:r1], dtype=np.int64) // top_k
             out[r0:r1] = expert_mlp(x[toks], w1[le], w2[le], activation, clamp, qdq)
     return out
+
+
+def experts_chunked(x: np.ndarray, topk_ids: np.ndarray, w1, w2, E: int, chunk_tokens: int,
+                    expert_map=None, activation: str = "silu", clamp=None):
+    """Activation chunking (modular_kernel.py, FusedMoEModularKernel.forward:
+    M is split into chunks of CHUNK_SIZE tokens and the experts' apply() runs
+    on each chunk's activations and topk_ids, writing that chunk's slice of
+    the output). Chunk c holds tokens [t0, t1), t0 = c * chunk_tokens; its
+    routes are permuted on their own (the canonical order of ``permute``),
+    its expert outputs fill rows [t0 * k, t0 * k + R_c) of a [M * k, K]
+    gemm2_permuted, and its map entries are offset by t0 * k to point there.
+    Returns (map int32 [M, k] with -1 for masked routes, gemm2_permuted
+    float64 [M * k, K] with NaN in rows no map entry points to)."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    M, k = ids.shape
+    x = np.asarray(x, dtype=np.float64)
+    pmap = np.full((M, k), -1, dtype=np.int32)
+    g2 = np.full((M * k, w2.shape[1]), np.nan)
+    for t0 in range(0, M, chunk_tokens):
+        t1 = min(M, t0 + chunk_tokens)
+        offsets, m, inverse, _ = permute(ids[t0:t1], E, expert_map)
+        R = int(offsets[-1])
+        g2[t0 * k:t0 * k + R] = experts(x[t0:t1], w1, w2, offsets, inverse, k, activation, clamp)
+        pmap[t0:t1] = np.where(m >= 0, m + t0 * k, -1)
+    return pmap, g2
 
 
 def experts_mxfp8(x: np.ndarray, w1: np.ndarray, w2: np.ndarray, offsets: np.ndarray,

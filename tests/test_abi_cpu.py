@@ -191,3 +191,26 @@ def test_permute_noalloc_validates_like_moe_permute(moe):
     M = (1 << 18) + 128
     assert moe.moe_permute_workspace_size(M, 8, 128) > (1 << 20)
     assert na(M, 8, 128, None, 128) == moe.MOE_ERR_WORKSPACE
+
+
+def test_chunked_workspace_is_sized_by_the_chunk(moe):
+    """Activation chunking caps the scratch: the chunked workspace depends on
+    M only through the ragged tail, so it is the same for every multiple of
+    the chunk, and far below the unchunked permute + experts workspaces."""
+    w = moe.make_weights(0, 128, 2048, 768, 0x1000, 0x1000)
+    a = moe.moe_experts_chunked_workspace_size(w, 8192, 8, 1024)
+    b = moe.moe_experts_chunked_workspace_size(w, 4096, 8, 1024)
+    c = moe.moe_experts_chunked_workspace_size(w, 65536, 8, 1024)
+    assert a == b == c > 0
+    whole = moe.moe_experts_workspace_size(w, 65536, 8) + 65536 * 8 * 2048 * 2
+    assert c * 8 < whole
+    assert moe.moe_experts_chunked_workspace_size(w, 8192, 8, 0) == 0
+    P = 0x1000
+    F = moe.MOE_DTYPE_F32
+    call = lambda M, k, E, chunk, fin, out: _status(moe.moe_experts_chunked, w, P, P, M, k, E, None, chunk, P, P,
+                                                    F, fin, P, F, None, F, 1.0, out, F, P, 1 << 30)
+    assert call(64, 8, 128, 0, 1, P + 4096) == moe.MOE_ERR_INVALID_ARG       # chunk_tokens >= 1
+    assert call(64, 8, 128, 16, 0, P + 4096) == moe.MOE_ERR_INVALID_ARG      # deferred: no destination
+    assert call(64, 8, 64, 16, 1, P + 4096) == moe.MOE_ERR_INVALID_ARG       # no map: E_local must be E
+    assert call(-1, 8, 128, 16, 1, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(0, 8, 128, 16, 0, None) == 0                                  # nothing to do

@@ -651,3 +651,48 @@ def test_experts_mxfp8_quantises_both_gemm_inputs():
     # first-order bound: |dy| <= |W2| (|da|), |da| <= 2^-4 |a| + |d act / dh| |W1| |dx| (loose, x4)
     rel = np.linalg.norm(got - exact) / np.linalg.norm(exact)
     assert 1e-4 < rel < 0.1
+
+
+# ---------------------------------------------------------------- activation chunking
+
+@pytest.mark.parametrize("chunk,masked", [(1, False), (3, True), (7, False), (16, True), (40, False)])
+def test_experts_chunked(chunk, masked):
+    """Chunked experts (one permute + experts per chunk of tokens): each
+    chunk's map entries are a bijection onto its own rows [t0*k, t0*k + R_c);
+    every route's row holds the same expert output as without chunking; the
+    finalize of the chunked triple equals the unchunked one; a chunk of at
+    least M tokens is the plain permute."""
+    rng = np.random.default_rng(31 + chunk)
+    M, K, N, E, k = 23, 32, 48, 6, 2
+    x = rng.standard_normal((M, K))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    w = rng.random((M, k))
+    emap = None
+    E_l = E
+    if masked:
+        emap = np.array([0, -1, 1, 2, -1, 3], np.int32)
+        E_l = 4
+    w1 = rng.standard_normal((E_l, 2 * N, K)) / np.sqrt(K)
+    w2 = rng.standard_normal((E_l, K, N)) / np.sqrt(N)
+    offs, pmap, inv, _ = O.permute(ids, E, emap)
+    g2 = O.experts(x, w1, w2, offs, inv, k)
+    cmap, cg2 = O.experts_chunked(x, ids, w1, w2, E, chunk, emap)
+    assert cmap.shape == (M, k) and cg2.shape == (M * k, K)
+    assert np.array_equal(cmap < 0, pmap < 0)                       # -1 exactly on masked routes
+    for t0 in range(0, M, chunk):
+        t1 = min(M, t0 + chunk)
+        part = cmap[t0:t1].reshape(-1)
+        valid = part[part >= 0]
+        assert sorted(valid.tolist()) == list(range(t0 * k, t0 * k + valid.size))
+    for t in range(M):
+        for j in range(k):
+            if pmap[t, j] >= 0:
+                np.testing.assert_allclose(cg2[cmap[t, j]], g2[pmap[t, j]], rtol=1e-12, atol=1e-14)
+    out = O.finalize(g2, w, pmap, None, 1.0)
+    cout = O.finalize(cg2, w, cmap, None, 1.0)
+    assert np.all(np.isfinite(cout))                                # unused (NaN) rows never read
+    np.testing.assert_allclose(cout, out, rtol=1e-12, atol=1e-14)
+    whole_map, whole_g2 = O.experts_chunked(x, ids, w1, w2, E, M, emap)
+    assert np.array_equal(whole_map, pmap)
+    R = int(offs[-1])
+    np.testing.assert_allclose(whole_g2[:R], g2, rtol=1e-12, atol=1e-14)
