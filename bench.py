@@ -144,7 +144,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_workload(cfg_name, device, only_m=None, experts=0, mxfp8_act=False):
+def make_workload(cfg_name, device, only_m=None, experts=0, mxfp8_act=False, mxfp4_path="a16"):
     import dataclasses
     import mixture_experts_layer_15_gb300 as moe
     cfg = synth.CONFIGS[cfg_name]
@@ -154,7 +154,12 @@ def make_workload(cfg_name, device, only_m=None, experts=0, mxfp8_act=False):
             kw.update(n_group=min(cfg.n_group, experts // 2), topk_group=min(cfg.topk_group, experts // 2))
         cfg = dataclasses.replace(cfg, **kw)
     li = synth.make_layer(cfg, device)
-    fmt = moe.MOE_WEIGHTS_MXFP4 if cfg.weight_format == "mxfp4" else moe.MOE_WEIGHTS_BF16
+    # MXFP4 weights with bf16 activations (W4A16) run on the block-scaled
+    # tensor cores (each activation as two E4M3 terms, MOE_WEIGHTS_MXFP4_A16);
+    # mxfp4_path="decode" takes the decode-to-bf16 kernel instead
+    fmt = moe.MOE_WEIGHTS_BF16
+    if cfg.weight_format == "mxfp4":
+        fmt = moe.MOE_WEIGHTS_MXFP4 if mxfp4_path == "decode" else moe.MOE_WEIGHTS_MXFP4_A16
     if mxfp8_act and cfg.weight_format == "mxfp4":
         fmt = moe.MOE_WEIGHTS_MXFP4_A8
     layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
@@ -397,14 +402,18 @@ def roofline_objects(per_m, pk, traffic=None, mult=1.0, kernel=None):
 def other_config(moe, name, args, pk, dev, stream, cpu=False):
     """The same measurement on another config (reported beside the headline),
     with the oracle baseline on the host cores when ``cpu``."""
-    cfg, li, layer, batches = make_workload(name, dev)
+    cfg, li, layer, batches = make_workload(name, dev, mxfp4_path=args.mxfp4_path)
     sweep = sorted(batches)
     forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
     warm_up(moe, layer, sweep, forward, 3)
     steps = max(5, args.steps // 5)
     secs, per_m, gf, gs, _ = timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk)
+    wf = cfg.weight_format + " weights"
+    if cfg.weight_format == "mxfp4":
+        wf += (", bf16 activations decoded" if args.mxfp4_path == "decode" else
+               ", bf16 activations as two E4M3 terms on block-scaled MMAs (W4A16)")
     out = {"workload": f"{cfg.name}-shaped MoE layer (K={cfg.K}, N={cfg.N}, E={cfg.E}, top_k={cfg.top_k}, "
-                       f"{cfg.weight_format} weights{', shared expert' if cfg.shared_N else ''})",
+                       f"{wf}{', shared expert' if cfg.shared_N else ''})",
            "tokens_per_s": sum(sweep) * steps / secs, "steps": steps, "gemm_tflops": gf / gs / 1e12,
            "roofline": roofline_objects(per_m, pk),
            "sweep": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()} for r in per_m]}
@@ -556,13 +565,14 @@ def next_rows(moe, pk, dev, stream):
     del xb, counts, yb, wsb
     del li, x, logits, batches
     torch.cuda.empty_cache()
-    out["mxfp8_activations"] = a8_rows(moe, pk, dev, stream, scrub)
+    out["mxfp4_paths"] = a8_rows(moe, pk, dev, stream, scrub,
+                                 fmts=(moe.MOE_WEIGHTS_MXFP4, moe.MOE_WEIGHTS_MXFP4_A16, moe.MOE_WEIGHTS_MXFP4_A8))
     del buf
     torch.cuda.empty_cache()
     return out
 
 
-def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192)):
+def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192), fmts=None):
     """The DeepSeek-shaped layer with its MXFP4 routed experts on MXFP8
     activations (block-scaled MMAs, MOE_WEIGHTS_MXFP4_A8) beside the same
     layer on bf16 activations: the whole forward (route + permute, shared
@@ -576,8 +586,11 @@ def a8_rows(moe, pk, dev, stream, scrub, sweep=(1, 64, 1024, 8192)):
     li = synth.make_layer(cfg, dev)
     batches = {M: synth.make_tokens(cfg, M, dev, li) for M in sweep}
     rows = []
-    for fmt, tag in ((moe.MOE_WEIGHTS_MXFP4, "bf16 activations (decode to bf16, kind::f16)"),
-                     (moe.MOE_WEIGHTS_MXFP4_A8, "MXFP8 activations (kind::mxf8f6f4 block-scaled)")):
+    tags = {moe.MOE_WEIGHTS_MXFP4: "bf16 activations (decode to bf16, kind::f16)",
+            moe.MOE_WEIGHTS_MXFP4_A16: "bf16 activations as two E4M3 terms (kind::mxf8f6f4 block-scaled)",
+            moe.MOE_WEIGHTS_MXFP4_A8: "MXFP8 activations (kind::mxf8f6f4 block-scaled)"}
+    for fmt in (fmts or (moe.MOE_WEIGHTS_MXFP4, moe.MOE_WEIGHTS_MXFP4_A8)):
+        tag = tags[fmt]
         layer = moe.MoELayer(K=cfg.K, N=cfg.N, E=cfg.E, top_k=cfg.top_k, w1=li.w1, w2=li.w2,
                              w1_scale=li.w1_scale, w2_scale=li.w2_scale, fmt=fmt, route="sigmoid",
                              score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
@@ -630,7 +643,7 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     stream = torch.cuda.current_stream()
-    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts, args.mxfp8_act)
+    cfg, li, layer, batches = make_workload(args.config, dev, args.m, args.experts, args.mxfp8_act, args.mxfp4_path)
     sweep = sorted(batches)
     forward = make_forward(moe, cfg, layer, batches, stream, args.finalize)
     warm_up(moe, layer, sweep, forward, args.warmup)
@@ -929,6 +942,9 @@ def main():
                     help="other configs measured after the headline one and reported beside it ('' = none)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: keep the first N experts of the config (not the benchmark workload)")
+    ap.add_argument("--mxfp4-path", default="a16", choices=["a16", "decode"],
+                    help="MXFP4 weights with bf16 activations: on the block-scaled MMAs (two E4M3 terms per "
+                         "activation) or decoded to bf16 in shared memory")
     ap.add_argument("--mxfp8-act", action="store_true",
                     help="profiling only: MXFP4 configs run their experts on MXFP8 activations "
                          "(MOE_WEIGHTS_MXFP4_A8; not the benchmark workload)")

@@ -71,8 +71,11 @@ typedef enum moe_route_method {
 typedef enum moe_weight_format {
     MOE_WEIGHTS_BF16 = 0,          /* bf16 weights                                     */
     MOE_WEIGHTS_MXFP4 = 1,         /* e2m1 codes, two per byte, + one E8M0 byte per 32 */
-    MOE_WEIGHTS_MXFP4_A8 = 2       /* MXFP4 weights, scales as moe_mx_prepare_scales
+    MOE_WEIGHTS_MXFP4_A8 = 2,      /* MXFP4 weights, scales as moe_mx_prepare_scales
                                       writes them; activations quantised to MXFP8   */
+    MOE_WEIGHTS_MXFP4_A16 = 3      /* MXFP4 weights, scales as moe_mx_prepare_scales
+                                      writes them; bf16 activations (W4A16) on the
+                                      block-scaled tensor cores                      */
 } moe_weight_format;
 
 /*
@@ -105,6 +108,18 @@ typedef enum moe_weight_format {
  *          Outputs therefore differ from the MXFP4 format's by the
  *          activations' quantisation error. K % 256 == 0, N % 128 == 0;
  *          moe_experts and moe_experts_fused_finalize only.
+ *   MXFP4_A16: weights as for MXFP4_A8 (codes, prepared scales), bf16
+ *          activations: the W4A16 computation of MOE_WEIGHTS_MXFP4 -- the
+ *          same bf16 x and the same bf16 rounding of the activation output --
+ *          run on the block-scaled tensor cores instead of a decode to bf16.
+ *          Each bf16 value v of a 32-element block is written as two E4M3
+ *          terms, hi = e4m3(v / s1) * s1 and lo = e4m3((v - hi) / s2) * s2,
+ *          s1, s2 the smallest powers of two that keep the block's codes
+ *          within 448 (no saturation); hi + lo == v exactly for every v within
+ *          2^14 of its block's largest magnitude (the error of the others is
+ *          below 2^-21 of that magnitude). The MMAs take the two terms as two
+ *          B rows per token and the epilogues add their accumulators. Same
+ *          limits as MXFP4_A8.
  *
  * K and N must be multiples of 128 (of 512 for MXFP4). All pointers 16-byte
  * aligned.
@@ -509,6 +524,17 @@ moe_status moe_shared_expert(const void* ws1, const void* ws2, int K, int Ns,
  * ---------------------------------------------------------------------- */
 moe_status moe_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales,
                               cudaStream_t stream);
+
+/* moe_e4m3_split: the activation format of MOE_WEIGHTS_MXFP4_A16 on its own.
+ * x bf16 [rows, C] -> codes u8 [2 * rows, C] and E8M0 scale bytes u8
+ * [2 * rows, C/32]; rows 2p and 2p + 1 hold the hi and lo terms of row p: for
+ * every block of 32 consecutive values, hi = e4m3(v / s1) and
+ * lo = e4m3((v - hi * s1) / s2) (nearest, ties to even), s1 and s2 the
+ * smallest powers of two 2^(b - 127) with the block's largest |v| (|v - hi s1|
+ * for s2) at most 448 * s (b kept in 1..254). hi * s1 + lo * s2 == v for every v
+ * within 2^14 of its block's largest magnitude. C % 128 == 0
+ * (MOE_ERR_ALIGNMENT); x and codes 16-byte aligned. rows == 0 is a no-op. */
+moe_status moe_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 size_t moe_mx_prepared_scales_size(int E_local, int rows, int cols);
 moe_status moe_mx_prepare_scales(const uint8_t* scales, int E_local, int rows, int cols, uint8_t* out,
                                  cudaStream_t stream);

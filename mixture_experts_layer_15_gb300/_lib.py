@@ -30,6 +30,7 @@ MOE_ROUTE_SIGMOID_GROUPED_TOPK = 1
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_MXFP4 = 1
 MOE_WEIGHTS_MXFP4_A8 = 2
+MOE_WEIGHTS_MXFP4_A16 = 3
 MOE_ACT_SILU = 0
 MOE_ACT_GELU = 1
 
@@ -43,7 +44,7 @@ EXPORTS = (
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
     "moe_debug_sigmoid", "moe_debug_bounded_wait",
-    "moe_mxfp8_quantize", "moe_mx_prepared_scales_size", "moe_mx_prepare_scales",
+    "moe_mxfp8_quantize", "moe_mx_prepared_scales_size", "moe_mx_prepare_scales", "moe_e4m3_split",
 )
 
 
@@ -108,6 +109,7 @@ _SIGS = {
     "moe_debug_sigmoid": ([_P, _P, _I, _P], _I),
     "moe_debug_bounded_wait": ([_P, _I, ctypes.c_ulonglong, _P], _I),
     "moe_mxfp8_quantize": ([_P, _I, _I, _P, _P, _P], _I),
+    "moe_e4m3_split": ([_P, _I, _I, _P, _P, _P], _I),
     "moe_mx_prepared_scales_size": ([_I, _I, _I], _Z),
     "moe_mx_prepare_scales": ([_P, _I, _I, _I, _P, _P], _I),
 }
@@ -307,6 +309,10 @@ def moe_debug_sigmoid(x, y, n, stream=None):
 def moe_mxfp8_quantize(x, rows, C, codes, scales, stream=None):
     _check("moe_mxfp8_quantize", lib.moe_mxfp8_quantize(_ptr(x), rows, C, _ptr(codes), _ptr(scales),
                                                          _stream(stream)))
+
+
+def moe_e4m3_split(x, rows, C, codes, scales, stream=None):
+    _check("moe_e4m3_split", lib.moe_e4m3_split(_ptr(x), rows, C, _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def moe_mx_prepared_scales_size(E_local, rows, cols):

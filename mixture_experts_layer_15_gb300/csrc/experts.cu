@@ -135,6 +135,21 @@ GemmPlan plan_gemm(int gemm_index, int bt, int na, int n_wtiles, int kr, int row
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Counters at the start of the workspace, kept zero between calls: four
+// regions of kMaxSplitTiles (split-K arrivals of GEMM1 and GEMM2, token-tile
+// ready and consumed counts), then the output-start counters of a fused
+// finalizing launch (KernelArgs::init_done).
+constexpr size_t kCounterBytes = (4 * static_cast<size_t>(kMaxSplitTiles) + 64) * sizeof(int);
+
+// A finalizing call's output start, written by its GEMM1 launch: out = the
+// shared expert's output, or 0.
+void set_out_init(GemmArgs& a, const ExpertsProblem& p) {
+    a.init_out = p.fin_out;
+    a.init_src = p.fin_shared;
+    a.init_src_dtype = p.fin_shared_dtype;
+    a.init_n = static_cast<long long>(p.M) * p.w->K;
+}
+
 struct Layout {
     int bt;
     bool fused;
@@ -146,28 +161,35 @@ struct Layout {
     size_t off_xq = 0, off_xs = 0, off_aq = 0, off_as = 0;
 };
 
-// MXFP4 weights x MXFP8 activations: three launches (quantise x, GEMM1 with
-// the quantising epilogue, GEMM2), token tiles of at most 128 rows (one scale
-// atom per tile and k-block). Plans count k-blocks of 128 elements.
+// MXFP4 weights on the block-scaled MMAs: three launches (quantise x, GEMM1
+// with the quantising epilogue, GEMM2), token tiles of at most 128 B rows (one
+// scale atom per tile and k-block). MXFP8 activations (A8): one B row per
+// token. bf16 activations as two E4M3 terms (A16): two B rows per token, so
+// tiles of at most 64 tokens and twice the code buffers. L.bt counts tokens.
+// Plans count k-blocks of 128 elements.
 Layout make_layout_a8(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin) {
     Layout L;
     const int K = w->K, N = w->N;
+    const int rb = w->format == MOE_WEIGHTS_MXFP4_A16 ? 2 : 1;       // B rows per token
     L.bt = g_override.token_tile > 0 ? g_override.token_tile : pick_bt(M, rows_alloc, groups, K, N, false);
-    if (L.bt > 128) L.bt = 128;
+    if (L.bt > 128 / rb) L.bt = 128 / rb;
     L.g1 = plan_gemm(0, L.bt, 2, N / kBM, K / 2, rows_alloc, groups, sm_count);
     L.g2 = plan_gemm(1, L.bt, 2, K / (2 * kBM), N / 2, rows_alloc, groups, sm_count, fin);
+    // a split's fp32 partial tile holds every B row of the token tile: rb rows per token
+    L.g1.partial_bytes *= rb;
+    L.g2.partial_bytes *= rb;
     L.fused = false;
     L.pair = false;
     L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
     const size_t tiles = static_cast<size_t>(L.max_token_tiles);
-    size_t off = 4 * kMaxSplitTiles * sizeof(int);
+    size_t off = kCounterBytes;
     L.off_act = 0;
     L.off_xq = off;
-    off = align256(off + static_cast<size_t>(rows_alloc) * K);
+    off = align256(off + static_cast<size_t>(rb) * rows_alloc * K);
     L.off_xs = off;
     off = align256(off + tiles * (K / gemm::kMxBK) * gemm::kAtom);
     L.off_aq = off;
-    off = align256(off + static_cast<size_t>(rows_alloc) * N);
+    off = align256(off + static_cast<size_t>(rb) * rows_alloc * N);
     L.off_as = off;
     off = align256(off + tiles * (N / gemm::kMxBK) * gemm::kAtom);
     L.off_p1 = off;
@@ -182,7 +204,8 @@ Layout make_layout_a8(const moe_weights* w, int rows_alloc, int M, int groups, i
 // batched: the BatchedExperts layout, which runs as two one-CTA launches
 Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin = false,
                    bool batched = false) {
-    if (w->format == MOE_WEIGHTS_MXFP4_A8) return make_layout_a8(w, rows_alloc, M, groups, sm_count, fin);
+    if (w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16)
+        return make_layout_a8(w, rows_alloc, M, groups, sm_count, fin);
     Layout L;
     const int K = w->K, N = w->N;
     L.bt = g_override.token_tile > 0 ? g_override.token_tile
@@ -227,7 +250,7 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     }
     // four counter regions, kept zero between calls: split-K arrivals of
     // GEMM1 and GEMM2, token-tile ready and consumed counts
-    size_t off = 4 * kMaxSplitTiles * sizeof(int);
+    size_t off = kCounterBytes;
     L.off_act = off;
     off = align256(off + static_cast<size_t>(rows_alloc) * N * 2);
     L.off_p1 = off;
@@ -261,6 +284,9 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     const int K = w->K, N = w->N;
     const uint64_t E = static_cast<uint64_t>(w->E_local);
     const bool fin = p.fin_out != nullptr;
+    const bool hl = w->format == MOE_WEIGHTS_MXFP4_A16;
+    const int rb = hl ? 2 : 1;                                   // B rows per token
+    const uint64_t brows = static_cast<uint64_t>(rb) * p.rows_alloc;
     uint8_t* xq = ws + L.off_xq;
     uint8_t* xs = ws + L.off_xs;
     uint8_t* aq = ws + L.off_aq;
@@ -268,9 +294,9 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     int* counters = reinterpret_cast<int*>(ws);
     CUtensorMap tA1, tB1, tA2, tB2;
     if (!encode_fp4(&tA1, w->w1, K, E * 2 * N) || !encode_fp4(&tA2, w->w2, N, E * K) ||
-        !encode_2d(&tB1, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, p.rows_alloc, gemm::kMxBK, L.bt,
+        !encode_2d(&tB1, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, brows, gemm::kMxBK, rb * L.bt,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tB2, aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, p.rows_alloc, gemm::kMxBK, L.bt,
+        !encode_2d(&tB2, aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, brows, gemm::kMxBK, rb * L.bt,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     gemm::Mx8Args m1{};
@@ -298,6 +324,7 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     m1.max_token_tiles = L.max_token_tiles;
     gemm::Mx8Args m2 = m1;
     GemmArgs& a2 = m2.g;
+    a2.init_out = nullptr;
     a2.kr = N;
     a2.rows_per_group = K;
     a2.n_wtiles = L.g2.n_wtiles;
@@ -318,17 +345,14 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     m2.sfb = as;
     m2.sfb_out = nullptr;
     const int grid = dev.sm_count;
-    cudaError_t e;
-    if (fin) {
-        e = launch_out_init(p.fin_shared, p.fin_shared_dtype, p.M, K, p.fin_out, dev, s);
-        if (e != cudaSuccess) return e;
-    }
-    e = launch_mxfp8_quantize_tiles(p.x, p.rows_alloc, K, p.offsets, w->E_local, L.bt, L.max_token_tiles, xq, xs,
-                                    err, dev, s);
+    if (fin) set_out_init(a1, p);                       // GEMM1 writes the output start
+    cudaError_t e = launch_mxfp8_quantize_tiles(p.x, p.rows_alloc, K, p.offsets, w->E_local, L.bt, L.max_token_tiles, xq, xs,
+                                    err, dev, s, hl);
     if (e != cudaSuccess) return e;
-    e = gemm::launch_gemm_mx8(gemm::MODE_SWIGLU, L.bt, MOE_DTYPE_BF16, tA1, tB1, m1, grid, s);
+    auto gemm_launch = hl ? gemm::launch_gemm_mx8_hl : gemm::launch_gemm_mx8;
+    e = gemm_launch(gemm::MODE_SWIGLU, rb * L.bt, MOE_DTYPE_BF16, tA1, tB1, m1, grid, s);
     if (e != cudaSuccess) return e;
-    return gemm::launch_gemm_mx8(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, L.bt, p.y_dtype, tA2, tB2, m2, grid, s);
+    return gemm_launch(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, rb * L.bt, p.y_dtype, tA2, tB2, m2, grid, s);
 }
 
 cudaError_t launch_one(bool mx, int fused, int mode, int bt, int na, int out_dtype, const gemm::Maps& m,
@@ -368,9 +392,9 @@ cudaError_t launch_debug_bounded_wait(const int* flag, int target, unsigned long
 }
 
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev) {
-    if (w->format == MOE_WEIGHTS_MXFP4_A8) return (fin ? 1 : 0) + 3;
+    if (w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16) return 3;
     const Layout L = make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, fin);
-    return (fin ? 1 : 0) + ((L.pair || !L.fused) ? 2 : 1);
+    return (L.pair || !L.fused) ? 2 : 1;
 }
 
 cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*workspace_bytes*/, int* err,
@@ -387,7 +411,8 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     void* act = ws + L.off_act;
 
     const uint64_t E = static_cast<uint64_t>(w->E_local);
-    if (w->format == MOE_WEIGHTS_MXFP4_A8) return launch_experts_a8(p, L, ws, err, dev, s);
+    if (w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16)
+        return launch_experts_a8(p, L, ws, err, dev, s);
 
     gemm::Maps m;
     if (!encode_weights(&m.A[0], &m.S[0], mx, w->w1, w->w1_scale, K, E * 2 * N) ||
@@ -419,6 +444,7 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
     a1.batch_stride = p.batch_stride;
     GemmArgs& a2 = ka.g[1];
     a2 = a1;
+    a2.init_out = nullptr;
     a2.kr = N;
     a2.rows_per_group = K;
     a2.n_wtiles = L.g2.n_wtiles;
@@ -441,9 +467,10 @@ cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*wo
 
     const int grid = dev.sm_count;
     if (fin) {
-        // out = shared (or 0) first; the GEMM2 epilogue adds every route into it
-        const cudaError_t e0 = launch_out_init(p.fin_shared, p.fin_shared_dtype, p.M, K, p.fin_out, dev, s);
-        if (e0 != cudaSuccess) return e0;
+        // out = shared (or 0), written by GEMM1's launch before GEMM2's
+        // epilogues add every route into it
+        set_out_init(a1, p);
+        ka.init_done = counters + 4 * kMaxSplitTiles;
     }
     if (L.pair) {
         // the same units as the one-CTA plan; each CTA of a pair holds half of

@@ -82,43 +82,7 @@ cudaError_t launch_shared(int shared_dtype, int out_dtype, const void* g2, int n
     return launch_out<GT, __nv_bfloat16>(out_dtype, g2, num_rows, w, wdtype, map, M, top_k, K, shared, rsf, out, err, s);
 }
 
-// out = shared (or 0): the starting value of the fused finalize, whose GEMM2
-// epilogue then adds rsf * w * y of every route into out. Waits for the
-// previous kernel of the stream before it finishes, so the next kernel's
-// programmatic wait also covers everything before this one.
-template <typename ST>
-__global__ void __launch_bounds__(256)
-out_init_kernel(const ST* __restrict__ shared, size_t n8, float* __restrict__ out) {
-    pdl_wait();
-    pdl_trigger();
-    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-        float v[8];
-        if (shared != nullptr) {
-            Vec8<ST>::load(shared + i * 8, v);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-        }
-        Vec8<float>::store(out + i * 8, v);
-    }
-}
-
 }  // namespace
-
-cudaError_t launch_out_init(const void* shared, int shared_dtype, int M, int K, float* out, const DeviceInfo& dev,
-                            cudaStream_t s) {
-    const size_t n8 = static_cast<size_t>(M) * K / 8;
-    if (n8 == 0) return cudaSuccess;
-    size_t blocks = (n8 + 255) / 256;
-    const size_t cap = static_cast<size_t>(dev.sm_count > 0 ? dev.sm_count : 152) * 8;
-    if (blocks > cap) blocks = cap;
-    if (shared_dtype == MOE_DTYPE_F32 || shared == nullptr)
-        return launch_pdl(out_init_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                          static_cast<const float*>(shared), n8, out);
-    return launch_pdl(out_init_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                      static_cast<const __nv_bfloat16*>(shared), n8, out);
-}
 
 cudaError_t launch_finalize(const void* g2, int g2_dtype, int num_rows, const void* w, int wdtype,
                             const int32_t* map, int M, int top_k, int K, const void* shared,

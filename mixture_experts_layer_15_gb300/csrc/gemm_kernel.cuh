@@ -126,6 +126,16 @@ struct GemmArgs {
     int fw_dtype;
     int top_k;
     float rsf;
+    // The start of a folded finalize's f32 output, written by this launch
+    // (GEMM1 of a finalizing experts call): init_out[i] = init_src[i]
+    // (init_src_dtype; the shared expert's output) or 0, for i < init_n (a
+    // multiple of 4). Each CTA's epilogue threads write an even share of it
+    // before their first accumulator, so it overlaps the mainloop. nullptr:
+    // nothing to write.
+    float* init_out;
+    const void* init_src;
+    int init_src_dtype;
+    long long init_n;
 };
 
 // Arguments of one launch: a single GEMM (nphase = 1), or GEMM1 followed by
@@ -140,6 +150,11 @@ struct KernelArgs {
     int* ready;                  // [token tiles]
     int* consumed;               // [token tiles]
     int max_token_tiles;
+    // fused launches that write a finalize's output start (g[0].init_out):
+    // init_done[0] counts the CTAs whose share is written (GEMM2's reductions
+    // wait for all of them); init_done[1] counts the CTAs that have finished,
+    // and the last one returns both to zero
+    int* init_done;
 };
 
 template <int BT, int NA, bool MX>
@@ -286,6 +301,30 @@ __device__ __forceinline__ void store_out<float>(float* p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float v) {
     *p = __float2bfloat16_rn(v);
+}
+
+// This CTA's share of a folded finalize's output start (GemmArgs::init_out):
+// 16-byte vectors, thread t of nthreads.
+__device__ __forceinline__ void init_out_share(const GemmArgs& a, int cta, int nctas, int t, int nthreads) {
+    const long long n4 = a.init_n >> 2;
+    const long long per = (n4 + nctas - 1) / nctas;
+    const long long b = per * cta;
+    const long long e = b + per < n4 ? b + per : n4;
+    float4* o = reinterpret_cast<float4*>(a.init_out);
+    for (long long i = b + t; i < e; i += nthreads) {
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (a.init_src != nullptr) {
+            if (a.init_src_dtype == MOE_DTYPE_F32) {
+                v = __ldg(reinterpret_cast<const float4*>(a.init_src) + i);
+            } else {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(a.init_src) + i);
+                const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+                v = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+        o[i] = v;
+    }
 }
 
 // Epilogue of 16 token columns [c0, c0+16) for this thread's weight row.
@@ -739,6 +778,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             named_bar_sync(1, kEpiThreads);
             if (etid == 0) atomicAdd(ka.ready + tile_index(un), 1);
         };
+        // a finalizing call's output start (GEMM1's launch writes it): this
+        // CTA's share first; in a fused launch GEMM2's reductions may only
+        // start once every CTA's share is written
+        const bool init = a0.init_out != nullptr;
+        if (init) {
+            init_out_share(a0, blockIdx.x, gridDim.x, etid, kEpiThreads);
+            if (FUSED) {
+                __threadfence();
+                named_bar_sync(1, kEpiThreads);
+                if (etid == 0) atomicAdd(ka.init_done, 1);
+            }
+        }
+        bool init_seen = !(FUSED && MODE == MODE_FINAL && init);
         int it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
             int ph;
@@ -748,6 +800,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
             if (MODE == MODE_FINAL && (!FUSED || ph == 1)) {
                 named_bar_sync(1, kEpiThreads);              // the previous unit is done with the table
+                if (!init_seen) {
+                    // every other thread passes the barrier after the accumulator
+                    // wait below only once this wait is over
+                    if (etid == 0) wait_counter(ka.init_done, static_cast<int>(gridDim.x), abort_flag, a0.err);
+                    init_seen = true;
+                }
                 load_route_table(un, a, etid, kEpiThreads, route_tok, route_scl);
             }
             wait_bar(tfull_bar(buf), use, abort_flag, a0.err);
@@ -867,6 +925,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (FUSED && tid == 0 && a0.init_out != nullptr) {
+        // the last CTA to finish returns the output-start counters to zero
+        if (atomicAdd(ka.init_done + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            ka.init_done[0] = 0;
+            ka.init_done[1] = 0;
+        }
+    }
 }
 
 // ---- launching one instantiation ------------------------------------------------------

@@ -8,10 +8,10 @@ namespace gemm {
 
 cudaError_t launch_gemm_mx8(int mode, int bt, int out_dtype, const CUtensorMap& tA, const CUtensorMap& tB,
                             const Mx8Args& m, int grid, cudaStream_t s) {
-    if (mode == MODE_SWIGLU) return launch_mx8_bt<MODE_SWIGLU, uint8_t>(bt, tA, tB, m, grid, s);
-    if (mode == MODE_FINAL) return launch_mx8_bt<MODE_FINAL, float>(bt, tA, tB, m, grid, s);
-    if (out_dtype == MOE_DTYPE_F32) return launch_mx8_bt<MODE_PLAIN, float>(bt, tA, tB, m, grid, s);
-    return launch_mx8_bt<MODE_PLAIN, __nv_bfloat16>(bt, tA, tB, m, grid, s);
+    if (mode == MODE_SWIGLU) return launch_mx8_bt<MODE_SWIGLU, uint8_t, false>(bt, tA, tB, m, grid, s);
+    if (mode == MODE_FINAL) return launch_mx8_bt<MODE_FINAL, float, false>(bt, tA, tB, m, grid, s);
+    if (out_dtype == MOE_DTYPE_F32) return launch_mx8_bt<MODE_PLAIN, float, false>(bt, tA, tB, m, grid, s);
+    return launch_mx8_bt<MODE_PLAIN, __nv_bfloat16, false>(bt, tA, tB, m, grid, s);
 }
 
 }  // namespace gemm

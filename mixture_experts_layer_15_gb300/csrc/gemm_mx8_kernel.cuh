@@ -43,6 +43,7 @@
 // eight scale columns (its A atom, its B atom).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "gemm_kernel.cuh"
@@ -101,7 +102,10 @@ struct Mx8Args {
     int max_token_tiles;      // token tiles the atom buffers hold
 };
 
-__device__ __forceinline__ Unit decode_unit8(int u, const int* prefix, const int* offs, int BT, const GemmArgs& a) {
+// TT: tokens per token tile; HL: each token is two B rows (its hi and lo
+// terms), so the tile's MMA N is twice its tokens (rounded up to 16).
+__device__ __forceinline__ Unit decode_unit8(int u, const int* prefix, const int* offs, int TT, const GemmArgs& a,
+                                             bool hl = false) {
     int lo = 0, hi = a.groups;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -113,12 +117,12 @@ __device__ __forceinline__ Unit decode_unit8(int u, const int* prefix, const int
     un.s = local % a.splits;
     local /= a.splits;
     const int beg = offs[lo], end = offs[lo + 1];
-    const int ntt = (end - beg + BT - 1) / BT;
+    const int ntt = (end - beg + TT - 1) / TT;
     const int tt = local % ntt;
     un.wt = local / ntt;
-    un.row0 = beg + tt * BT;
+    un.row0 = beg + tt * TT;
     un.row_end = min(end, a.rows_alloc);
-    const int rows = min(BT, un.row_end - un.row0);
+    const int rows = min(TT, un.row_end - un.row0) * (hl ? 2 : 1);
     un.ncols = (rows + 15) & ~15;
     if (un.ncols < 16) un.ncols = 16;
     const int nkb = a.kr / kMxBK;
@@ -171,11 +175,103 @@ __device__ __forceinline__ void emit16_swiglu_mx8(const Unit& un, const Mx8Args&
     }
 }
 
-template <int BT, int MODE, typename OutT>
+// ---- bf16 activations as two E4M3 terms (MOE_WEIGHTS_MXFP4_A16) -------------------
+// A bf16 value x (8 significant bits) is split into hi + lo, each an E4M3 code
+// (4 significant bits) times a per-32-block power-of-two scale:
+//   hi = e4m3(x / s1) * s1,  lo = e4m3((x - hi) / s2) * s2,
+// with s = the smallest power of two for which the block's largest magnitude
+// is at most 448 * s (no code saturates). x - hi is exact in float32 and a
+// multiple of x's ulp no larger than 8 ulp, so lo holds it exactly whenever
+// it is a normal or subnormal E4M3 multiple of s2 -- every element within 2^14
+// of its block's largest magnitude. The block-scaled MMA then computes the
+// bf16-activation contraction as two e2m1 x E4M3 products summed in float32.
+
+// Scale byte b (scale 2^(b-127)): smallest with amax <= 448 * 2^(b-127), in 1..254.
+__device__ __forceinline__ uint32_t hl_scale_byte(uint32_t amax_bits) {
+    const int e = static_cast<int>((amax_bits >> 23) & 0xFFu);
+    const int b = e - 8 + ((amax_bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return static_cast<uint32_t>(b < 1 ? 1 : (b > 254 ? 254 : b));
+}
+__device__ __forceinline__ float e4m3_value(uint8_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// GEMM1 epilogue of 16 accumulator columns = 8 tokens (hi and lo columns of a
+// token summed): act = act(gate) * up, rounded to bf16, split into hi and lo
+// over the warp's 32 features (one MX block of GEMM2's reduction); codes to
+// act rows 2r (hi) and 2r + 1 (lo), block scales to the act atom.
+__device__ __forceinline__ void emit16_swiglu_hl(const Unit& un, const Mx8Args& m, int q, int lane, int c0, int T,
+                                                 const float (&v0)[16], const float (&v1)[16]) {
+    const GemmArgs& a = m.g;
+    uint8_t* out = static_cast<uint8_t*>(a.out);
+    const int f = un.wt * kBM + q * 32 + lane;
+    const size_t atom = (static_cast<size_t>(T) * (a.out_ld / kMxBK) + un.wt) * kAtom;
+    const bool plain = act_is_plain(a.act, a.clamp);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float g = v0[2 * i] + v0[2 * i + 1], u = v1[2 * i] + v1[2 * i + 1];
+        const float x = __bfloat162float(__float2bfloat16_rn(plain ? silu_mul(g, u) : act_mul(g, u, a.act, a.clamp)));
+        const uint32_t b1 = hl_scale_byte(__reduce_max_sync(0xffffffffu, __float_as_uint(x) & 0x7FFFFFFFu));
+        const uint8_t c1 = e4m3_rn(x * mx8_inv_scale(b1));
+        const float r = x - e4m3_value(c1) * __uint_as_float(b1 << 23);      // exact
+        const uint32_t b2 = hl_scale_byte(__reduce_max_sync(0xffffffffu, __float_as_uint(r) & 0x7FFFFFFFu));
+        const uint8_t c2 = e4m3_rn(r * mx8_inv_scale(b2));
+        const int row = un.row0 + c0 / 2 + i;
+        if (row < un.row_end) {
+            out[static_cast<size_t>(2 * row) * a.out_ld + f] = c1;
+            out[static_cast<size_t>(2 * row + 1) * a.out_ld + f] = c2;
+            if (lane == 0) {
+                m.sfb_out[atom + atom_byte(c0 + 2 * i, q)] = static_cast<uint8_t>(b1);
+                m.sfb_out[atom + atom_byte(c0 + 2 * i + 1, q)] = static_cast<uint8_t>(b2);
+            }
+        }
+    }
+}
+
+// GEMM2 epilogues of 16 accumulator columns = 8 tokens: y = hi column + lo
+// column, then as emit16 / emit16_final for token (not column) i.
+template <typename OutT>
+__device__ __forceinline__ void emit8_plain_hl(const Unit& un, const GemmArgs& a, int row_in_tile, int c0,
+                                               const float (&v0)[16], const float (&v1)[16]) {
+    OutT* out = static_cast<OutT*>(a.out);
+    const int col = un.wt * a.wtile_rows + row_in_tile;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = un.row0 + c0 / 2 + i;
+        if (r < un.row_end) {
+            const size_t rb = static_cast<size_t>(r) * a.out_ld;
+            store_out<OutT>(out + rb + col, v0[2 * i] + v0[2 * i + 1]);
+            store_out<OutT>(out + rb + col + kBM, v1[2 * i] + v1[2 * i + 1]);
+        }
+    }
+}
+
+__device__ __forceinline__ void emit8_final_hl(const Unit& un, const GemmArgs& a, int row_in_tile, int c0,
+                                               const int* tok, const float* scl, const float (&v0)[16],
+                                               const float (&v1)[16]) {
+    float* out = static_cast<float*>(a.out);
+    const int col = un.wt * a.wtile_rows + row_in_tile;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int t = tok[c0 / 2 + i];
+        if (t >= 0) {
+            const float si = scl[c0 / 2 + i];
+            float* o = out + static_cast<size_t>(t) * a.out_ld + col;
+            atomicAdd(o, si * (v0[2 * i] + v0[2 * i + 1]));
+            atomicAdd(o + kBM, si * (v1[2 * i] + v1[2 * i + 1]));
+        }
+    }
+}
+
+// BT: B rows per token tile (<= 128: one scale atom). HL: each token is two
+// B rows (bf16 activations as two E4M3 terms), so a tile holds BT / 2 tokens.
+template <int BT, int MODE, typename OutT, bool HL>
 __global__ void __launch_bounds__(Cfg8<BT>::THREADS, 1)
 grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Mx8Args m) {
     using C = Cfg8<BT>;
+    constexpr int TT = HL ? BT / 2 : BT;                   // tokens per token tile
     constexpr int kEpiThreads = C::EPI_THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -231,7 +327,7 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     for (int g = tid; g < groups; g += C::THREADS) {
         int cnt = offs[g + 1] - offs[g];
         if (cnt < 0) { set_error(a.err, MOE_ERR_DEVICE_INDEX); cnt = 0; }
-        const int ntt = (cnt + BT - 1) / BT;
+        const int ntt = (cnt + TT - 1) / TT;
         prefix[g] = ntt * a.n_wtiles * a.splits;
         ttp[g] = ntt;
     }
@@ -248,7 +344,7 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // global index of a unit's token tile: the row of its activation atoms
-    auto tile_index = [&](const Unit& un) { return ttp[un.g] + (un.row0 - offs[un.g]) / BT; };
+    auto tile_index = [&](const Unit& un) { return ttp[un.g] + (un.row0 - offs[un.g]) / TT; };
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -258,7 +354,7 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             uint32_t issued = 0, issued_phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit8(u, prefix, offs, BT, a);
+                const Unit un = decode_unit8(u, prefix, offs, TT, a, HL);
                 const int a_row = un.g * a.rows_per_group + un.wt * a.wtile_rows;
                 const uint8_t* sfa0 = m.sfa + static_cast<size_t>(a_row / kBM) * nkb_all * kAtom;
                 const uint8_t* sfa1 = m.sfa + static_cast<size_t>((a_row + a.a1_offset) / kBM) * nkb_all * kAtom;
@@ -269,7 +365,7 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
                     tma_load_2d(st, &tmA, kb * kMxBK, a_row, full_bar(stage));
                     tma_load_2d(st + C::A_BYTES, &tmA, kb * kMxBK, a_row + a.a1_offset, full_bar(stage));
-                    tma_load_2d(st + 2 * C::A_BYTES, &tmB, kb * kMxBK, un.row0, full_bar(stage));
+                    tma_load_2d(st + 2 * C::A_BYTES, &tmB, kb * kMxBK, HL ? 2 * un.row0 : un.row0, full_bar(stage));
                     bulk_load(st + C::OFF_SF, sfa0 + kb * kAtom, kAtom, full_bar(stage));
                     bulk_load(st + C::OFF_SF + kAtom, sfa1 + kb * kAtom, kAtom, full_bar(stage));
                     bulk_load(st + C::OFF_SF + 2 * kAtom, sfb + kb * kAtom, kAtom, full_bar(stage));
@@ -297,7 +393,7 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
-                const Unit un = decode_unit8(u, prefix, offs, BT, a);
+                const Unit un = decode_unit8(u, prefix, offs, TT, a, HL);
                 const int buf = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!wait_bar(tempty_bar(buf), use ^ 1u, abort_flag, a.err)) break;
@@ -343,18 +439,29 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int c_first = 16 * ((warp - 3) >> 2);
         constexpr int c_step = 16 * (C::EPI_WARPS / 4);
         auto emit = [&](const Unit& un, int c0, const float (&v0)[16], const float (&v1)[16]) {
-            if (MODE == MODE_SWIGLU) emit16_swiglu_mx8(un, m, q, lane, c0, tile_index(un), v0, v1);
-            else if (MODE == MODE_FINAL) emit16_final<2>(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
-            else emit16<2, MODE_PLAIN, OutT>(un, a, row_in_tile, c0, v0, v1);
+            if (HL) {
+                if (MODE == MODE_SWIGLU) emit16_swiglu_hl(un, m, q, lane, c0, tile_index(un), v0, v1);
+                else if (MODE == MODE_FINAL) emit8_final_hl(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
+                else emit8_plain_hl<OutT>(un, a, row_in_tile, c0, v0, v1);
+            } else {
+                if (MODE == MODE_SWIGLU) emit16_swiglu_mx8(un, m, q, lane, c0, tile_index(un), v0, v1);
+                else if (MODE == MODE_FINAL) emit16_final<2>(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
+                else emit16<2, MODE_PLAIN, OutT>(un, a, row_in_tile, c0, v0, v1);
+            }
         };
+        // a finalizing call's output start (written by its GEMM1 launch)
+        if (a.init_out != nullptr) init_out_share(a, blockIdx.x, gridDim.x, etid, kEpiThreads);
         int it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
-            const Unit un = decode_unit8(u, prefix, offs, BT, a);
+            const Unit un = decode_unit8(u, prefix, offs, TT, a, HL);
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t use = C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1);
             if (MODE == MODE_FINAL) {
                 named_bar_sync(1, kEpiThreads);
-                load_route_table(un, a, etid, kEpiThreads, route_tok, route_scl);
+                // one table entry per token (HL: half the tile's columns)
+                Unit ut = un;
+                if (HL) ut.ncols = un.ncols / 2;
+                load_route_table(ut, a, etid, kEpiThreads, route_tok, route_scl);
             }
             wait_bar(tfull_bar(buf), use, abort_flag, a.err);
             if (named_bar_or(1, kEpiThreads, *abort_flag != 0)) break;
@@ -434,11 +541,11 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int BT, int MODE, typename OutT>
+template <int BT, int MODE, typename OutT, bool HL>
 cudaError_t launch_mx8_kernel(const CUtensorMap& tA, const CUtensorMap& tB, const Mx8Args& m, int grid,
                               cudaStream_t s) {
     using C = Cfg8<BT>;
-    auto kern = grouped_gemm_mx8_kernel<BT, MODE, OutT>;
+    auto kern = grouped_gemm_mx8_kernel<BT, MODE, OutT, HL>;
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -451,21 +558,26 @@ cudaError_t launch_mx8_kernel(const CUtensorMap& tA, const CUtensorMap& tB, cons
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, tA, tB, m);
 }
 
-template <int MODE, typename OutT>
+// bt: B rows per token tile (16, 32, 64 or 128).
+template <int MODE, typename OutT, bool HL>
 cudaError_t launch_mx8_bt(int bt, const CUtensorMap& tA, const CUtensorMap& tB, const Mx8Args& m, int grid,
                           cudaStream_t s) {
     switch (bt) {
-        case 16: return launch_mx8_kernel<16, MODE, OutT>(tA, tB, m, grid, s);
-        case 32: return launch_mx8_kernel<32, MODE, OutT>(tA, tB, m, grid, s);
-        case 64: return launch_mx8_kernel<64, MODE, OutT>(tA, tB, m, grid, s);
-        default: return launch_mx8_kernel<128, MODE, OutT>(tA, tB, m, grid, s);
+        case 16: return launch_mx8_kernel<16, MODE, OutT, HL>(tA, tB, m, grid, s);
+        case 32: return launch_mx8_kernel<32, MODE, OutT, HL>(tA, tB, m, grid, s);
+        case 64: return launch_mx8_kernel<64, MODE, OutT, HL>(tA, tB, m, grid, s);
+        default: return launch_mx8_kernel<128, MODE, OutT, HL>(tA, tB, m, grid, s);
     }
 }
 
-// Defined in gemm_mx8.cu. mode: MODE_SWIGLU (GEMM1, act codes + atoms),
-// MODE_PLAIN (GEMM2 into y of out_dtype) or MODE_FINAL (GEMM2 into the f32 out).
+// Defined in gemm_mx8.cu (hl = false: MXFP8 activations) and gemm_mx8_hl.cu
+// (hl = true: bf16 activations as two E4M3 terms). mode: MODE_SWIGLU (GEMM1,
+// act codes + atoms), MODE_PLAIN (GEMM2 into y of out_dtype) or MODE_FINAL
+// (GEMM2 into the f32 out). bt: B rows per token tile.
 cudaError_t launch_gemm_mx8(int mode, int bt, int out_dtype, const CUtensorMap& tA, const CUtensorMap& tB,
                             const Mx8Args& m, int grid, cudaStream_t s);
+cudaError_t launch_gemm_mx8_hl(int mode, int bt, int out_dtype, const CUtensorMap& tA, const CUtensorMap& tB,
+                               const Mx8Args& m, int grid, cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace moe

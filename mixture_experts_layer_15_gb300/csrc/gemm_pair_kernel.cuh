@@ -243,6 +243,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         float* xg = xchg + grp * 16 * 64;                     // [16][64]: up values of this group's chunk
         const int l64 = (q & 1) * 32 + lane;                  // lane within the 64 gate (or up) rows
         const uint32_t tempty_even = mapa_shared(tempty_bar(0), 0);
+        // a finalizing call's output start (written by its GEMM1 launch)
+        if (a.init_out != nullptr) init_out_share(a, blockIdx.x, gridDim.x, etid, kEpiThreads);
         int it = 0;
         for (int u = pair; u < total_units; u += npairs, ++it) {
             const Unit un = unit_at(u);

@@ -119,13 +119,14 @@ inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : 
 moe_status check_weights(const moe_weights* w) {
     if (w == nullptr || w->w1 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
     if (w->E_local < 1 || w->E_local > 1024 || w->K <= 0 || w->N <= 0) return MOE_ERR_INVALID_ARG;
-    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4 && w->format != MOE_WEIGHTS_MXFP4_A8)
+    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_MXFP4 && w->format != MOE_WEIGHTS_MXFP4_A8 &&
+        w->format != MOE_WEIGHTS_MXFP4_A16)
         return MOE_ERR_INVALID_ARG;
     if (w->activation != MOE_ACT_SILU && w->activation != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
     if (!(w->activation_clamp == w->activation_clamp) || w->activation_clamp == INFINITY) return MOE_ERR_INVALID_ARG;
     if (w->K % 128 != 0 || w->N % 128 != 0) return MOE_ERR_ALIGNMENT;
     if (!aligned16(w->w1) || !aligned16(w->w2)) return MOE_ERR_ALIGNMENT;
-    if (w->format == MOE_WEIGHTS_MXFP4_A8) {
+    if (w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16) {
         // codes by 16U4 TMA (32-byte aligned); prepared scale atoms by bulk copies
         if (w->w1_scale == nullptr || w->w2_scale == nullptr) return MOE_ERR_INVALID_ARG;
         if (!aligned16(w->w1_scale) || !aligned16(w->w2_scale)) return MOE_ERR_ALIGNMENT;
@@ -249,6 +250,20 @@ moe_status moe_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, ui
     const moe_status st = device_gate(&info, &err);
     if (st != MOE_OK) return st;
     return from_cuda(moe::launch_mxfp8_quantize(x, rows, C, codes, scales, err, info, stream));
+}
+
+moe_status moe_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+    if (rows < 0 || C <= 0) return MOE_ERR_INVALID_ARG;
+    if (C % 128 != 0) return MOE_ERR_ALIGNMENT;
+    if (static_cast<long long>(rows) * C >= (1LL << 39)) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_e4m3_split(x, rows, C, codes, scales, err, info, stream));
 }
 
 size_t moe_mx_prepared_scales_size(int E_local, int rows, int cols) {
@@ -657,7 +672,7 @@ moe_status moe_experts_batched(const moe_weights* w, const void* x, const int32_
     if (max_tokens < 0) return MOE_ERR_INVALID_ARG;
     const moe_status ws_ok = check_weights(w);
     if (ws_ok != MOE_OK) return ws_ok;
-    if (w->format == MOE_WEIGHTS_MXFP4_A8) return MOE_ERR_UNSUPPORTED;
+    if (w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16) return MOE_ERR_UNSUPPORTED;
     if (!valid_dtype(y_dtype)) return MOE_ERR_INVALID_ARG;
     const long long rows = static_cast<long long>(w->E_local) * max_tokens;
     if (rows >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;

@@ -81,10 +81,6 @@ cudaError_t launch_finalize_rmsnorm(const void* gemm2, int gemm2_dtype, int num_
                                     const void* shared, int shared_dtype, float rsf, void* residual,
                                     int residual_dtype, const void* gamma, int gamma_dtype, float eps, void* y,
                                     int y_dtype, int* err, cudaStream_t stream);
-// out[M, K] f32 = shared (shared_dtype) or 0, the start of the fused finalize.
-cudaError_t launch_out_init(const void* shared, int shared_dtype, int M, int K, float* out, const DeviceInfo& dev,
-                            cudaStream_t stream);
-
 // ---- grouped expert GEMMs (gemm.cu) --------------------------------------------
 // One grouped "gated MLP" problem: E groups of rows of `x` (bf16 [rows_alloc, K]),
 // group g = rows [offsets[g], offsets[g+1]) (or one group of `single_rows`
@@ -118,11 +114,18 @@ struct ExpertsProblem {
 // x bf16 [rows, C] -> E4M3 codes [rows, C] + E8M0 scales [rows, C/32] (C % 128 == 0).
 cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
                                   const DeviceInfo& dev, cudaStream_t stream);
+// x bf16 [rows, C] -> two E4M3 terms per value: codes [2 * rows, C] and E8M0
+// scales [2 * rows, C/32] (rows 2p hi, 2p + 1 lo; C % 128 == 0).
+cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
+                              const DeviceInfo& dev, cudaStream_t stream);
 // The same for the grouped rows of x_perm, scales into the token-tile atoms
 // of the block-scaled GEMM (tiles of bt rows per group, at most max_tiles).
+// hl: split each value into two E4M3 terms (hi, lo) that sum to it: codes
+// [2 * rows_alloc, C] (row 2p hi, 2p + 1 lo), B rows 2n and 2n + 1 of a tile's
+// atoms for its token n (bt tokens per tile).
 cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
                                         int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
-                                        const DeviceInfo& dev, cudaStream_t stream);
+                                        const DeviceInfo& dev, cudaStream_t stream, bool hl = false);
 // Weight scales [rows_total, cols/32] -> atoms [rows_total/128][cols/128][512].
 cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,
                                      const DeviceInfo& dev, cudaStream_t stream);

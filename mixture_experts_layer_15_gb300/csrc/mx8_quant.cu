@@ -25,7 +25,13 @@ constexpr int kQThreads = 256;
 // byte (n % 32) * 16 + (n / 32) * 4 + j). Rows outside [offsets[0],
 // offsets[groups]) are not touched; neither is anything when the groups need
 // more than `max_tiles` tiles.
-template <bool ATOM>
+//
+// HL: each row is split into two E4M3 terms, hi and lo, that sum to the bf16
+// value (gemm_mx8_kernel.cuh, MOE_WEIGHTS_MXFP4_A16): row p's hi codes go to
+// codes row 2p, its lo codes to row 2p + 1; in the tile atoms token n of a
+// tile (bt tokens) has B rows 2n (hi) and 2n + 1 (lo), in the row-major scales
+// rows 2p and 2p + 1.
+template <bool ATOM, bool HL>
 __global__ void __launch_bounds__(kQThreads)
 mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint8_t* __restrict__ codes,
                       uint8_t* __restrict__ scales, const int32_t* __restrict__ offsets, int groups, int bt,
@@ -89,6 +95,50 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
             // a block of 32 = 4 lanes x 8 values
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            if (HL) {
+                // hi = e4m3(v / s1) * s1, lo = e4m3((v - hi) / s2) * s2
+                const uint32_t b1 = gemm::hl_scale_byte(__float_as_uint(am));
+                const float inv1 = gemm::mx8_inv_scale(b1), s1 = __uint_as_float(b1 << 23);
+                uint8_t c1[8];
+                float r[8];
+                float ar = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c1[i] = gemm::e4m3_rn(v[i] * inv1);
+                    r[i] = v[i] - gemm::e4m3_value(c1[i]) * s1;          // exact
+                    ar = fmaxf(ar, fabsf(r[i]));
+                }
+                ar = fmaxf(ar, __shfl_xor_sync(0xffffffffu, ar, 1));
+                ar = fmaxf(ar, __shfl_xor_sync(0xffffffffu, ar, 2));
+                const uint32_t b2 = gemm::hl_scale_byte(__float_as_uint(ar));
+                const float inv2 = gemm::mx8_inv_scale(b2);
+                if (on) {
+                    uint32_t h0 = 0, h1 = 0, l0 = 0, l1 = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        h0 |= static_cast<uint32_t>(c1[i]) << (8 * i);
+                        h1 |= static_cast<uint32_t>(c1[4 + i]) << (8 * i);
+                        l0 |= static_cast<uint32_t>(gemm::e4m3_rn(r[i] * inv2)) << (8 * i);
+                        l1 |= static_cast<uint32_t>(gemm::e4m3_rn(r[4 + i] * inv2)) << (8 * i);
+                    }
+                    uint8_t* ch = codes + static_cast<size_t>(2 * p) * C;
+                    *reinterpret_cast<uint2*>(ch + c) = make_uint2(h0, h1);
+                    *reinterpret_cast<uint2*>(ch + C + c) = make_uint2(l0, l1);
+                    if ((lane & 3) == 0) {
+                        if (ATOM) {
+                            uint8_t* at = scales + (static_cast<size_t>(T) * nkb + c / gemm::kMxBK) * gemm::kAtom;
+                            const int j = (c % gemm::kMxBK) / 32;
+                            at[gemm::atom_byte(2 * n, j)] = static_cast<uint8_t>(b1);
+                            at[gemm::atom_byte(2 * n + 1, j)] = static_cast<uint8_t>(b2);
+                        } else {
+                            uint8_t* sr = scales + static_cast<size_t>(2 * p) * (C / 32) + c / 32;
+                            sr[0] = static_cast<uint8_t>(b1);
+                            sr[C / 32] = static_cast<uint8_t>(b2);
+                        }
+                    }
+                }
+                continue;
+            }
             const uint32_t sb = gemm::mx8_scale_byte(__float_as_uint(am));
             const float inv = gemm::mx8_inv_scale(sb);
             if (on) {
@@ -138,21 +188,32 @@ cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes
     const int nw = kQThreads / 32;
     int grid = (rows + nw - 1) / nw;
     if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
-    return launch_pdl(mxfp8_quantize_kernel<false>, dim3(grid), dim3(kQThreads), 0, s,
+    return launch_pdl(mxfp8_quantize_kernel<false, false>, dim3(grid), dim3(kQThreads), 0, s,
+                      static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
+                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err);
+}
+
+cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
+                              const DeviceInfo& dev, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    const int nw = kQThreads / 32;
+    int grid = (rows + nw - 1) / nw;
+    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    return launch_pdl(mxfp8_quantize_kernel<false, true>, dim3(grid), dim3(kQThreads), 0, s,
                       static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
                       static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err);
 }
 
 cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
                                         int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
-                                        const DeviceInfo& dev, cudaStream_t s) {
+                                        const DeviceInfo& dev, cudaStream_t s, bool hl) {
     const int nw = kQThreads / 32;
     int grid = (rows_alloc + nw - 1) / nw;
     if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
     if (grid < 1) grid = 1;
-    return launch_pdl(mxfp8_quantize_kernel<true>, dim3(grid), dim3(kQThreads), 0, s,
-                      static_cast<const __nv_bfloat16*>(x), rows_alloc, C, codes, atoms, offsets, groups, bt,
-                      rows_alloc, max_tiles, err);
+    auto kern = hl ? mxfp8_quantize_kernel<true, true> : mxfp8_quantize_kernel<true, false>;
+    return launch_pdl(kern, dim3(grid), dim3(kQThreads), 0, s, static_cast<const __nv_bfloat16*>(x), rows_alloc, C,
+                      codes, atoms, offsets, groups, bt, rows_alloc, max_tiles, err);
 }
 
 cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,

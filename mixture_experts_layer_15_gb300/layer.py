@@ -48,7 +48,9 @@ class MoELayer:
     With ``fmt`` = MOE_WEIGHTS_MXFP4_A8 the MXFP4 weights are given as for
     MOE_WEIGHTS_MXFP4 (codes + row-major E8M0 scales); the layer rearranges
     the scales once (moe_mx_prepare_scales) and the experts run with MXFP8
-    activations on the block-scaled tensor cores.
+    activations on the block-scaled tensor cores. MOE_WEIGHTS_MXFP4_A16 takes
+    the same weights and keeps bf16 activations (W4A16), each split into two
+    E4M3 terms for the block-scaled tensor cores.
     """
 
     def __init__(self, *, K, N, E, top_k, w1, w2, w1_scale=None, w2_scale=None,
@@ -73,7 +75,7 @@ class MoELayer:
             raise ValueError("fused_finalize accumulates into an f32 output")
         self.fused_finalize = bool(fused_finalize)
         act = {"silu": L.MOE_ACT_SILU, "gelu": L.MOE_ACT_GELU}[activation]
-        if fmt == L.MOE_WEIGHTS_MXFP4_A8:
+        if fmt in (L.MOE_WEIGHTS_MXFP4_A8, L.MOE_WEIGHTS_MXFP4_A16):
             w1_scale = self._prepare_scales(w1_scale, 2 * N, K)
             w2_scale = self._prepare_scales(w2_scale, K, N)
             self.w1_scale, self.w2_scale = w1_scale, w2_scale

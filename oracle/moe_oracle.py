@@ -81,6 +81,7 @@ __all__ = [
     "moe_forward", "bf16_round", "gelu_erf", "experts_batched", "add_rmsnorm",
     "finalize_add_rmsnorm", "E4M3_MAX", "e4m3_value", "e4m3_round", "mxfp8_scale_byte",
     "mxfp8_quantize", "mxfp8_dequantize", "mxfp8_qdq", "experts_mxfp8", "experts_chunked",
+    "e4m3_split_scale_byte", "e4m3_split", "e4m3_split_value",
 ]
 
 # --------------------------------------------------------------------------
@@ -235,6 +236,46 @@ def mxfp8_dequantize(codes, scales) -> np.ndarray:
     vals = e4m3_value(codes).reshape(codes.shape[:-1] + (C // 32, 32))
     scale = np.exp2(np.asarray(scales, dtype=np.float64) - 127.0)
     return (vals * scale[..., None]).reshape(codes.shape)
+
+
+def e4m3_split_scale_byte(amax) -> np.ndarray:
+    """Scale byte of a block of the two-term split: the smallest b with
+    amax <= 448 * 2^(b - 127) (no code of the block saturates), kept in
+    1..254 (an all-zero block gets 1). With amax = m * 2^e, m in [1, 2),
+    the candidates are e + 119 and e + 120."""
+    a = np.abs(np.asarray(amax, dtype=np.float64))
+    m, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = m * 2^ex, m in [0.5, 1)
+    b = (ex - 1) + 119
+    b = np.where(a > 448.0 * np.exp2(b - 127.0), b + 1, b)
+    b = np.where(a > 0, b, 1)
+    return np.clip(b, 1, 254).astype(np.uint8)
+
+
+def e4m3_split(x):
+    """bf16 activations as two E4M3 terms (the MXFP4_A16 path): along the last
+    axis, every block of 32 values (float32) gets
+        hi = e4m3_round(x / s1),          s1 = 2^(b1 - 127), b1 from max |x|,
+        r  = x - e4m3_value(hi) * s1      (exact),
+        lo = e4m3_round(r / s2),          s2 = 2^(b2 - 127), b2 from max |r|,
+    with the scale bytes of e4m3_split_scale_byte. Returns (hi codes, hi scale
+    bytes, lo codes, lo scale bytes): codes [..., C], bytes [..., C/32]."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    C = x.shape[-1]
+    assert C % 32 == 0
+    blk = x.reshape(x.shape[:-1] + (C // 32, 32))
+    b1 = e4m3_split_scale_byte(np.abs(blk).max(axis=-1))
+    s1 = np.exp2(b1.astype(np.float64) - 127.0)[..., None]
+    hi = e4m3_round(blk / s1)
+    r = blk - e4m3_value(hi) * s1
+    b2 = e4m3_split_scale_byte(np.abs(r).max(axis=-1))
+    s2 = np.exp2(b2.astype(np.float64) - 127.0)[..., None]
+    lo = e4m3_round(r / s2)
+    return hi.reshape(x.shape), b1, lo.reshape(x.shape), b2
+
+
+def e4m3_split_value(hi, b1, lo, b2) -> np.ndarray:
+    """The value a two-term split stands for: hi * s1 + lo * s2, float64."""
+    return mxfp8_dequantize(hi, b1) + mxfp8_dequantize(lo, b2)
 
 
 def mxfp8_qdq(x) -> np.ndarray:

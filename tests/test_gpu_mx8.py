@@ -261,7 +261,7 @@ def test_experts_a8_argument_checks(moe):
     assert moe.moe_experts_workspace_size(cw, 4, 1) == 0
     cw.K = 256
     assert moe.moe_experts_workspace_size(cw, 4, 1) > 0
-    assert moe.moe_experts_launches(cw, 4, 1, True) == 4     # out init, quantiser, GEMM1, GEMM2
+    assert moe.moe_experts_launches(cw, 4, 1, True) == 3     # quantiser, GEMM1 (+ output start), GEMM2
     assert moe.moe_experts_launches(cw, 4, 1, False) == 3
     ws = torch.zeros(16, dtype=torch.uint8, device=DEV)
     with pytest.raises(moe.MoEError) as e:

@@ -279,7 +279,7 @@ def test_bounded_wait_gives_up_and_reports(moe):
 # ------------------------------------------------------------------ whole layer
 
 def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, seed_offset=0, fused_finalize=False,
-                 activation="silu", clamp=None, a8=False, few_experts=False):
+                 activation="silu", clamp=None, a8=False, few_experts=False, a16=False):
     cfg = synth.CONFIGS[name]
     li = layer_inputs(name)
     x, logits = synth.make_tokens(cfg, M, DEV, li, seed_offset=seed_offset)
@@ -300,6 +300,8 @@ def _check_layer(moe, name, M, sample=None, masked=False, bf16_storage=False, se
         kw.update(activation=activation, activation_clamp=clamp)
     if a8:                        # MXFP4 weights x MXFP8 activations (block-scaled MMAs)
         kw.update(fmt=moe.MOE_WEIGHTS_MXFP4_A8)
+    if a16:                       # MXFP4 weights x bf16 activations as two E4M3 terms (block-scaled MMAs)
+        kw.update(fmt=moe.MOE_WEIGHTS_MXFP4_A16)
     layer = make_layer(moe, name, li, **kw)
     b = layer.forward(x, logits)
     torch.cuda.synchronize()

@@ -696,3 +696,54 @@ def test_experts_chunked(chunk, masked):
     assert np.array_equal(whole_map, pmap)
     R = int(offs[-1])
     np.testing.assert_allclose(whole_g2[:R], g2, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- two-term E4M3 split (MXFP4_A16)
+
+def test_e4m3_split_scale_rule_closed_form():
+    """The split's scale is the smallest power of two s with amax <= 448 s:
+    then amax / s lies in (224, 448]; an all-zero block gets byte 1."""
+    amax = np.concatenate([np.exp2(np.arange(-100, 100)), np.exp2(np.arange(-100, 100)) * 1.75,
+                           np.exp2(np.arange(-100, 100)) * np.nextafter(1.75, 2),
+                           np.random.default_rng(3).uniform(1e-20, 1e20, 5000)]).astype(np.float32)
+    b = O.e4m3_split_scale_byte(amax).astype(np.float64)
+    s = np.exp2(b - 127.0)
+    a = amax.astype(np.float64)
+    assert np.all(a <= 448.0 * s) and np.all(a > 224.0 * s)
+    assert O.e4m3_split_scale_byte(np.float32(448.0)) == 127          # 448 = 448 * 2^0: no step up
+    assert O.e4m3_split_scale_byte(np.float32(449.0)) == 128
+    assert O.e4m3_split_scale_byte(np.float32(0.0)) == 1
+
+
+def test_e4m3_split_is_exact_on_bf16():
+    """hi + lo equals the bf16 value exactly for every element within 2^14 of
+    its block's largest magnitude, and within 2^-22 of that magnitude
+    otherwise; no code saturates (every |code value| <= 448, no NaN code). Rows
+    span 2^-40 .. 2^40, with an all-zero row, a block whose largest value sits
+    in (448, 512) times a power of two (the plain MX scale would saturate it),
+    a value 2^20 times its neighbours, and bf16 subnormals."""
+    rng = np.random.default_rng(41)
+    R, C = 96, 512
+    x = rng.standard_normal((R, C)) * np.exp2(rng.uniform(-40, 40, (R, 1)))
+    x[1] = 0.0
+    x[2, :32] = rng.standard_normal(32)
+    x[2, 5] = 1.875                                   # 480 * 2^-8
+    x[3, 64:96] = rng.standard_normal(32) * 1e-3
+    x[3, 70] = 2.0 ** 10
+    x[4] = rng.standard_normal(C) * 2.0 ** -130       # bf16 subnormals
+    xb = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    hi, b1, lo, b2 = O.e4m3_split(xb)
+    v = O.e4m3_split_value(hi, b1, lo, b2)
+    amax = np.repeat(np.abs(xb.reshape(R, C // 32, 32)).max(axis=-1), 32, axis=1)
+    near = np.abs(xb) >= amax * 2.0 ** -14
+    assert np.array_equal(v[near], xb[near].astype(np.float64))
+    assert np.all(np.abs(v - xb) <= amax * 2.0 ** -22)
+    for c in (hi, lo):
+        assert np.all(np.abs(O.e4m3_value(c)) <= 448.0) and not np.any((c & 0x7F) == 0x7F)
+    # hi is the MX-style rounding of x to E4M3 at the split scale
+    s1 = np.repeat(np.exp2(b1.astype(np.float64) - 127.0), 32, axis=1)
+    assert np.array_equal(hi, O.e4m3_round(xb / s1))
+    # the plain MX rule would saturate row 2's first block: the split rule keeps it exact
+    sb = O.mxfp8_scale_byte(np.float32(1.875))
+    assert 1.875 / 2.0 ** (int(sb) - 127) > 448.0
+    assert v[2, 5] == 1.875
