@@ -224,9 +224,12 @@ def make_forward(moe, cfg, layer, batches, stream, finalize="fused"):
         x, logits = batches[M]
         b = layer.buffers(M)
         rsf_r = layer.rsf if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0
+        # the folded finalize on the block-scaled formats gathers the rows in
+        # the experts (moe_experts_fused_finalize_x): the permute copies none
+        gx = finalize == "fused" and layer.gathers_in_experts(M)
         moe.moe_route_permute(logits, M, cfg.E, cfg.top_k, layer.method, layer.score_bias, layer.n_group,
                               layer.topk_group, rsf_r, b.topk_ids, b.topk_weights, layer.weights_dtype, None,
-                              cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse, b.x_perm, b.perm_ws,
+                              cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse, None if gx else b.x_perm, b.perm_ws,
                               b.perm_ws.numel())
         if layer.ws1 is not None:
             moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.shared, layer.gemm2_dtype,
@@ -234,6 +237,13 @@ def make_forward(moe, cfg, layer, batches, stream, finalize="fused"):
         rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
         if ev is not None:
             ev[0].record(stream)
+        if finalize == "fused" and gx:
+            moe.moe_experts_fused_finalize_x(layer.cw, x, b.offsets, M, cfg.top_k, b.topk_weights,
+                                             layer.weights_dtype, b.inverse, b.shared, layer.gemm2_dtype, rsf,
+                                             b.out, b.exp_ws, b.exp_ws.numel())
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if finalize == "fused":
             moe.moe_experts_fused_finalize(layer.cw, b.x_perm, b.offsets, M, cfg.top_k, b.topk_weights,
                                            layer.weights_dtype, b.inverse, b.shared, layer.gemm2_dtype, rsf,

@@ -425,6 +425,34 @@ moe_status moe_experts_fused_finalize(const moe_weights* w,
                                       float routed_scaling_factor, float* out,
                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_experts_fused_finalize_x -- moe_experts_fused_finalize with the
+ * permute's row gather folded in: it reads the token activations x in token
+ * order, and permuted row p is x[permuted_to_expanded[p] / top_k] (the row
+ * that moe_permute would have copied to x_perm[p]; pair it with moe_permute
+ * or moe_route_permute called with x_perm = NULL). The block-scaled formats
+ * (MOE_WEIGHTS_MXFP4_A8, MOE_WEIGHTS_MXFP4_A16) quantise the gathered rows
+ * straight from x, so the [M*top_k, K] x_perm is never written or read; the
+ * other formats gather x_perm into the workspace first. Results equal
+ * moe_experts_fused_finalize's on the gathered rows.
+ *
+ *   x                bf16 [M, K] (16-byte aligned).
+ *   permuted_to_expanded  i32 [M*top_k]: entries [0, R) as moe_permute writes
+ *                    them; an entry outside [0, M*top_k) sets
+ *                    MOE_ERR_DEVICE_INDEX and its row reads as zeros (block-
+ *                    scaled formats) or is skipped.
+ *   workspace        moe_experts_x_workspace_size() bytes, zero-filled before
+ *                    first use (the moe_experts rule).
+ *   the rest         as in moe_experts_fused_finalize.
+ * ---------------------------------------------------------------------- */
+size_t moe_experts_x_workspace_size(const moe_weights* w, int M, int top_k);
+
+moe_status moe_experts_fused_finalize_x(const moe_weights* w, const void* x, const int32_t* expert_offsets, int M,
+                                        int top_k, const void* expert_weights, moe_dtype weights_dtype,
+                                        const int32_t* permuted_to_expanded, const void* shared_out,
+                                        moe_dtype shared_dtype, float routed_scaling_factor, float* out,
+                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* The number of kernels that moe_experts_fused_finalize (fused_finalize = 1,
  * counting the initialisation of out) or moe_experts with do_finalize = 0
  * (fused_finalize = 0) launches for this batch size, from the same launch plan

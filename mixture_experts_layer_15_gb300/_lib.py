@@ -39,7 +39,8 @@ EXPORTS = (
     "moe_route", "moe_permute_workspace_size", "moe_permute", "moe_route_permute", "moe_permute_noalloc",
     "moe_experts_workspace_size",
     "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize",
-    "moe_experts_chunked_workspace_size", "moe_experts_chunked",
+    "moe_experts_chunked_workspace_size", "moe_experts_chunked", "moe_experts_x_workspace_size",
+    "moe_experts_fused_finalize_x",
     "moe_finalize_add_rmsnorm", "moe_experts_batched_workspace_size", "moe_experts_batched", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
@@ -92,6 +93,9 @@ _SIGS = {
     "moe_experts_fused_finalize": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
                                     _P, _Z, _P], _I),
     "moe_experts_launches": ([ctypes.POINTER(moe_weights), _I, _I, _I], _I),
+    "moe_experts_x_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I], _Z),
+    "moe_experts_fused_finalize_x": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
+                                      _P, _Z, _P], _I),
     "moe_experts_chunked_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I, _I], _Z),
     "moe_experts_chunked": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _I, _P, _I, _P, _P, _I, _I, _P, _I, _P,
                              _I, _F, _P, _I, _P, _Z, _P], _I),
@@ -226,6 +230,19 @@ def moe_experts_chunked(weights: moe_weights, x, topk_ids, M, top_k, E, expert_m
         _ptr(expanded_idx_to_permuted_idx), _ptr(gemm2_permuted), gemm2_dtype, int(do_finalize),
         _ptr(expert_weights), weights_dtype, _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
         out_dtype, _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def moe_experts_x_workspace_size(weights: moe_weights, M, top_k) -> int:
+    return int(lib.moe_experts_x_workspace_size(ctypes.byref(weights), M, top_k))
+
+
+def moe_experts_fused_finalize_x(weights: moe_weights, x, expert_offsets, M, top_k, expert_weights, weights_dtype,
+                                 permuted_to_expanded, shared_out, shared_dtype, routed_scaling_factor, out, workspace,
+                                 workspace_bytes, stream=None):
+    _check("moe_experts_fused_finalize_x", lib.moe_experts_fused_finalize_x(
+        ctypes.byref(weights), _ptr(x), _ptr(expert_offsets), M, top_k, _ptr(expert_weights), weights_dtype,
+        _ptr(permuted_to_expanded), _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def moe_experts_fused_finalize(weights: moe_weights, x_perm, expert_offsets, M, top_k, expert_weights,

@@ -159,6 +159,8 @@ struct Layout {
     size_t off_act, off_p1, off_p2, total;
     // MXFP8 activations (MOE_WEIGHTS_MXFP4_A8): x codes and atoms, act codes and atoms
     size_t off_xq = 0, off_xs = 0, off_aq = 0, off_as = 0;
+    // x in token order on a format that reads x_perm by TMA: the gathered rows
+    size_t off_xg = 0;
 };
 
 // MXFP4 weights on the block-scaled MMAs: three launches (quantise x, GEMM1
@@ -346,8 +348,8 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     m2.sfb_out = nullptr;
     const int grid = dev.sm_count;
     if (fin) set_out_init(a1, p);                       // GEMM1 writes the output start
-    cudaError_t e = launch_mxfp8_quantize_tiles(p.x, p.rows_alloc, K, p.offsets, w->E_local, L.bt, L.max_token_tiles, xq, xs,
-                                    err, dev, s, hl);
+    cudaError_t e = launch_mxfp8_quantize_tiles(p.x, p.rows_alloc, K, p.offsets, w->E_local, L.bt, L.max_token_tiles,
+                                                xq, xs, err, dev, s, hl, p.x_tokens ? p.inverse : nullptr, p.top_k);
     if (e != cudaSuccess) return e;
     auto gemm_launch = hl ? gemm::launch_gemm_mx8_hl : gemm::launch_gemm_mx8;
     e = gemm_launch(gemm::MODE_SWIGLU, rb * L.bt, MOE_DTYPE_BF16, tA1, tB1, m1, grid, s);
@@ -371,8 +373,30 @@ void set_plan_override(int token_tile, int splits1, int splits2, int gemm2_na, i
     g_override.fuse = fuse;
 }
 
-size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev, bool batched) {
-    return make_layout(w, rows_alloc, M, w->E_local, dev.sm_count, false, batched).total;
+namespace {
+// The block-scaled formats quantise x row by row and can read it in token
+// order; the others load x_perm by TMA and need it gathered first.
+bool reads_x_tokens(const moe_weights* w) {
+    return w->format == MOE_WEIGHTS_MXFP4_A8 || w->format == MOE_WEIGHTS_MXFP4_A16;
+}
+
+// With x in token order on a format that needs x_perm, the gathered rows
+// [rows_alloc, K] bf16 go after the rest of the workspace (whose layout does
+// not change).
+Layout make_layout_x(const moe_weights* w, int rows_alloc, int M, int groups, int sm_count, bool fin, bool batched,
+                     bool x_tokens) {
+    Layout L = make_layout(w, rows_alloc, M, groups, sm_count, fin, batched);
+    if (x_tokens && !reads_x_tokens(w)) {
+        L.off_xg = L.total;
+        L.total = align256(L.total + static_cast<size_t>(rows_alloc) * w->K * 2);
+    }
+    return L;
+}
+}  // namespace
+
+size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev, bool batched,
+                               bool x_tokens) {
+    return make_layout_x(w, rows_alloc, M, w->E_local, dev.sm_count, false, batched, x_tokens).total;
 }
 
 namespace {
@@ -397,8 +421,26 @@ int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, cons
     return (L.pair || !L.fused) ? 2 : 1;
 }
 
-cudaError_t launch_experts(const ExpertsProblem& p, void* workspace, size_t /*workspace_bytes*/, int* err,
+cudaError_t launch_experts(const ExpertsProblem& p_in, void* workspace, size_t /*workspace_bytes*/, int* err,
                            const DeviceInfo& dev, cudaStream_t s) {
+    // x in token order: the block-scaled formats read it so (their quantiser
+    // gathers the rows); the others get x_perm gathered into the workspace
+    // first and then run on it
+    ExpertsProblem pg;
+    const ExpertsProblem* pp = &p_in;
+    if (p_in.x_tokens && !reads_x_tokens(p_in.w)) {
+        const Layout Lx = make_layout_x(p_in.w, p_in.rows_alloc, p_in.M, p_in.w->E_local, dev.sm_count,
+                                        p_in.fin_out != nullptr, false, true);
+        uint8_t* xg = static_cast<uint8_t*>(workspace) + Lx.off_xg;
+        const cudaError_t eg = launch_gather_rows(p_in.offsets, p_in.w->E_local, p_in.inverse, p_in.top_k,
+                                                  p_in.rows_alloc, p_in.x, p_in.w->K, xg, dev, s);
+        if (eg != cudaSuccess) return eg;
+        pg = p_in;
+        pg.x = xg;
+        pg.x_tokens = false;
+        pp = &pg;
+    }
+    const ExpertsProblem& p = *pp;
     const moe_weights* w = p.w;
     const int K = w->K, N = w->N;
     const bool mx = w->format == MOE_WEIGHTS_MXFP4;

@@ -108,6 +108,9 @@ struct ExpertsProblem {
     // (counts on the device); offsets is then unused.
     const int32_t* counts = nullptr;
     int batch_stride = 0;
+    // x given in token order (M rows): permuted row p is x[inverse[p] / top_k]
+    // (the block-scaled formats read it so; the others gather into the workspace)
+    bool x_tokens = false;
 };
 
 // ---- MXFP8 activations (mx8_quant.cu) ----------------------------------------------
@@ -122,17 +125,24 @@ cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, ui
 // of the block-scaled GEMM (tiles of bt rows per group, at most max_tiles).
 // hl: split each value into two E4M3 terms (hi, lo) that sum to it: codes
 // [2 * rows_alloc, C] (row 2p hi, 2p + 1 lo), B rows 2n and 2n + 1 of a tile's
-// atoms for its token n (bt tokens per tile).
+// atoms for its token n (bt tokens per tile). gather_inv (or NULL): x is in
+// token order and row p reads token gather_inv[p] / gather_topk.
 cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
                                         int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
-                                        const DeviceInfo& dev, cudaStream_t stream, bool hl = false);
+                                        const DeviceInfo& dev, cudaStream_t stream, bool hl = false,
+                                        const int32_t* gather_inv = nullptr, int gather_topk = 1);
+// x_perm[p] = x[inverse[p] / top_k] for p < offsets[E_l] (the permute's row
+// gather on its own; permute.cu).
+cudaError_t launch_gather_rows(const int32_t* offsets, int E_l, const int32_t* inverse, int top_k, int rows_alloc,
+                               const void* x, int K, void* x_perm, const DeviceInfo& dev, cudaStream_t stream);
 // Weight scales [rows_total, cols/32] -> atoms [rows_total/128][cols/128][512].
 cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,
                                      const DeviceInfo& dev, cudaStream_t stream);
 
 void set_plan_override(int token_tile, int splits_gemm1, int splits_gemm2, int gemm2_tiles, int fuse);
+// x_tokens: x is given in token order (ExpertsProblem::x_tokens).
 size_t experts_workspace_bytes(const moe_weights* w, int rows_alloc, int M, const DeviceInfo& dev,
-                               bool batched = false);
+                               bool batched = false, bool x_tokens = false);
 // Kernels one experts call launches (fin: the finalize folded into GEMM2,
 // counting its out initialisation).
 int experts_launches(const moe_weights* w, int rows_alloc, int M, bool fin, const DeviceInfo& dev);

@@ -31,11 +31,17 @@ constexpr int kQThreads = 256;
 // codes row 2p, its lo codes to row 2p + 1; in the tile atoms token n of a
 // tile (bt tokens) has B rows 2n (hi) and 2n + 1 (lo), in the row-major scales
 // rows 2p and 2p + 1.
+//
+// gather_inv (ATOM only, may be NULL): x holds the tokens in token order and
+// row p reads token gather_inv[p] / gather_topk (the row gather of the permute,
+// done here instead of through x_perm); an entry outside [0, rows_alloc) sets
+// MOE_ERR_DEVICE_INDEX and the row is taken as zeros.
 template <bool ATOM, bool HL>
 __global__ void __launch_bounds__(kQThreads)
 mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint8_t* __restrict__ codes,
                       uint8_t* __restrict__ scales, const int32_t* __restrict__ offsets, int groups, int bt,
-                      int rows_alloc, int max_tiles, int* err) {
+                      int rows_alloc, int max_tiles, int* err, const int32_t* __restrict__ gather_inv,
+                      int gather_topk) {
     __shared__ int s_offs[gemm::kMaxGroups + 1];
     __shared__ int s_ttp[gemm::kMaxGroups + 1];
     __shared__ int tmp[36];
@@ -65,7 +71,16 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
     }
     const int nkb = C / gemm::kMxBK;
     const int nw = kQThreads / 32;
-    for (int p = p0 + blockIdx.x * nw + warp; p < R; p += gridDim.x * nw) {
+    // one warp per (row, group of four 256-column chunks): a row's groups go to
+    // different warps, so a few rows still spread over many warps, and a warp
+    // has the loads of its four chunks in flight at once
+    const int chunks = (C + 255) / 256;
+    const int groups4 = (chunks + 3) / 4;
+    const long long items = static_cast<long long>(R > p0 ? R - p0 : 0) * groups4;
+    for (long long it = static_cast<long long>(blockIdx.x) * nw + warp; it < items;
+         it += static_cast<long long>(gridDim.x) * nw) {
+        const int p = p0 + static_cast<int>(it / groups4);
+        const int cbase = static_cast<int>(it % groups4) * 1024;
         int T = 0, n = 0;
         if (ATOM) {
             int lo = 0, hi = groups;                       // s_offs[lo] <= p < s_offs[hi]
@@ -77,18 +92,37 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
             T = s_ttp[lo] + local / bt;
             n = local % bt;
         }
-        const __nv_bfloat16* xr = x + static_cast<size_t>(p) * C;
+        size_t src = static_cast<size_t>(p);
+        bool zero = false;
+        if (ATOM && gather_inv != nullptr) {
+            const int e = __ldg(gather_inv + p);
+            if (e < 0 || e >= rows_alloc) {
+                if (lane == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
+                zero = true;
+                src = 0;
+            } else {
+                src = static_cast<size_t>(e / gather_topk);
+            }
+        }
+        const __nv_bfloat16* xr = x + src * C;
         uint8_t* cr = codes + static_cast<size_t>(p) * C;
-        for (int c0 = 0; c0 < C; c0 += 256) {              // uniform over the warp
-            const int c = c0 + lane * 8;
-            const bool on = c < C;
-            float v[8];
-            if (on) {
-                Vec8<__nv_bfloat16>::load(xr + c, v);
+        float vv[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = cbase + 256 * j + lane * 8;
+            if (c < C && !zero) {
+                Vec8<__nv_bfloat16>::load(xr + c, vv[j]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+                for (int i = 0; i < 8; ++i) vv[j][i] = 0.0f;
             }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (cbase + 256 * j >= C) break;               // uniform over the warp
+            const int c = cbase + 256 * j + lane * 8;
+            const bool on = c < C;
+            const float (&v)[8] = vv[j];
             float am = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
@@ -127,9 +161,9 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
                     if ((lane & 3) == 0) {
                         if (ATOM) {
                             uint8_t* at = scales + (static_cast<size_t>(T) * nkb + c / gemm::kMxBK) * gemm::kAtom;
-                            const int j = (c % gemm::kMxBK) / 32;
-                            at[gemm::atom_byte(2 * n, j)] = static_cast<uint8_t>(b1);
-                            at[gemm::atom_byte(2 * n + 1, j)] = static_cast<uint8_t>(b2);
+                            const int jj = (c % gemm::kMxBK) / 32;
+                            at[gemm::atom_byte(2 * n, jj)] = static_cast<uint8_t>(b1);
+                            at[gemm::atom_byte(2 * n + 1, jj)] = static_cast<uint8_t>(b2);
                         } else {
                             uint8_t* sr = scales + static_cast<size_t>(2 * p) * (C / 32) + c / 32;
                             sr[0] = static_cast<uint8_t>(b1);
@@ -182,38 +216,48 @@ __global__ void mx_prepare_scales_kernel(const uint8_t* __restrict__ sc, long lo
 
 }  // namespace
 
+namespace {
+// CTAs for rows x groups of four 256-column chunks, one warp per item, at
+// most 8 per SM.
+int quantize_grid(int rows, int C, const DeviceInfo& dev) {
+    const long long items = static_cast<long long>(rows) * ((C + 1023) / 1024);
+    const int nw = kQThreads / 32;
+    long long grid = (items + nw - 1) / nw;
+    const long long cap = 8LL * (dev.sm_count > 0 ? dev.sm_count : 152);
+    if (grid > cap) grid = cap;
+    return grid < 1 ? 1 : static_cast<int>(grid);
+}
+}  // namespace
+
 cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
                                   const DeviceInfo& dev, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int nw = kQThreads / 32;
-    int grid = (rows + nw - 1) / nw;
-    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    const int grid = quantize_grid(rows, C, dev);
     return launch_pdl(mxfp8_quantize_kernel<false, false>, dim3(grid), dim3(kQThreads), 0, s,
                       static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
-                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err);
+                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err, static_cast<const int32_t*>(nullptr),
+                      1);
 }
 
 cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
                               const DeviceInfo& dev, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int nw = kQThreads / 32;
-    int grid = (rows + nw - 1) / nw;
-    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    const int grid = quantize_grid(rows, C, dev);
     return launch_pdl(mxfp8_quantize_kernel<false, true>, dim3(grid), dim3(kQThreads), 0, s,
                       static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
-                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err);
+                      static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err, static_cast<const int32_t*>(nullptr),
+                      1);
 }
 
 cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
                                         int bt, int max_tiles, uint8_t* codes, uint8_t* atoms, int* err,
-                                        const DeviceInfo& dev, cudaStream_t s, bool hl) {
-    const int nw = kQThreads / 32;
-    int grid = (rows_alloc + nw - 1) / nw;
-    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
-    if (grid < 1) grid = 1;
+                                        const DeviceInfo& dev, cudaStream_t s, bool hl, const int32_t* gather_inv,
+                                        int gather_topk) {
+    const int grid = quantize_grid(rows_alloc, C, dev);
     auto kern = hl ? mxfp8_quantize_kernel<true, true> : mxfp8_quantize_kernel<true, false>;
     return launch_pdl(kern, dim3(grid), dim3(kQThreads), 0, s, static_cast<const __nv_bfloat16*>(x), rows_alloc, C,
-                      codes, atoms, offsets, groups, bt, rows_alloc, max_tiles, err);
+                      codes, atoms, offsets, groups, bt, rows_alloc, max_tiles, err, gather_inv,
+                      gather_topk > 0 ? gather_topk : 1);
 }
 
 cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,

@@ -86,6 +86,24 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* _
     for (; c < n16; c += 32) dst[c] = __ldg(src + c);
 }
 
+// Segments of a row copy: 128 16-byte vectors (2 KB; four per lane, loaded
+// before any is stored), so that a few long rows still spread over many warps.
+constexpr int kSegVec = 128;
+__host__ __device__ inline int row_segments(int K) { return (K / 8 + kSegVec - 1) / kSegVec; }
+
+__device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint4* __restrict__ dst, int n16, int seg,
+                                             int lane) {
+    const int b = seg * kSegVec + lane;
+    const int e = (seg + 1) * kSegVec < n16 ? (seg + 1) * kSegVec : n16;
+    uint4 v[kSegVec / 32];
+#pragma unroll
+    for (int j = 0; j < kSegVec / 32; ++j)
+        if (b + 32 * j < e) v[j] = __ldg(src + b + 32 * j);
+#pragma unroll
+    for (int j = 0; j < kSegVec / 32; ++j)
+        if (b + 32 * j < e) dst[b + 32 * j] = v[j];
+}
+
 // ---- single chunk: one kernel ------------------------------------------------
 // The whole permute of at most blockDim.x routes (ids in global or shared
 // memory): every CTA sorts them in shared memory; CTA 0 writes the offsets and
@@ -119,13 +137,15 @@ __device__ __forceinline__ void permute_single_chunk(const int32_t* ids, int n, 
     }
     if (x_perm == nullptr) return;
     __syncthreads();
-    // rows: route i (< n, local) is copied by global warp i % (grid * W)
-    const int gw = blockIdx.x * W + warp, nw = gridDim.x * W, n16 = K / 8;
-    for (int i = gw; i < n; i += nw) {
+    // rows: segment s of route i's row (i < n, local) is copied by global warp
+    // (i * segs + s) % (grid * W)
+    const int gw = blockIdx.x * W + warp, nw = gridDim.x * W, n16 = K / 8, segs = row_segments(K);
+    for (int it = gw; it < n * segs; it += nw) {
+        const int i = it / segs;
         const int pi = pos[i];
         if (pi < 0) continue;
-        copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(i / top_k) * K),
-                 reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(pi) * K), n16, tid & 31);
+        copy_segment(reinterpret_cast<const uint4*>(x + static_cast<size_t>(i / top_k) * K),
+                     reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(pi) * K), n16, it % segs, tid & 31);
     }
 }
 
@@ -309,18 +329,29 @@ __global__ void permute_scatter_kernel(const int32_t* __restrict__ ids, int n, i
 }
 
 // x_perm[p] = x[inverse[p] / top_k] for p < offsets[E_l]; one warp per row.
+// R and the inverse entries are checked against rows_alloc (when they come
+// from a caller, not from this permute): an out-of-range one sets
+// MOE_ERR_DEVICE_INDEX and its row is skipped.
 __global__ void permute_gather_kernel(const int32_t* __restrict__ offsets, int E_l,
                                       const int32_t* __restrict__ inverse, int top_k,
                                       const __nv_bfloat16* __restrict__ x, int K,
-                                      __nv_bfloat16* __restrict__ x_perm) {
+                                      __nv_bfloat16* __restrict__ x_perm, int rows_alloc, int* err) {
     pdl_wait();
     pdl_trigger();
-    const int R = __ldg(offsets + E_l);
+    int R = __ldg(offsets + E_l);
+    if (R < 0 || R > rows_alloc) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
+        R = R < 0 ? 0 : rows_alloc;
+    }
     const int warps = blockDim.x >> 5;
     const int n16 = K / 8;
     for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < R; p += gridDim.x * warps) {
-        const int t = __ldg(inverse + p) / top_k;
-        copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * K),
+        const int e = __ldg(inverse + p);
+        if (e < 0 || e >= rows_alloc) {
+            if ((threadIdx.x & 31) == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
+            continue;
+        }
+        copy_row(reinterpret_cast<const uint4*>(x + static_cast<size_t>(e / top_k) * K),
                  reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(p) * K), n16, threadIdx.x & 31);
     }
 }
@@ -345,7 +376,7 @@ cudaError_t launch_route_permute(const float* logits, int M, int E, int top_k, i
     // clusters: one is enough to route; more add row-copy bandwidth (one warp per row)
     int clusters = 1;
     if (x_perm != nullptr) {
-        clusters = ceil_div(n, r.G * r.W);
+        clusters = ceil_div(n * row_segments(K), r.G * r.W);
         const int cap = (2 * dev.sm_count) / r.G;
         if (clusters > cap) clusters = cap;
         if (clusters < 1) clusters = 1;
@@ -395,8 +426,8 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
         const size_t smem = sizeof(int) * (w1 * E_l + E_l + 1 + t1 + 33);
         int grid = 1;
         if (x_perm != nullptr) {
-            // one warp per gathered row (at most 2 CTAs per SM)
-            grid = ceil_div(n, w1);
+            // one warp per 2 KB segment of a gathered row (at most 2 CTAs per SM)
+            grid = ceil_div(n * row_segments(K), w1);
             grid = grid < 1 ? 1 : (grid > 2 * dev.sm_count ? 2 * dev.sm_count : grid);
         }
         return launch_pdl(permute_fused_kernel, dim3(grid), dim3(t1), smem, s, ids, n, top_k, E, emap, E_l,
@@ -418,7 +449,18 @@ cudaError_t launch_permute(const int32_t* ids, int M, int top_k, int E, const in
     if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
     return launch_pdl(permute_gather_kernel, dim3(grid), dim3(32 * rows_per_block), 0, s,
                       static_cast<const int32_t*>(offsets), E_l, static_cast<const int32_t*>(inverse), top_k, xb,
-                      K, xp);
+                      K, xp, n, err);
+}
+
+cudaError_t launch_gather_rows(const int32_t* offsets, int E_l, const int32_t* inverse, int top_k, int rows_alloc,
+                               const void* x, int K, void* x_perm, const DeviceInfo& dev, cudaStream_t s) {
+    const int rows_per_block = 8;
+    int grid = ceil_div(rows_alloc, rows_per_block);
+    if (grid > 8 * dev.sm_count) grid = 8 * dev.sm_count;
+    if (grid < 1) grid = 1;
+    return launch_pdl(permute_gather_kernel, dim3(grid), dim3(32 * rows_per_block), 0, s, offsets, E_l, inverse,
+                      top_k, static_cast<const __nv_bfloat16*>(x), K, static_cast<__nv_bfloat16*>(x_perm),
+                      rows_alloc, device_error_word());
 }
 
 }  // namespace moe

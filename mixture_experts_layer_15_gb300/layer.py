@@ -57,7 +57,8 @@ class MoELayer:
                  fmt=L.MOE_WEIGHTS_BF16, route="softmax", score_bias=None, n_group=1, topk_group=1,
                  routed_scaling_factor=1.0, expert_map=None, E_local=None, ws1=None, ws2=None,
                  weights_dtype=L.MOE_DTYPE_F32, gemm2_dtype=L.MOE_DTYPE_F32,
-                 out_dtype=L.MOE_DTYPE_F32, fused_finalize=False, activation="silu", activation_clamp=None):
+                 out_dtype=L.MOE_DTYPE_F32, fused_finalize=False, activation="silu", activation_clamp=None,
+                 gather_in_experts=None):
         self.K, self.N, self.E, self.top_k = K, N, E, top_k
         self.E_local = E if E_local is None else E_local
         self.w1, self.w2, self.w1_scale, self.w2_scale = w1, w2, w1_scale, w2_scale
@@ -74,6 +75,11 @@ class MoELayer:
         if fused_finalize and out_dtype != L.MOE_DTYPE_F32:
             raise ValueError("fused_finalize accumulates into an f32 output")
         self.fused_finalize = bool(fused_finalize)
+        # the folded finalize can read x in token order and gather its rows in
+        # the experts (moe_experts_fused_finalize_x); None: on the block-scaled
+        # formats, whose quantiser then reads x directly, for batches past the
+        # one-kernel route + permute (M > 64), which copies its rows cheaply
+        self.gather_in_experts = gather_in_experts
         act = {"silu": L.MOE_ACT_SILU, "gelu": L.MOE_ACT_GELU}[activation]
         if fmt in (L.MOE_WEIGHTS_MXFP4_A8, L.MOE_WEIGHTS_MXFP4_A16):
             w1_scale = self._prepare_scales(w1_scale, 2 * N, K)
@@ -81,6 +87,13 @@ class MoELayer:
             self.w1_scale, self.w2_scale = w1_scale, w2_scale
         self.cw = L.make_weights(fmt, self.E_local, K, N, w1, w2, w1_scale, w2_scale, act, activation_clamp)
         self._bufs = {}
+
+    def gathers_in_experts(self, M: int) -> bool:
+        """Whether a folded-finalize forward of M tokens gathers the rows in the
+        experts (moe_experts_fused_finalize_x) instead of in the permute."""
+        if self.gather_in_experts is not None:
+            return bool(self.gather_in_experts)
+        return self.fmt in (L.MOE_WEIGHTS_MXFP4_A8, L.MOE_WEIGHTS_MXFP4_A16) and M > 64
 
     def _prepare_scales(self, scales, rows, cols):
         out = torch.empty(L.moe_mx_prepared_scales_size(self.E_local, rows, cols), dtype=torch.uint8,
@@ -96,7 +109,8 @@ class MoELayer:
         R = max(M * self.top_k, 1)
         i32 = dict(dtype=torch.int32, device=dev)
         pws = L.moe_permute_workspace_size(M, self.top_k, self.E_local)
-        ews = L.moe_experts_workspace_size(self.cw, M, self.top_k)
+        ews = max(L.moe_experts_workspace_size(self.cw, M, self.top_k),
+                  L.moe_experts_x_workspace_size(self.cw, M, self.top_k))
         shared = shared_ws = None
         if self.ws1 is not None:
             shared = torch.empty(M, self.K, dtype=_TORCH[self.gemm2_dtype], device=dev)
@@ -133,18 +147,21 @@ class MoELayer:
         skip the router and use the given routing instead."""
         M = x.shape[0]
         b = self.buffers(M)
+        # with the row gather folded into the experts the permute copies no rows
+        gx = do_finalize and self.fused_finalize and self.gathers_in_experts(M)
+        xp = None if gx else b.x_perm
         if topk_ids is None:
             # route and permute (one kernel for small batches)
             rsf = self.rsf if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0
             L.moe_route_permute(logits, M, self.E, self.top_k, self.method, self.score_bias, self.n_group,
                                 self.topk_group, rsf, b.topk_ids, b.topk_weights, self.weights_dtype,
-                                self.expert_map, self.E_local, x, self.K, b.offsets, b.pmap, b.inverse, b.x_perm,
+                                self.expert_map, self.E_local, x, self.K, b.offsets, b.pmap, b.inverse, xp,
                                 b.perm_ws, b.perm_ws.numel(), stream)
             ids, wts = b.topk_ids, b.topk_weights
         else:
             ids, wts = topk_ids, topk_weights
             L.moe_permute(ids, M, self.top_k, self.E, self.expert_map, self.E_local, x, self.K, b.offsets,
-                          b.pmap, b.inverse, b.x_perm, b.perm_ws, b.perm_ws.numel(), stream)
+                          b.pmap, b.inverse, xp, b.perm_ws, b.perm_ws.numel(), stream)
         if self.ws1 is not None:
             L.moe_shared_expert(self.ws1, self.ws2, self.K, self.Ns, x, M, b.shared, self.gemm2_dtype,
                                 b.shared_ws, b.shared_ws.numel(), stream)
@@ -152,9 +169,13 @@ class MoELayer:
         rsf = 1.0 if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else self.rsf
         wdt = L.MOE_DTYPE_F32 if wts.dtype == torch.float32 else L.MOE_DTYPE_BF16
         if do_finalize and self.fused_finalize:
-            L.moe_experts_fused_finalize(self.cw, b.x_perm, b.offsets, M, self.top_k, wts, wdt, b.inverse,
-                                         b.shared, self.gemm2_dtype, rsf, b.out, b.exp_ws, b.exp_ws.numel(),
-                                         stream)
+            if gx:
+                L.moe_experts_fused_finalize_x(self.cw, x, b.offsets, M, self.top_k, wts, wdt, b.inverse, b.shared,
+                                               self.gemm2_dtype, rsf, b.out, b.exp_ws, b.exp_ws.numel(), stream)
+            else:
+                L.moe_experts_fused_finalize(self.cw, b.x_perm, b.offsets, M, self.top_k, wts, wdt, b.inverse,
+                                             b.shared, self.gemm2_dtype, rsf, b.out, b.exp_ws, b.exp_ws.numel(),
+                                             stream)
             return b
         L.moe_experts(self.cw, b.x_perm, b.offsets, M, self.top_k, b.gemm2, self.gemm2_dtype,
                       1 if do_finalize else 0,

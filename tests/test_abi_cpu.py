@@ -214,3 +214,24 @@ def test_chunked_workspace_is_sized_by_the_chunk(moe):
     assert call(64, 8, 64, 16, 1, P + 4096) == moe.MOE_ERR_INVALID_ARG       # no map: E_local must be E
     assert call(-1, 8, 128, 16, 1, P + 4096) == moe.MOE_ERR_INVALID_ARG
     assert call(0, 8, 128, 16, 0, None) == 0                                  # nothing to do
+
+
+def test_fused_finalize_x_validates_on_the_host(moe):
+    """The token-order experts entry: its workspace holds the gathered rows
+    only for formats that read x_perm by TMA, and its argument rules fail
+    before any device is touched."""
+    P = 0x1000
+    F = moe.MOE_DTYPE_F32
+    bf = moe.make_weights(0, 8, 4096, 1024, P, P)
+    a16 = moe.make_weights(moe.MOE_WEIGHTS_MXFP4_A16, 8, 4096, 1024, P, P, P, P)
+    M, k = 512, 2
+    assert moe.moe_experts_x_workspace_size(bf, M, k) >= moe.moe_experts_workspace_size(bf, M, k) + M * k * 4096 * 2
+    assert moe.moe_experts_x_workspace_size(a16, M, k) == moe.moe_experts_workspace_size(a16, M, k)
+    call = lambda w, x, M, k, out: _status(moe.moe_experts_fused_finalize_x, w, x, P, M, k, P, F, P, None, F, 1.0,
+                                           out, P, 1 << 30)
+    assert call(bf, P, -1, k, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(bf, P, M, 0, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(bf, None, M, k, P + 4096) == moe.MOE_ERR_INVALID_ARG            # x required
+    assert call(bf, P + 8, M, k, P + 4096) == moe.MOE_ERR_ALIGNMENT
+    assert call(bf, P, M, k, P) == moe.MOE_ERR_INVALID_ARG                      # out may not alias x
+    assert call(bf, P, 0, k, P + 4096) == 0                                     # nothing to do

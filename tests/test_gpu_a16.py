@@ -207,3 +207,50 @@ def test_layer_deepseek_a16_equals_decode_path(moe, M):
     _check_no_error(moe)
     a, b = outs[0].cpu().numpy(), outs[1].cpu().numpy()
     assert max_err(a, b) <= 5e-3 * float(np.sqrt(np.mean(b ** 2)))
+
+
+@pytest.mark.parametrize("fmt_name", ["MOE_WEIGHTS_MXFP4_A16", "MOE_WEIGHTS_MXFP4_A8", "MOE_WEIGHTS_MXFP4",
+                                      "MOE_WEIGHTS_BF16"])
+def test_fused_finalize_x_gathers_rows(moe, fmt_name):
+    """moe_experts_fused_finalize_x (x in token order, rows gathered through
+    permuted_to_expanded inside the experts) equals moe_experts_fused_finalize
+    on x_perm up to the order of the folded finalize's float32 additions
+    (1e-4 * RMS), on every weight format; an out-of-range inverse entry is
+    reported as MOE_ERR_DEVICE_INDEX."""
+    fmt = getattr(moe, fmt_name)
+    E, K, N, M, k = 8, 512, 512, 96, 2
+    p1, s1, p2, s2, x, ids = _random_mx_problem(E, K, N, M, k, seed=77)
+    if fmt == moe.MOE_WEIGHTS_BF16:
+        g = torch.Generator().manual_seed(78)
+        p1 = (torch.randn(E, 2 * N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+        p2 = (torch.randn(E, K, N, generator=g) / N ** 0.5).to(torch.bfloat16)
+    offs, pmap, inv, _ = O.permute(ids, E)
+    xp = x[torch.from_numpy(inv.astype(np.int64) // k)]
+    w = np.random.default_rng(9).uniform(0.1, 1.0, (M, k)).astype(np.float32)
+    if fmt == moe.MOE_WEIGHTS_BF16:
+        d = dict(p1=p1.to(DEV), p2=p2.to(DEV))
+        cw = moe.make_weights(fmt, E, K, N, d["p1"], d["p2"])
+    else:
+        cw, d = _weights(moe, fmt, p1, s1, p2, s2, E, K, N)
+    n = max(moe.moe_experts_workspace_size(cw, M, k), moe.moe_experts_x_workspace_size(cw, M, k))
+    assert moe.moe_experts_x_workspace_size(cw, M, k) >= moe.moe_experts_workspace_size(cw, M, k)
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    offs_d = torch.from_numpy(offs).to(DEV)
+    inv_d = torch.from_numpy(inv.astype(np.int32)).to(DEV)
+    w_d = torch.from_numpy(w).to(DEV)
+    xd = x.to(DEV)
+    ref = torch.empty(M, K, dtype=torch.float32, device=DEV)
+    moe.moe_experts_fused_finalize(cw, xp.to(DEV), offs_d, M, k, w_d, F32, inv_d, None, F32, 1.0, ref, ws, n)
+    got = torch.empty(M, K, dtype=torch.float32, device=DEV)
+    moe.moe_experts_fused_finalize_x(cw, xd, offs_d, M, k, w_d, F32, inv_d, None, F32, 1.0, got, ws, n)
+    torch.cuda.synchronize()
+    _check_no_error(moe)
+    rms = float(ref.pow(2).mean().sqrt())
+    assert float((got - ref).abs().max()) <= 1e-4 * rms
+    bad = inv_d.clone()
+    bad[3] = 10 ** 7
+    moe.moe_experts_fused_finalize_x(cw, xd, offs_d, M, k, w_d, F32, bad, None, F32, 1.0, got, ws, n)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error() == moe.MOE_ERR_DEVICE_INDEX
+    assert moe.moe_get_error() == 0
+    assert torch.isfinite(got).all()
