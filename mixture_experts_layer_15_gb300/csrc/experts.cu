@@ -219,15 +219,25 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
     // GEMM1 and GEMM2 in one launch when GEMM2 units take two A tiles and the
     // token-tile counters fit their region
     L.max_token_tiles = rows_alloc / L.bt + (groups < rows_alloc ? groups : rows_alloc) + 1;
+    // With many experts that each hold long runs of rows (16 or more groups,
+    // at least 256 rows on average) the two GEMMs run as two launches: a
+    // same-box sweep of the Qwen3-shaped layer at M = 8192 measured 518 us
+    // against 531 us for the one fused launch (which still wins at M = 2048,
+    // 212 us against 217 us).
+    const bool long_runs = g_override.fuse == 0 && groups >= 16 && rows_alloc / groups >= 256;
     L.fused = L.g2.na == 2 && L.max_token_tiles <= kMaxSplitTiles && g_override.fuse != 2 &&
-              g_override.fuse != 3 && !batched;
+              g_override.fuse != 3 && !batched && !long_runs;
     // GEMM1 and GEMM2 on CTA pairs (two launches): bf16 weights, 128- or
     // 256-token tiles, every unit whole (no split-K), 256-row GEMM2 units.
     // Forced by the override (fuse = 3, with its tile width); chosen
     // automatically with 256-token tiles when the experts average at least
-    // 256 rows, so that most tiles are full and the units fill the grid. The
-    // choice does not depend on `fin`, so the workspace query and the launch
-    // agree on the layout.
+    // 256 rows, so that most tiles are full and the units fill the grid, and
+    // the intermediate size is at least 2048: a same-box sweep measured pairs
+    // ahead at Mixtral M = 4096 (1.67 ms against 1.90 on one CTA) and for the
+    // DeepSeek shared expert at M = 8192 (413 us against 467), and behind at
+    // Qwen3 M = 8192 (N = 768: 546 us against 518). The choice does not
+    // depend on `fin`, so the workspace query and the launch agree on the
+    // layout.
     const bool pair_ok = w->format == MOE_WEIGHTS_BF16 && K % 256 == 0 && N % kBM == 0 &&
                          g_override.gemm2_na != 1 && !batched;
     L.pair = false;
@@ -235,7 +245,7 @@ Layout make_layout(const moe_weights* w, int rows_alloc, int M, int groups, int 
         plan_gemm(1, L.bt, 2, K / (2 * kBM), N, rows_alloc, groups, sm_count).splits == 1) {
         L.pair = true;
     } else if (pair_ok && g_override.fuse == 0 && g_override.token_tile == 0 && groups > 0 &&
-               rows_alloc / groups >= 256) {
+               rows_alloc / groups >= 256 && N >= 2048) {
         const GemmPlan p1 = plan_gemm(0, 256, 2, N / kBM, K, rows_alloc, groups, sm_count);
         const GemmPlan p2 = plan_gemm(1, 256, 2, K / (2 * kBM), N, rows_alloc, groups, sm_count);
         if (p1.splits == 1 && p2.splits == 1) {
