@@ -175,6 +175,11 @@ Layout make_layout_a8(const moe_weights* w, int rows_alloc, int M, int groups, i
     const int rb = w->format == MOE_WEIGHTS_MXFP4_A16 ? 2 : 1;       // B rows per token
     L.bt = g_override.token_tile > 0 ? g_override.token_tile : pick_bt(M, rows_alloc, groups, K, N, false);
     if (L.bt > 128 / rb) L.bt = 128 / rb;
+    // bf16 activations (two B rows per token): 56-token tiles rather than 64,
+    // so that the 112-column accumulators leave TMEM room for two buffers
+    // (2 x 2 x 112 + the ring's scale columns = 512) and the epilogue of one
+    // unit overlaps the next unit's MMAs
+    if (rb == 2 && L.bt == 64 && g_override.token_tile == 0) L.bt = 56;
     L.g1 = plan_gemm(0, L.bt, 2, N / kBM, K / 2, rows_alloc, groups, sm_count);
     L.g2 = plan_gemm(1, L.bt, 2, K / (2 * kBM), N / 2, rows_alloc, groups, sm_count, fin);
     // a split's fp32 partial tile holds every B row of the token tile: rb rows per token

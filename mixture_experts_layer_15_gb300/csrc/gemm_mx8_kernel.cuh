@@ -439,13 +439,15 @@ grouped_gemm_mx8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int c_first = 16 * ((warp - 3) >> 2);
         constexpr int c_step = 16 * (C::EPI_WARPS / 4);
         auto emit = [&](const Unit& un, int c0, const float (&v0)[16], const float (&v1)[16]) {
-            if (HL) {
-                if (MODE == MODE_SWIGLU) emit16_swiglu_hl(un, m, q, lane, c0, tile_index(un), v0, v1);
-                else if (MODE == MODE_FINAL) emit8_final_hl(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
+            if constexpr (HL) {
+                if constexpr (MODE == MODE_SWIGLU) emit16_swiglu_hl(un, m, q, lane, c0, tile_index(un), v0, v1);
+                else if constexpr (MODE == MODE_FINAL)
+                    emit8_final_hl(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
                 else emit8_plain_hl<OutT>(un, a, row_in_tile, c0, v0, v1);
             } else {
-                if (MODE == MODE_SWIGLU) emit16_swiglu_mx8(un, m, q, lane, c0, tile_index(un), v0, v1);
-                else if (MODE == MODE_FINAL) emit16_final<2>(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
+                if constexpr (MODE == MODE_SWIGLU) emit16_swiglu_mx8(un, m, q, lane, c0, tile_index(un), v0, v1);
+                else if constexpr (MODE == MODE_FINAL)
+                    emit16_final<2>(un, a, row_in_tile, c0, route_tok, route_scl, v0, v1);
                 else emit16<2, MODE_PLAIN, OutT>(un, a, row_in_tile, c0, v0, v1);
             }
         };
@@ -558,7 +560,7 @@ cudaError_t launch_mx8_kernel(const CUtensorMap& tA, const CUtensorMap& tB, cons
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, tA, tB, m);
 }
 
-// bt: B rows per token tile (16, 32, 64 or 128).
+// bt: B rows per token tile (16, 32, 64 or 128; HL also 112).
 template <int MODE, typename OutT, bool HL>
 cudaError_t launch_mx8_bt(int bt, const CUtensorMap& tA, const CUtensorMap& tB, const Mx8Args& m, int grid,
                           cudaStream_t s) {
@@ -566,6 +568,9 @@ cudaError_t launch_mx8_bt(int bt, const CUtensorMap& tA, const CUtensorMap& tB, 
         case 16: return launch_mx8_kernel<16, MODE, OutT, HL>(tA, tB, m, grid, s);
         case 32: return launch_mx8_kernel<32, MODE, OutT, HL>(tA, tB, m, grid, s);
         case 64: return launch_mx8_kernel<64, MODE, OutT, HL>(tA, tB, m, grid, s);
+        case 112:
+            if constexpr (HL) return launch_mx8_kernel<112, MODE, OutT, HL>(tA, tB, m, grid, s);
+            else return cudaErrorInvalidValue;
         default: return launch_mx8_kernel<128, MODE, OutT, HL>(tA, tB, m, grid, s);
     }
 }

@@ -209,16 +209,45 @@ def test_layer_deepseek_a16_equals_decode_path(moe, M):
     assert max_err(a, b) <= 5e-3 * float(np.sqrt(np.mean(b ** 2)))
 
 
+_X_PLANS = {
+    # automatic plan
+    "auto": (None, 96),
+    # two one-CTA launches, GEMM1 split in two along K (several token tiles
+    # per expert and ragged tails)
+    "two_split": ((0, 2, 1, 0, 2), 700),
+    # the same with 16-token tiles
+    "two_t16": ((16, 1, 1, 0, 2), 300),
+    # CTA pairs (bf16)
+    "pairs": ((128, 0, 0, 0, 3), 700),
+}
+
+
+@pytest.mark.parametrize("plan", list(_X_PLANS))
 @pytest.mark.parametrize("fmt_name", ["MOE_WEIGHTS_MXFP4_A16", "MOE_WEIGHTS_MXFP4_A8", "MOE_WEIGHTS_MXFP4",
                                       "MOE_WEIGHTS_BF16"])
-def test_fused_finalize_x_gathers_rows(moe, fmt_name):
+def test_fused_finalize_x_gathers_rows(moe, fmt_name, plan):
     """moe_experts_fused_finalize_x (x in token order, rows gathered through
     permuted_to_expanded inside the experts) equals moe_experts_fused_finalize
-    on x_perm up to the order of the folded finalize's float32 additions
-    (1e-4 * RMS), on every weight format; an out-of-range inverse entry is
-    reported as MOE_ERR_DEVICE_INDEX."""
+    on x_perm under the same launch plan up to the order of the folded
+    finalize's float32 additions (1e-4 * RMS), on every weight format; an
+    out-of-range inverse entry is reported as MOE_ERR_DEVICE_INDEX and leaves
+    the output finite."""
     fmt = getattr(moe, fmt_name)
-    E, K, N, M, k = 8, 512, 512, 96, 2
+    override, M = _X_PLANS[plan]
+    if plan != "auto" and fmt in (moe.MOE_WEIGHTS_MXFP4_A16, moe.MOE_WEIGHTS_MXFP4_A8):
+        pytest.skip("the block-scaled formats have one launch plan")
+    if plan == "pairs" and fmt != moe.MOE_WEIGHTS_BF16:
+        pytest.skip("CTA pairs run bf16 weights")
+    if override is not None:
+        moe.moe_set_plan_override(*override)
+    try:
+        _fused_finalize_x_case(moe, fmt, M)
+    finally:
+        moe.moe_set_plan_override(0, 0, 0, 0, 0)
+
+
+def _fused_finalize_x_case(moe, fmt, M):
+    E, K, N, k = 8, 512, 512, 2
     p1, s1, p2, s2, x, ids = _random_mx_problem(E, K, N, M, k, seed=77)
     if fmt == moe.MOE_WEIGHTS_BF16:
         g = torch.Generator().manual_seed(78)
