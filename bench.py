@@ -383,6 +383,18 @@ def timed_sweep(moe, cfg, layer, sweep, forward, steps, stream, pk, world=1, clo
     return secs, per_m, gemm_flops, gemm_secs, clk
 
 
+def experts_step_desc(moe, cfg, layer, M):
+    """What the dominant launch is for this layer at batch M (its launch count
+    from the library's plan)."""
+    if layer.fmt in (moe.MOE_WEIGHTS_MXFP4_A8, moe.MOE_WEIGHTS_MXFP4_A16):
+        act = "bf16 activations as two E4M3 terms" if layer.fmt == moe.MOE_WEIGHTS_MXFP4_A16 else "MXFP8 activations"
+        return (f"the experts step at the largest M on the block-scaled MMAs ({act}): the activation quantiser, "
+                "GEMM1 + activation and GEMM2 with the folded finalize, three launches")
+    n = moe.moe_experts_launches(layer.cw, M, cfg.top_k, True)
+    return (f"the experts step at the largest M: grouped GEMM1 + silu_and_mul and GEMM2 with the "
+            f"folded finalize, {'one fused launch' if n == 1 else f'{n} launches'}")
+
+
 def roofline_objects(per_m, pk, traffic=None, mult=1.0, kernel=None):
     """The roofline report of one config's sweep, each regime against its own
     peak (burst figures: every per-M call is timed alone):
@@ -673,9 +685,7 @@ def run_gpu(args):
                 traffic, tcase, talg = t.get("bytes_per_launch"), t.get("case"), t.get("algorithmic_bytes")
         except Exception:
             traffic = None
-    objs = roofline_objects(per_m, pk, traffic=traffic,
-                            kernel=("the experts step at the largest M: grouped GEMM1 + silu_and_mul and GEMM2 "
-                                    "with the folded finalize (and its out-init); two CTA-pair launches here"))
+    objs = roofline_objects(per_m, pk, traffic=traffic, kernel=experts_step_desc(moe, cfg, layer, big_m))
     roof = dict(objs["dominant"])
     roof.update(traffic_case=tcase, traffic_algorithmic=talg)
 
