@@ -227,16 +227,35 @@ def make_forward(moe, cfg, layer, batches, stream, finalize="fused"):
         # the folded finalize on the block-scaled formats gathers the rows in
         # the experts (moe_experts_fused_finalize_x): the permute copies none
         gx = finalize == "fused" and layer.gathers_in_experts(M)
+        side = finalize == "fused" and layer.overlap_shared
+        if side:
+            # the shared expert on a second stream writes out's start (f32)
+            # beside the router, the permute and the routed experts' first launches
+            if layer._side is None:
+                layer._side = (torch.cuda.Stream(device=x.device), torch.cuda.Event(), torch.cuda.Event())
+            sstream, ev_in, ev_sh = layer._side
+            ev_in.record(torch.cuda.current_stream())
+            sstream.wait_event(ev_in)
+            moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.out, moe.MOE_DTYPE_F32,
+                                  b.shared_ws, b.shared_ws.numel(), sstream)
+            ev_sh.record(sstream)
         moe.moe_route_permute(logits, M, cfg.E, cfg.top_k, layer.method, layer.score_bias, layer.n_group,
                               layer.topk_group, rsf_r, b.topk_ids, b.topk_weights, layer.weights_dtype, None,
                               cfg.E, x, cfg.K, b.offsets, b.pmap, b.inverse, None if gx else b.x_perm, b.perm_ws,
                               b.perm_ws.numel())
-        if layer.ws1 is not None:
+        if layer.ws1 is not None and not side:
             moe.moe_shared_expert(layer.ws1, layer.ws2, cfg.K, layer.Ns, x, M, b.shared, layer.gemm2_dtype,
                                   b.shared_ws, b.shared_ws.numel())
         rsf = 1.0 if layer.method == moe.MOE_ROUTE_SIGMOID_GROUPED_TOPK else layer.rsf
         if ev is not None:
             ev[0].record(stream)
+        if side:
+            moe.moe_experts_fused_finalize_after(layer.cw, x if gx else b.x_perm, 1 if gx else 0, b.offsets, M,
+                                                 cfg.top_k, b.topk_weights, layer.weights_dtype, b.inverse, rsf,
+                                                 b.out, ev_sh, b.exp_ws, b.exp_ws.numel())
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if finalize == "fused" and gx:
             moe.moe_experts_fused_finalize_x(layer.cw, x, b.offsets, M, cfg.top_k, b.topk_weights,
                                              layer.weights_dtype, b.inverse, b.shared, layer.gemm2_dtype, rsf,

@@ -453,6 +453,44 @@ moe_status moe_experts_fused_finalize_x(const moe_weights* w, const void* x, con
                                         moe_dtype shared_dtype, float routed_scaling_factor, float* out,
                                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_experts_fused_finalize_after -- the routed experts with the finalize
+ * folded in, added into an output that already holds its start.
+ * (moe_output.py, MoEOutput: the shared-expert output plus the routed sum;
+ * modular_kernel.py, FusedMoEModularKernel.forward: the shared experts run
+ * beside the routed ones.) The shared expert can then run on another stream
+ * at the same time as the router, the permute and the routed experts' first
+ * launches: moe_shared_expert with shared_out = out (shared_dtype F32) writes
+ * the start, an event recorded after it is out_ready, and this call waits for
+ * that event only before its first launch that adds into out.
+ *
+ *   x, x_order       x_order = 0: x is x_perm [M*top_k, K], as in
+ *                    moe_experts_fused_finalize (workspace:
+ *                    moe_experts_workspace_size); x_order = 1: x is in token
+ *                    order [M, K], as in moe_experts_fused_finalize_x
+ *                    (workspace: moe_experts_x_workspace_size).
+ *   out              f32 [M, K]: holds the output start when the wait ends;
+ *                    out[t] += rsf * sum over t's routes of w * y.
+ *   out_ready        an event (recorded on the stream that writes the start),
+ *                    or NULL when the start is already ordered before this
+ *                    call on `stream`. It is waited for on `stream`, as with
+ *                    cudaStreamWaitEvent; the event itself is not changed.
+ *   the rest         as in moe_experts_fused_finalize (no shared_out: the
+ *                    start is out's own content).
+ *
+ * Results equal moe_experts_fused_finalize's with shared_out = the start (f32),
+ * up to the order of the f32 additions. The launches before the wait (the
+ * activation quantiser and GEMM1 where the plan has them) neither read nor
+ * write out. Returns MOE_ERR_INVALID_ARG for x_order outside {0, 1} or when
+ * out aliases x or expert_weights.
+ * ---------------------------------------------------------------------- */
+moe_status moe_experts_fused_finalize_after(const moe_weights* w, const void* x, int x_order,
+                                            const int32_t* expert_offsets, int M, int top_k,
+                                            const void* expert_weights, moe_dtype weights_dtype,
+                                            const int32_t* permuted_to_expanded, float routed_scaling_factor,
+                                            float* out, cudaEvent_t out_ready, void* workspace,
+                                            size_t workspace_bytes, cudaStream_t stream);
+
 /* The number of kernels that moe_experts_fused_finalize (fused_finalize = 1,
  * counting the initialisation of out) or moe_experts with do_finalize = 0
  * (fused_finalize = 0) launches for this batch size, from the same launch plan

@@ -41,6 +41,7 @@ EXPORTS = (
     "moe_experts", "moe_experts_fused_finalize", "moe_experts_launches", "moe_finalize",
     "moe_experts_chunked_workspace_size", "moe_experts_chunked", "moe_experts_x_workspace_size",
     "moe_experts_fused_finalize_x",
+    "moe_experts_fused_finalize_after",
     "moe_finalize_add_rmsnorm", "moe_experts_batched_workspace_size", "moe_experts_batched", "moe_shared_expert_workspace_size",
     "moe_shared_expert",
     "moe_status_string", "moe_get_error", "moe_device_check", "moe_set_plan_override",
@@ -96,6 +97,8 @@ _SIGS = {
     "moe_experts_x_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I], _Z),
     "moe_experts_fused_finalize_x": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _P, _I, _P, _P, _I, _F, _P,
                                       _P, _Z, _P], _I),
+    "moe_experts_fused_finalize_after": ([ctypes.POINTER(moe_weights), _P, _I, _P, _I, _I, _P, _I, _P, _F, _P,
+                                          _P, _P, _Z, _P], _I),
     "moe_experts_chunked_workspace_size": ([ctypes.POINTER(moe_weights), _I, _I, _I], _Z),
     "moe_experts_chunked": ([ctypes.POINTER(moe_weights), _P, _P, _I, _I, _I, _P, _I, _P, _P, _I, _I, _P, _I, _P,
                              _I, _F, _P, _I, _P, _Z, _P], _I),
@@ -242,6 +245,22 @@ def moe_experts_fused_finalize_x(weights: moe_weights, x, expert_offsets, M, top
     _check("moe_experts_fused_finalize_x", lib.moe_experts_fused_finalize_x(
         ctypes.byref(weights), _ptr(x), _ptr(expert_offsets), M, top_k, _ptr(expert_weights), weights_dtype,
         _ptr(permuted_to_expanded), _ptr(shared_out), shared_dtype, routed_scaling_factor, _ptr(out),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def _event(e):
+    """A torch.cuda.Event (recorded), a raw cudaEvent_t as int, or None."""
+    if e is None or isinstance(e, int):
+        return e
+    return e.cuda_event
+
+
+def moe_experts_fused_finalize_after(weights: moe_weights, x, x_order, expert_offsets, M, top_k, expert_weights,
+                                     weights_dtype, permuted_to_expanded, routed_scaling_factor, out, out_ready,
+                                     workspace, workspace_bytes, stream=None):
+    _check("moe_experts_fused_finalize_after", lib.moe_experts_fused_finalize_after(
+        ctypes.byref(weights), _ptr(x), int(x_order), _ptr(expert_offsets), M, top_k, _ptr(expert_weights),
+        weights_dtype, _ptr(permuted_to_expanded), routed_scaling_factor, _ptr(out), _event(out_ready),
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 

@@ -144,10 +144,17 @@ constexpr size_t kCounterBytes = (4 * static_cast<size_t>(kMaxSplitTiles) + 64) 
 // A finalizing call's output start, written by its GEMM1 launch: out = the
 // shared expert's output, or 0.
 void set_out_init(GemmArgs& a, const ExpertsProblem& p) {
+    if (p.out_preset) return;                          // the caller wrote the start
     a.init_out = p.fin_out;
     a.init_src = p.fin_shared;
     a.init_src_dtype = p.fin_shared_dtype;
     a.init_n = static_cast<long long>(p.M) * p.w->K;
+}
+
+// Before the first launch that adds into a preset output start: wait for
+// the event after which the start is written (another stream's work).
+cudaError_t wait_out_ready(const ExpertsProblem& p, cudaStream_t s) {
+    return (p.fin_out != nullptr && p.out_ready != nullptr) ? cudaStreamWaitEvent(s, p.out_ready, 0) : cudaSuccess;
 }
 
 struct Layout {
@@ -369,6 +376,7 @@ cudaError_t launch_experts_a8(const ExpertsProblem& p, const Layout& L, uint8_t*
     auto gemm_launch = hl ? gemm::launch_gemm_mx8_hl : gemm::launch_gemm_mx8;
     e = gemm_launch(gemm::MODE_SWIGLU, rb * L.bt, MOE_DTYPE_BF16, tA1, tB1, m1, grid, s);
     if (e != cudaSuccess) return e;
+    if ((e = wait_out_ready(p, s)) != cudaSuccess) return e;
     return gemm_launch(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, rb * L.bt, p.y_dtype, tA2, tB2, m2, grid, s);
 }
 
@@ -540,11 +548,14 @@ cudaError_t launch_experts(const ExpertsProblem& p_in, void* workspace, size_t /
         const int pairs = dev.sm_count / 2;
         cudaError_t e = gemm::launch_gemm_pair_bf16(gemm::MODE_SWIGLU, L.bt, MOE_DTYPE_BF16, pa1, pb1, a1, pairs, s);
         if (e != cudaSuccess) return e;
+        if ((e = wait_out_ready(p, s)) != cudaSuccess) return e;
         return gemm::launch_gemm_pair_bf16(fin ? gemm::MODE_FINAL : gemm::MODE_PLAIN, L.bt, p.y_dtype, pa2, pb2, a2,
                                            pairs, s);
     }
     if (L.fused) {
         ka.nphase = 2;
+        const cudaError_t ew = wait_out_ready(p, s);
+        if (ew != cudaSuccess) return ew;
         if (fin) return mx ? gemm::launch_gemm_final_mxfp4(1, L.bt, 2, m, ka, grid, s)
                            : gemm::launch_gemm_final_bf16(1, L.bt, 2, m, ka, grid, s);
         return launch_one(mx, 1, gemm::MODE_PLAIN, L.bt, 2, p.y_dtype, m, ka, grid, s);
@@ -559,6 +570,7 @@ cudaError_t launch_experts(const ExpertsProblem& p_in, void* workspace, size_t /
     m2.A[0] = m.A[1];
     m2.S[0] = m.S[1];
     m2.B[0] = m.B[1];
+    if ((e = wait_out_ready(p, s)) != cudaSuccess) return e;
     if (fin) return mx ? gemm::launch_gemm_final_mxfp4(0, L.bt, L.g2.na, m2, k2, grid, s)
                        : gemm::launch_gemm_final_bf16(0, L.bt, L.g2.na, m2, k2, grid, s);
     return launch_one(mx, 0, gemm::MODE_PLAIN, L.bt, L.g2.na, p.y_dtype, m2, k2, grid, s);

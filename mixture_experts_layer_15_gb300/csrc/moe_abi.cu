@@ -705,6 +705,54 @@ moe_status moe_experts_fused_finalize_x(const moe_weights* w, const void* x, con
     return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
 }
 
+moe_status moe_experts_fused_finalize_after(const moe_weights* w, const void* x, int x_order,
+                                            const int32_t* expert_offsets, int M, int top_k,
+                                            const void* expert_weights, moe_dtype weights_dtype,
+                                            const int32_t* permuted_to_expanded, float routed_scaling_factor,
+                                            float* out, cudaEvent_t out_ready, void* workspace,
+                                            size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0) return MOE_ERR_INVALID_ARG;
+    if (top_k <= 0) return MOE_ERR_INVALID_ARG;
+    if (x_order != 0 && x_order != 1) return MOE_ERR_INVALID_ARG;
+    const moe_status ws_ok = check_weights(w);
+    if (ws_ok != MOE_OK) return ws_ok;
+    if (static_cast<long long>(M) * top_k >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    const moe_status a = check_finalize_args(expert_weights, weights_dtype, permuted_to_expanded, nullptr,
+                                             MOE_DTYPE_F32, out, MOE_DTYPE_F32);
+    if (a != MOE_OK) return a;
+    if (static_cast<const void*>(out) == expert_weights || static_cast<const void*>(out) == x)
+        return MOE_ERR_INVALID_ARG;
+    if (M == 0) return MOE_OK;
+    if (x == nullptr || expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x)) return MOE_ERR_ALIGNMENT;
+    DeviceInfo info;
+    int* err = nullptr;
+    const moe_status st = device_gate(&info, &err);
+    if (st != MOE_OK) return st;
+    const int rows = M * top_k;
+    const size_t need = moe::experts_workspace_bytes(w, rows, M, info, false, x_order == 1);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    moe::ExpertsProblem p;
+    p.w = w;
+    p.x = x;
+    p.x_tokens = x_order == 1;
+    p.rows_alloc = rows;
+    p.M = M;
+    p.offsets = expert_offsets;
+    p.single_rows = 0;
+    p.y = nullptr;
+    p.y_dtype = MOE_DTYPE_F32;
+    p.fin_out = out;
+    p.inverse = permuted_to_expanded;
+    p.fin_weights = expert_weights;
+    p.fin_weights_dtype = weights_dtype;
+    p.top_k = top_k;
+    p.rsf = routed_scaling_factor;
+    p.out_preset = true;
+    p.out_ready = out_ready;
+    return from_cuda(moe::launch_experts(p, workspace, workspace_bytes, err, info, stream));
+}
+
 int moe_experts_launches(const moe_weights* w, int M, int top_k, int fused_finalize) {
     if (M <= 0 || top_k <= 0 || check_weights(w) != MOE_OK) return 0;
     if (static_cast<long long>(M) * top_k >= (1LL << 30)) return 0;

@@ -111,6 +111,10 @@ struct ExpertsProblem {
     // x given in token order (M rows): permuted row p is x[inverse[p] / top_k]
     // (the block-scaled formats read it so; the others gather into the workspace)
     bool x_tokens = false;
+    // fin_out already holds the output start (nothing is copied into it); the
+    // first launch that adds into it waits for out_ready (if not null) first
+    bool out_preset = false;
+    cudaEvent_t out_ready = nullptr;
 };
 
 // ---- MXFP8 activations (mx8_quant.cu) ----------------------------------------------

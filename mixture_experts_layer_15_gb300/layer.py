@@ -36,6 +36,15 @@ class Buffers:
     shared_ws: Optional[torch.Tensor]
 
 
+def _as_stream(stream):
+    """The torch stream for a stream argument of the binding (None: current)."""
+    if stream is None:
+        return torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return torch.cuda.ExternalStream(stream)
+    return stream
+
+
 class MoELayer:
     """One MoE layer on the current CUDA device.
 
@@ -58,7 +67,7 @@ class MoELayer:
                  routed_scaling_factor=1.0, expert_map=None, E_local=None, ws1=None, ws2=None,
                  weights_dtype=L.MOE_DTYPE_F32, gemm2_dtype=L.MOE_DTYPE_F32,
                  out_dtype=L.MOE_DTYPE_F32, fused_finalize=False, activation="silu", activation_clamp=None,
-                 gather_in_experts=None):
+                 gather_in_experts=None, overlap_shared=None):
         self.K, self.N, self.E, self.top_k = K, N, E, top_k
         self.E_local = E if E_local is None else E_local
         self.w1, self.w2, self.w1_scale, self.w2_scale = w1, w2, w1_scale, w2_scale
@@ -80,6 +89,13 @@ class MoELayer:
         # formats, whose quantiser then reads x directly, for batches past the
         # one-kernel route + permute (M > 64), which copies its rows cheaply
         self.gather_in_experts = gather_in_experts
+        # with the folded finalize the shared expert runs on a second stream
+        # beside the router, the permute and the routed experts' first
+        # launches, writing the output start into out itself
+        # (moe_experts_fused_finalize_after); None: whenever there is one
+        self.overlap_shared = (ws1 is not None and self.fused_finalize) if overlap_shared is None \
+            else bool(overlap_shared) and ws1 is not None and self.fused_finalize
+        self._side = None
         act = {"silu": L.MOE_ACT_SILU, "gelu": L.MOE_ACT_GELU}[activation]
         if fmt in (L.MOE_WEIGHTS_MXFP4_A8, L.MOE_WEIGHTS_MXFP4_A16):
             w1_scale = self._prepare_scales(w1_scale, 2 * N, K)
@@ -150,6 +166,18 @@ class MoELayer:
         # with the row gather folded into the experts the permute copies no rows
         gx = do_finalize and self.fused_finalize and self.gathers_in_experts(M)
         xp = None if gx else b.x_perm
+        side = do_finalize and self.overlap_shared
+        if side:
+            main = _as_stream(stream)
+            if self._side is None:
+                self._side = (torch.cuda.Stream(device=x.device), torch.cuda.Event(), torch.cuda.Event())
+            sstream, ev_in, ev_sh = self._side
+            # the shared expert writes out's start (f32) on the second stream
+            ev_in.record(main)
+            sstream.wait_event(ev_in)
+            L.moe_shared_expert(self.ws1, self.ws2, self.K, self.Ns, x, M, b.out, L.MOE_DTYPE_F32,
+                                b.shared_ws, b.shared_ws.numel(), sstream)
+            ev_sh.record(sstream)
         if topk_ids is None:
             # route and permute (one kernel for small batches)
             rsf = self.rsf if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else 1.0
@@ -162,12 +190,19 @@ class MoELayer:
             ids, wts = topk_ids, topk_weights
             L.moe_permute(ids, M, self.top_k, self.E, self.expert_map, self.E_local, x, self.K, b.offsets,
                           b.pmap, b.inverse, xp, b.perm_ws, b.perm_ws.numel(), stream)
-        if self.ws1 is not None:
+        if self.ws1 is not None and not side:
             L.moe_shared_expert(self.ws1, self.ws2, self.K, self.Ns, x, M, b.shared, self.gemm2_dtype,
                                 b.shared_ws, b.shared_ws.numel(), stream)
         # the sigmoid router folds the routed scale into its weights
         rsf = 1.0 if self.method == L.MOE_ROUTE_SIGMOID_GROUPED_TOPK else self.rsf
         wdt = L.MOE_DTYPE_F32 if wts.dtype == torch.float32 else L.MOE_DTYPE_BF16
+        if side:
+            # routed contributions added into the start, once the second stream
+            # has written it (waited for before the first launch that adds)
+            L.moe_experts_fused_finalize_after(self.cw, x if gx else b.x_perm, 1 if gx else 0, b.offsets, M,
+                                               self.top_k, wts, wdt, b.inverse, rsf, b.out, ev_sh, b.exp_ws,
+                                               b.exp_ws.numel(), main)
+            return b
         if do_finalize and self.fused_finalize:
             if gx:
                 L.moe_experts_fused_finalize_x(self.cw, x, b.offsets, M, self.top_k, wts, wdt, b.inverse, b.shared,

@@ -235,3 +235,26 @@ def test_fused_finalize_x_validates_on_the_host(moe):
     assert call(bf, P + 8, M, k, P + 4096) == moe.MOE_ERR_ALIGNMENT
     assert call(bf, P, M, k, P) == moe.MOE_ERR_INVALID_ARG                      # out may not alias x
     assert call(bf, P, 0, k, P + 4096) == 0                                     # nothing to do
+
+
+def test_fused_finalize_after_validates_on_the_host(moe):
+    """The preset-start experts entry: x_order picks x_perm (0) or token
+    order (1); its argument rules fail before any device is touched, and an
+    empty batch is a no-op whatever the event."""
+    P = 0x1000
+    F = moe.MOE_DTYPE_F32
+    bf = moe.make_weights(0, 8, 4096, 1024, P, P)
+    M, k = 512, 2
+    call = lambda x, order, M, k, wts, out: _status(moe.moe_experts_fused_finalize_after, bf, x, order, P, M, k,
+                                                    wts, F, P, 1.0, out, None, P, 1 << 30)
+    assert call(P, 2, M, k, P, P + 4096) == moe.MOE_ERR_INVALID_ARG             # x_order 0 or 1
+    assert call(P, -1, M, k, P, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(P, 0, -1, k, P, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(P, 1, M, 0, P, P + 4096) == moe.MOE_ERR_INVALID_ARG
+    assert call(P, 0, M, k, None, P + 4096) == moe.MOE_ERR_INVALID_ARG          # routing weights required
+    assert call(P, 0, M, k, P, None) == moe.MOE_ERR_INVALID_ARG                 # out required
+    assert call(P, 1, M, k, P, P + 8) == moe.MOE_ERR_ALIGNMENT
+    assert call(P, 0, M, k, P, P) == moe.MOE_ERR_INVALID_ARG                    # out may not alias x
+    assert call(None, 1, M, k, P, P + 4096) == moe.MOE_ERR_INVALID_ARG          # x required
+    assert call(P + 8, 1, M, k, P, P + 4096) == moe.MOE_ERR_ALIGNMENT
+    assert call(P, 0, 0, k, P, P + 4096) == 0                                   # nothing to do

@@ -283,3 +283,71 @@ def _fused_finalize_x_case(moe, fmt, M):
     assert moe.moe_get_error() == moe.MOE_ERR_DEVICE_INDEX
     assert moe.moe_get_error() == 0
     assert torch.isfinite(got).all()
+
+
+_AFTER_PLANS = {"auto": None, "two": (0, 0, 0, 0, 2), "pairs": (128, 0, 0, 0, 3), "fused": (0, 0, 0, 0, 1)}
+
+
+@pytest.mark.parametrize("plan", list(_AFTER_PLANS))
+@pytest.mark.parametrize("x_order", [0, 1])
+@pytest.mark.parametrize("fmt_name", ["MOE_WEIGHTS_MXFP4_A16", "MOE_WEIGHTS_MXFP4_A8", "MOE_WEIGHTS_MXFP4",
+                                      "MOE_WEIGHTS_BF16"])
+def test_fused_finalize_after_adds_into_a_preset_start(moe, fmt_name, x_order, plan):
+    """moe_experts_fused_finalize_after: out holds a start written on a
+    second stream after a long wait there (the event is what orders it),
+    and the routed sum is added into it. Equal to moe_experts_fused_finalize
+    with shared_out = the start (f32) up to the order of the f32 additions
+    (1e-5 * RMS), for x_perm (x_order 0) and token order (1), on every weight
+    format and, for bf16, on each plan (one fused launch, two launches, CTA
+    pairs: the wait sits before a different launch in each). A NULL event
+    with the start written on the same stream gives the same."""
+    fmt = getattr(moe, fmt_name)
+    override = _AFTER_PLANS[plan]
+    if plan != "auto" and fmt != moe.MOE_WEIGHTS_BF16:
+        pytest.skip("plan overrides are exercised on bf16 weights")
+    E, K, N, M, k = 8, 512, 512, 300, 2
+    p1, s1, p2, s2, x, ids = _random_mx_problem(E, K, N, M, k, seed=91)
+    if fmt == moe.MOE_WEIGHTS_BF16:
+        g = torch.Generator().manual_seed(92)
+        p1 = (torch.randn(E, 2 * N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+        p2 = (torch.randn(E, K, N, generator=g) / N ** 0.5).to(torch.bfloat16)
+        d = dict(p1=p1.to(DEV), p2=p2.to(DEV))
+        cw = moe.make_weights(fmt, E, K, N, d["p1"], d["p2"])
+    else:
+        cw, d = _weights(moe, fmt, p1, s1, p2, s2, E, K, N)
+    offs, pmap, inv, _ = O.permute(ids, E)
+    xp = x[torch.from_numpy(inv.astype(np.int64) // k)]
+    w = np.random.default_rng(93).uniform(0.1, 1.0, (M, k)).astype(np.float32)
+    start = (torch.randn(M, K, generator=torch.Generator().manual_seed(94)) * 0.7).to(DEV)
+    offs_d = torch.from_numpy(offs).to(DEV)
+    inv_d = torch.from_numpy(inv.astype(np.int32)).to(DEV)
+    w_d = torch.from_numpy(w).to(DEV)
+    xin = (x if x_order else xp).to(DEV)
+    if override is not None:
+        moe.moe_set_plan_override(*override)
+    try:
+        n = max(moe.moe_experts_workspace_size(cw, M, k), moe.moe_experts_x_workspace_size(cw, M, k))
+        ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+        ref = torch.empty(M, K, dtype=torch.float32, device=DEV)
+        moe.moe_experts_fused_finalize(cw, xp.to(DEV), offs_d, M, k, w_d, F32, inv_d, start, F32, 1.5, ref, ws, n)
+        torch.cuda.synchronize()
+        # the start, written on a second stream after a long wait there
+        got = torch.full((M, K), float("nan"), device=DEV)
+        side, ev = torch.cuda.Stream(), torch.cuda.Event()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(20_000_000)
+            got.copy_(start)
+        ev.record(side)
+        moe.moe_experts_fused_finalize_after(cw, xin, x_order, offs_d, M, k, w_d, F32, inv_d, 1.5, got, ev, ws, n)
+        # the start on the same stream, no event
+        got2 = start.clone()
+        moe.moe_experts_fused_finalize_after(cw, xin, x_order, offs_d, M, k, w_d, F32, inv_d, 1.5, got2, None,
+                                             ws, n)
+        torch.cuda.synchronize()
+        _check_no_error(moe)
+    finally:
+        moe.moe_set_plan_override(0, 0, 0, 0, 0)
+    rms = float(ref.pow(2).mean().sqrt())
+    assert float((got - ref).abs().max()) <= 1e-5 * rms
+    assert float((got2 - ref).abs().max()) <= 1e-5 * rms
