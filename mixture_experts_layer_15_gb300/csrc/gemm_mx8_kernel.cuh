@@ -66,7 +66,9 @@ struct Cfg8 {
     static constexpr int OFF_SF = 2 * A_BYTES + B_BYTES;   // three atoms: A0, A1, B
     static constexpr int STAGE_BYTES = (OFF_SF + 3 * kAtom + 1023) / 1024 * 1024;
     static constexpr int STAGE_TX = 2 * A_TX + B_BYTES + 3 * kAtom;
-    static constexpr int STAGES_FIT = (kSmemBudget - 20 * 1024) / STAGE_BYTES;
+    // the ring takes what the 227 KB a CTA may have leaves beside the rest of
+    // the layout below (barriers, group tables, route table, alignment: < 16 KB)
+    static constexpr int STAGES_FIT = (227 * 1024 - 16 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SF_COLS = 16;                     // TMEM scale columns per stage (8 per issuer)
     static constexpr int ACC_COLS = 2 * BT;
