@@ -166,7 +166,8 @@ def make_workload(cfg_name, device, only_m=None, experts=0, mxfp8_act=False, mxf
                          w1_scale=li.w1_scale, w2_scale=li.w2_scale, fmt=fmt,
                          route="softmax" if cfg.route == "softmax" else "sigmoid",
                          score_bias=li.score_bias, n_group=cfg.n_group, topk_group=cfg.topk_group,
-                         routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2)
+                         routed_scaling_factor=cfg.routed_scaling_factor, ws1=li.ws1, ws2=li.ws2,
+                         fused_finalize=True)
     sweep = cfg.m_sweep if not only_m else tuple(only_m)
     batches = {M: synth.make_tokens(cfg, M, device, li) for M in sweep}
     return cfg, li, layer, batches
