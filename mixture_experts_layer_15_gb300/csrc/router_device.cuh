@@ -150,12 +150,21 @@ __device__ __forceinline__ void route_token_sigmoid(const float* __restrict__ ro
                                                     int E, int top_k, int n_group, int topk_group, float rsf,
                                                     int lane, float* b_row, int& out_id, float& out_w) {
     float key[SLOTS], sc[SLOTS];
+    // every load first (one memory round trip for the token, not one per slot:
+    // the sigmoid's branches would otherwise keep the later loads behind it)
+    float lg[SLOTS], bs[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int id = lane + 32 * s;
+        lg[s] = id < E ? __ldg(row + id) : 0.0f;
+        bs[s] = id < E ? __ldg(bias + id) : 0.0f;
+    }
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
         const int id = lane + 32 * s;
         if (id < E) {
-            sc[s] = sigmoid_spec(row[id]);
-            key[s] = __fadd_rn(sc[s], bias[id]);
+            sc[s] = sigmoid_spec(lg[s]);
+            key[s] = __fadd_rn(sc[s], bs[s]);
             b_row[id] = key[s];
         } else {
             sc[s] = 0.0f;
