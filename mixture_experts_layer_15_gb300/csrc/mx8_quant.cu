@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kQThreads)
 mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint8_t* __restrict__ codes,
                       uint8_t* __restrict__ scales, const int32_t* __restrict__ offsets, int groups, int bt,
                       int rows_alloc, int max_tiles, int* err, const int32_t* __restrict__ gather_inv,
-                      int gather_topk) {
+                      int gather_topk, int cpi) {
     __shared__ int s_offs[gemm::kMaxGroups + 1];
     __shared__ int s_ttp[gemm::kMaxGroups + 1];
     __shared__ int tmp[36];
@@ -71,16 +71,17 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
     }
     const int nkb = C / gemm::kMxBK;
     const int nw = kQThreads / 32;
-    // one warp per (row, group of four 256-column chunks): a row's groups go to
-    // different warps, so a few rows still spread over many warps, and a warp
-    // has the loads of its four chunks in flight at once
+    // one warp per (row, group of cpi 256-column chunks): a row's groups go to
+    // different warps, so a few rows still spread over many warps, and with
+    // cpi = 4 a warp has the loads of its four chunks in flight at once
+    // (cpi = 1 when the rows are too few to fill the GPU that way)
     const int chunks = (C + 255) / 256;
-    const int groups4 = (chunks + 3) / 4;
-    const long long items = static_cast<long long>(R > p0 ? R - p0 : 0) * groups4;
+    const int ngr = (chunks + cpi - 1) / cpi;
+    const long long items = static_cast<long long>(R > p0 ? R - p0 : 0) * ngr;
     for (long long it = static_cast<long long>(blockIdx.x) * nw + warp; it < items;
          it += static_cast<long long>(gridDim.x) * nw) {
-        const int p = p0 + static_cast<int>(it / groups4);
-        const int cbase = static_cast<int>(it % groups4) * 1024;
+        const int p = p0 + static_cast<int>(it / ngr);
+        const int cbase = static_cast<int>(it % ngr) * 256 * cpi;
         int T = 0, n = 0;
         if (ATOM) {
             int lo = 0, hi = groups;                       // s_offs[lo] <= p < s_offs[hi]
@@ -110,7 +111,7 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = cbase + 256 * j + lane * 8;
-            if (c < C && !zero) {
+            if (j < cpi && c < C && !zero) {
                 Vec8<__nv_bfloat16>::load(xr + c, vv[j]);
             } else {
 #pragma unroll
@@ -119,7 +120,7 @@ mxfp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, int rows, int C, uint
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if (cbase + 256 * j >= C) break;               // uniform over the warp
+            if (j >= cpi || cbase + 256 * j >= C) break;   // uniform over the warp
             const int c = cbase + 256 * j + lane * 8;
             const bool on = c < C;
             const float (&v)[8] = vv[j];
@@ -219,8 +220,17 @@ __global__ void mx_prepare_scales_kernel(const uint8_t* __restrict__ sc, long lo
 namespace {
 // CTAs for rows x groups of four 256-column chunks, one warp per item, at
 // most 8 per SM.
+// Chunks per work item: 4, unless the rows give fewer items of four chunks
+// than one CTA's warps per SM (then 1: four times the warps, each a quarter
+// of the dependent work).
+int quantize_cpi(int rows, int C, const DeviceInfo& dev) {
+    const long long items4 = static_cast<long long>(rows) * ((C + 1023) / 1024);
+    return items4 < static_cast<long long>(kQThreads / 32) * (dev.sm_count > 0 ? dev.sm_count : 152) ? 1 : 4;
+}
+
 int quantize_grid(int rows, int C, const DeviceInfo& dev) {
-    const long long items = static_cast<long long>(rows) * ((C + 1023) / 1024);
+    const int cpi = quantize_cpi(rows, C, dev);
+    const long long items = static_cast<long long>(rows) * ((C + 256 * cpi - 1) / (256 * cpi));
     const int nw = kQThreads / 32;
     long long grid = (items + nw - 1) / nw;
     const long long cap = 8LL * (dev.sm_count > 0 ? dev.sm_count : 152);
@@ -236,7 +246,7 @@ cudaError_t launch_mxfp8_quantize(const void* x, int rows, int C, uint8_t* codes
     return launch_pdl(mxfp8_quantize_kernel<false, false>, dim3(grid), dim3(kQThreads), 0, s,
                       static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
                       static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err, static_cast<const int32_t*>(nullptr),
-                      1);
+                      1, quantize_cpi(rows, C, dev));
 }
 
 cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, uint8_t* scales, int* err,
@@ -246,7 +256,7 @@ cudaError_t launch_e4m3_split(const void* x, int rows, int C, uint8_t* codes, ui
     return launch_pdl(mxfp8_quantize_kernel<false, true>, dim3(grid), dim3(kQThreads), 0, s,
                       static_cast<const __nv_bfloat16*>(x), rows, C, codes, scales,
                       static_cast<const int32_t*>(nullptr), 0, 1, rows, 0, err, static_cast<const int32_t*>(nullptr),
-                      1);
+                      1, quantize_cpi(rows, C, dev));
 }
 
 cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, const int32_t* offsets, int groups,
@@ -257,7 +267,7 @@ cudaError_t launch_mxfp8_quantize_tiles(const void* x, int rows_alloc, int C, co
     auto kern = hl ? mxfp8_quantize_kernel<true, true> : mxfp8_quantize_kernel<true, false>;
     return launch_pdl(kern, dim3(grid), dim3(kQThreads), 0, s, static_cast<const __nv_bfloat16*>(x), rows_alloc, C,
                       codes, atoms, offsets, groups, bt, rows_alloc, max_tiles, err, gather_inv,
-                      gather_topk > 0 ? gather_topk : 1);
+                      gather_topk > 0 ? gather_topk : 1, quantize_cpi(rows_alloc, C, dev));
 }
 
 cudaError_t launch_mx_prepare_scales(const uint8_t* scales, long long rows_total, int cols, uint8_t* out,
