@@ -59,7 +59,11 @@ class MoELayer:
     the scales once (moe_mx_prepare_scales) and the experts run with MXFP8
     activations on the block-scaled tensor cores. MOE_WEIGHTS_MXFP4_A16 takes
     the same weights and keeps bf16 activations (W4A16), each split into two
-    E4M3 terms for the block-scaled tensor cores.
+    E4M3 terms for the block-scaled tensor cores. With a shared expert and
+    ``fused_finalize``, ``overlap_shared`` (the default then) runs the shared
+    expert on a second stream, writing its output straight into ``out`` as the
+    start that the routed experts add into (moe_experts_fused_finalize_after);
+    the buffers' ``shared`` tensor is then not written.
     """
 
     def __init__(self, *, K, N, E, top_k, w1, w2, w1_scale=None, w2_scale=None,
