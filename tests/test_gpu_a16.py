@@ -351,3 +351,30 @@ def test_fused_finalize_after_adds_into_a_preset_start(moe, fmt_name, x_order, p
     rms = float(ref.pow(2).mean().sqrt())
     assert float((got - ref).abs().max()) <= 1e-5 * rms
     assert float((got2 - ref).abs().max()) <= 1e-5 * rms
+
+
+@pytest.mark.parametrize("M", [1, 64, 1024])
+def test_layer_shared_expert_overlap_equals_serial(moe, M):
+    """The DeepSeek-shaped layer (A16 routed experts, bf16 shared expert)
+    with the shared expert on a second stream writing the output start
+    (MoELayer's default with the folded finalize) equals the same layer with
+    the shared expert first on the one stream, up to the order of the f32
+    additions (1e-5 * RMS); routing and map are the same bits."""
+    import synth
+    cfg = synth.CONFIGS["deepseek"]
+    li = layer_inputs("deepseek")
+    x, logits = synth.make_tokens(cfg, M, DEV, li)
+    res = []
+    for ov in (True, False):
+        lay = make_layer(moe, "deepseek", li, fmt=moe.MOE_WEIGHTS_MXFP4_A16, fused_finalize=True,
+                         overlap_shared=ov)
+        assert lay.overlap_shared == ov
+        b = lay.forward(x, logits)
+        res.append((b.out.clone(), b.topk_ids.clone(), b.pmap.clone()))
+        del lay
+    torch.cuda.synchronize()
+    _check_no_error(moe)
+    (o1, i1, p1), (o2, i2, p2) = res
+    assert torch.equal(i1, i2) and torch.equal(p1, p2)
+    rms = float(o2.pow(2).mean().sqrt())
+    assert float((o1 - o2).abs().max()) <= 1e-5 * rms
